@@ -1,0 +1,450 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 SDPA forward (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload caseD] [--quick]
+
+A step is one full forward pass (every stage of the path: QK^T, mask, online softmax,
+PV, normalisation, O and LSE stores) over one batch of synthetic inputs of the chosen
+workload (default caseD: B=8 H=32 L=512 d=128 causal, the largest head_dim-128 causal
+case of "An Optimal Mapper Meets a Real GPU", "Experiment one").
+
+Timing (ours): the K steps are captured in a CUDA graph and replayed, so the number is
+device time, not Python launch overhead.  Consecutive steps cycle through R copies of
+the inputs and outputs whose total is more than twice the L2 size, so every step reads
+its Q, K, V from HBM (no L2 flush needed).  W warm-up steps run first.  A barrier and a
+device synchronise bracket the timed region on every rank; the maximum over ranks is
+used and rank 0 prints the line.  `value` is TFLOPS with causal FLOPs counted as half.
+
+`e2e` is the same metric through the public API with host buffers: per step, the H2D
+copy of Q, K, V from pinned host memory, the forward call, and the D2H copy of O and
+LSE into pinned host memory, all inside the timed region.
+
+`cpu_baseline` (rank 0, N=1 only) times the float64 CPU oracle (test infrastructure) on
+the same workload on the host cores; `--impl reference` times that oracle as the
+reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOPS (causal-halved) and % of GB300 FP16 tensor peak; µs/call"
+L2_BYTES = 126.5 * 2 ** 20
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+def kernel_source_hash() -> str:
+    """Hash of every source the kernels are built from (to tell whether a stored ncu
+    capture still describes the current kernel)."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "scaled_dot_product_sdpa_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".inc")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload: str):
+    """dram read+write bytes per launch from the committed ncu summary of this workload,
+    if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"attn_fwd_kernel_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- ours
+def capture_graph(fn_list, stream, torch):
+    """Capture the launches in fn_list, in order, into one CUDA graph on `stream`."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for fn in fn_list:
+            fn(stream)
+    torch.cuda.synchronize()
+    return g
+
+
+def make_sets(w, n_sets, device, torch, inputs):
+    q, k, v = inputs.qkv(w.B, w.H, w.L, w.d, w.seed, w.sigma)
+    sets = []
+    for _ in range(n_sets):
+        dq, dk, dv = (t.to(device) for t in (q, k, v))
+        o = torch.empty_like(dq)
+        lse = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device=device)
+        sets.append((dq, dk, dv, o, lse))
+    return (q, k, v), sets
+
+
+def n_rotating_sets(w):
+    per = w.bytes()
+    return max(2, math.ceil(2.0 * L2_BYTES / per) + 1)
+
+
+def bench_workload(w, steps, warmup, device, torch, gb, inputs, world):
+    """Device time per forward call of workload w: exactly `steps` launches, replayed
+    from CUDA graphs, cycling through R rotating input/output sets."""
+    R = n_rotating_sets(w)
+    host, sets = make_sets(w, R, device, torch, inputs)
+
+    def launcher(s):
+        return lambda st: gb.attn_fwd(s[0], s[1], s[2], causal=w.causal, scale=w.scale, o=s[3], lse=s[4],
+                                      stream=st)
+
+    per = R * max(1, math.ceil(64 / R))  # launches per main graph, a multiple of R
+    stream = torch.cuda.Stream(device=device)
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):  # first calls (attributes, descriptors) outside capture
+        for i in range(R):
+            launcher(sets[i])(stream)
+    torch.cuda.synchronize()
+    main = capture_graph([launcher(sets[i % R]) for i in range(per)], stream, torch)
+    n_main, n_tail = divmod(steps, per)
+    tail = capture_graph([launcher(sets[i % R]) for i in range(n_tail)], stream, torch) if n_tail else None
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, math.ceil(warmup / per))):
+            main.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(n_main):
+            main.replay()
+        if tail is not None:
+            tail.replay()
+        b.record(stream)
+    b.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    t = a.elapsed_time(b) * 1e-3 / steps
+    return t, steps, R, host, sets, (main, stream, per)
+
+
+def bench_e2e(w, steps, warmup, device, torch, gb, host):
+    """Through the public API with host buffers: H2D(Q,K,V) + forward + D2H(O, LSE)."""
+    q, k, v = (t.pin_memory() for t in host)
+    o_h = torch.empty(q.shape, dtype=torch.float16).pin_memory()
+    l_h = torch.empty((w.B, w.H, w.L), dtype=torch.float32).pin_memory()
+    dq, dk, dv = (torch.empty_like(t, device=device) for t in (q, k, v))
+    o = torch.empty_like(dq)
+    lse = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        dq.copy_(q, non_blocking=True)
+        dk.copy_(k, non_blocking=True)
+        dv.copy_(v, non_blocking=True)
+        gb.attn_fwd(dq, dk, dv, causal=w.causal, scale=w.scale, o=o, lse=lse, stream=stream)
+        o_h.copy_(o, non_blocking=True)
+        l_h.copy_(lse, non_blocking=True)
+
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, min(steps, 200))
+    t0 = time.perf_counter()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    b.synchronize()
+    wall = time.perf_counter() - t0
+    dev = a.elapsed_time(b) * 1e-3
+    t = max(wall, dev) / n
+    h2d = 3 * q.numel() * 2
+    d2h = o_h.numel() * 2 + l_h.numel() * 4
+    return t, h2d, d2h
+
+
+def cpu_oracle_baseline(w, min_seconds=10.0, max_reps=20):
+    """Float64 oracle, as it stands, on the host cores: whole workload, repeated until
+    about `min_seconds` of CPU work (bounded by max_reps)."""
+    import oracle
+    from scaled_dot_product_sdpa_gb300 import inputs
+    q, k, v = inputs.qkv(w.B, w.H, w.L, w.d, w.seed, w.sigma)
+    scale = float(__import__("numpy").float32(w.scale))
+    qf, kf, vf = (oracle._f64(t) for t in (q, k, v))
+    reps, total, cores = 0, 0.0, 0
+    while reps < max_reps and (total < min_seconds or reps == 0):
+        t0 = time.perf_counter()
+        o, lse = oracle.sdpa_fwd(qf, kf, vf, w.causal, scale)
+        total += time.perf_counter() - t0
+        reps += 1
+    nthreads = int(os.environ.get("OMP_NUM_THREADS", "0")) or len(os.sched_getaffinity(0))
+    t = total / reps
+    return t, reps, nthreads
+
+
+def bench_ours(args):
+    import torch
+    import scaled_dot_product_sdpa_gb300 as gb
+    from scaled_dot_product_sdpa_gb300 import inputs
+    from scaled_dot_product_sdpa_gb300.configs import WORKLOADS
+    from scaled_dot_product_sdpa_gb300 import build as gbuild
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    gb.load_library(gbuild.build())
+    peaks, peak_kind = load_peaks()
+    w = WORKLOADS[args.workload]
+
+    sampler = ClockSampler(local) if not args.quick else None
+    if sampler:
+        sampler.start()
+    t, nsteps, R, host, sets, graph = bench_workload(w, args.steps, args.warmup, device, torch, gb, inputs, world)
+    clock_note = "sampled during the timed region"
+    if sampler:
+        clocks = sampler.stop()
+        if clocks.get("samples", 0) < 3:
+            # Timed region too short for 100 ms sampling: sample again over ~1.5 s of the
+            # same graph replays (untimed) and say so.
+            sampler.start()
+            g, stream, per_graph = graph
+            t_end = time.perf_counter() + 1.5
+            while time.perf_counter() < t_end:
+                for _ in range(20):
+                    g.replay()
+                torch.cuda.synchronize()
+            clocks = sampler.stop()
+            clock_note = "timed region shorter than the sampling period; sampled over 1.5 s of the same replays"
+        clocks["note"] = clock_note
+    else:
+        clocks = None
+    status = gb.attn_last_device_error()
+    if status != 0:
+        raise RuntimeError(f"device status {status}: {gb.attn_strerror(status)}")
+    t_max = max_over_ranks(t, world, device)
+    tflops = w.flops() / t_max / 1e12 * world
+    fp16_peak = peaks["bf16_tflops"] * 1.0  # fp16 dense = bf16 dense (nominal ratio 1)
+    hbm_peak = peaks["hbm_gbs"]
+    achieved_gbs = w.bytes() / t_max / 1e9
+    bound = "hbm" if w.flops() / w.bytes() < fp16_peak * 1e12 / (hbm_peak * 1e9) else "tensor"
+    traffic = stored_traffic(w.name)
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved_gbs / hbm_peak, 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(w.flops() / t_max / 1e12, 1), "peak": fp16_peak,
+                "unit": "TFLOP/s", "frac": round(w.flops() / t_max / 1e12 / fp16_peak, 4)}
+    roof["traffic"] = traffic
+    roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
+    roof["algorithmic_bytes_per_launch"] = w.bytes()
+    roof["algorithmic_flops_per_launch"] = w.flops()
+    roof["tensor_frac"] = round(w.flops() / t_max / 1e12 / fp16_peak, 4)
+    roof["hbm_frac"] = round(achieved_gbs / hbm_peak, 4)
+
+    line = {
+        "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOPS", "n_gpus": world, "steps": nsteps,
+        "warmup": args.warmup, "ms_per_step": round(t_max * 1e3, 6), "us_per_call": round(t_max * 1e6, 3),
+        "pct_fp16_peak": round(100 * w.flops() / t_max / 1e12 / fp16_peak, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "accumulate": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "shape": w.describe(), "global_batch": w.B * world,
+                   "seq_len": w.L, "head_dim": w.d, "heads": w.H,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"{R} rotating input/output sets ({R * w.bytes() / 2**20:.0f} MiB > 2x L2); no flush",
+                   "timing": "CUDA graph of the steps, CUDA events on the replay stream"},
+        "gpu_launches": nsteps, "roofline": roof, "clocks": clocks,
+    }
+    if not args.quick:
+        te, h2d, d2h = bench_e2e(w, args.steps, args.warmup, device, torch, gb, host)
+        te = max_over_ranks(te, world, device)
+        line["e2e"] = {"value": round(w.flops() / te / 1e12 * world, 3), "unit": "TFLOPS",
+                       "us_per_call": round(te * 1e6, 2), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        per = {}
+        for name, wk in WORKLOADS.items():
+            tk = bench_workload(wk, 200, 10, device, torch, gb, inputs, world)[0]
+            fl = wk.flops() / tk / 1e12
+            per[name] = {"shape": wk.describe(), "us": round(tk * 1e6, 3), "tflops": round(fl, 1),
+                         "pct_fp16_peak": round(100 * fl / fp16_peak, 2),
+                         "hbm_gbs": round(wk.bytes() / tk / 1e9, 1),
+                         "pct_hbm_peak": round(100 * wk.bytes() / tk / 1e9 / hbm_peak, 2)}
+        line["per_config"] = per
+        status = gb.attn_last_device_error()
+        if status != 0:
+            raise RuntimeError(f"device status {status}: {gb.attn_strerror(status)}")
+        if rank == 0 and world == 1 and not args.no_cpu:
+            tc, reps, cores = cpu_oracle_baseline(w)
+            line["cpu_baseline"] = {"value": round(w.flops() / tc / 1e12, 6), "unit": "TFLOPS", "cores": cores,
+                                    "kind": "oracle", "seconds_per_call": round(tc, 3),
+                                    "sample": f"the whole {w.name} workload, {reps} call(s), float64 C oracle"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- reference
+def bench_reference(args):
+    """The reference arm: the float64 CPU oracle, as it stands, on the host cores."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from scaled_dot_product_sdpa_gb300.configs import WORKLOADS
+    import oracle
+    import numpy as np
+    from scaled_dot_product_sdpa_gb300 import inputs
+    oracle.build()
+    w = WORKLOADS[args.workload]
+    q, k, v = inputs.qkv(w.B, w.H, w.L, w.d, w.seed, w.sigma)
+    qf, kf, vf = (oracle._f64(t) for t in (q, k, v))
+    # Bounded sample: a slice of the heads sized so that one step is ~1-2 s of CPU work.
+    heads = w.B * w.H
+    probe_heads = max(1, heads // 64)
+    t0 = time.perf_counter()
+    oracle.sdpa_fwd(qf.reshape(heads, 1, w.L, w.d)[:probe_heads], kf.reshape(heads, 1, w.L, w.d)[:probe_heads],
+                    vf.reshape(heads, 1, w.L, w.d)[:probe_heads], w.causal, float(np.float32(w.scale)))
+    per_head = (time.perf_counter() - t0) / probe_heads
+    step_budget = min(1.5, 90.0 / (args.steps + args.warmup))  # whole run ~1.5 min at most
+    nh = int(min(heads, max(1, step_budget / max(per_head, 1e-9))))
+    sl = lambda x: np.ascontiguousarray(x.reshape(heads, 1, w.L, w.d)[:nh])
+    qs, ks, vs = sl(qf), sl(kf), sl(vf)
+    for _ in range(args.warmup):
+        oracle.sdpa_fwd(qs, ks, vs, w.causal, float(np.float32(w.scale)))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.sdpa_fwd(qs, ks, vs, w.causal, float(np.float32(w.scale)))
+    dt = (time.perf_counter() - t0) / args.steps
+    flops = w.flops() * nh / heads
+    value = flops / dt / 1e12
+    cores = int(os.environ.get("OMP_NUM_THREADS", "0")) or len(os.sched_getaffinity(0))
+    line = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOPS", "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "shape": w.describe(), "global_batch": w.B, "seq_len": w.L,
+                       "head_dim": w.d, "parallelism": "host cores"},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                             "sample": f"{nh} of {heads} heads of {w.name} per step"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="caseD")
+    ap.add_argument("--quick", action="store_true", help="timed region only (for profiler runs)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,117 @@
+/*
+ * gbattn.h -- C ABI of libgbattn.so: exact scaled-dot-product attention forward on one
+ * GB300 (sm_103a), FP16 inputs, FP32 accumulation, FP16 output plus FP32 row LSE.
+ *
+ * The operation ("An Optimal Mapper Meets a Real GPU", sections "Ground rules" and
+ * "Experiment one", Cases table; STAGE_D.md of nvfp4-megamoe-kernel, sections 2, 4
+ * and 6):
+ *     O[b,h,i,:] = sum_j softmax_j(scale * q_i . k_j + mask_ij) * v[b,h,j,:]
+ *     LSE[b,h,i] = log sum_j exp(scale * q_i . k_j + mask_ij)       (natural log)
+ * with query length = key/value length = L, mask_ij = -inf for j > i when causal, else 0.
+ * The QK reduction over head_dim d is summed in full (in logit space) before the
+ * softmax, also when d is wider than one 256-wide sub-tile.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are contiguous row-major [B, H, L, d] (PyTorch SDPA layout); q, k, v, o
+ *     hold IEEE fp16 values, lse holds fp32 [B, H, L].
+ *   - Every pointer is a DEVICE pointer owned by the caller (for example memory that
+ *     PyTorch allocated).  The library never allocates, frees or retains device memory
+ *     and never synchronises; it caches only TMA descriptors' host-side encodings and
+ *     per-device attributes.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Work is enqueued asynchronously on it; on return the outputs are not yet written.
+ *   - Return value: 0 if the work was enqueued, otherwise one of the negative
+ *     GBATTN_ERR_* codes below; on an error nothing is enqueued and no output is touched.
+ *   - Outputs must not overlap inputs or each other.
+ *   - Not thread-safe for concurrent first calls on a new device (the per-device setup
+ *     is done once); later calls from several host threads are safe.
+ */
+#ifndef GBATTN_H
+#define GBATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GBATTN_OK 0
+#define GBATTN_ERR_NULL (-1)        /* a required pointer is NULL                            */
+#define GBATTN_ERR_DIMS (-2)        /* B, H or L <= 0, or B*H*L*d too large                  */
+#define GBATTN_ERR_HEAD_DIM (-3)    /* d not in {64, 128, 256, 512}                          */
+#define GBATTN_ERR_ALIGN (-4)       /* a pointer is not 16-byte aligned                      */
+#define GBATTN_ERR_LAUNCH (-5)      /* a CUDA call or the kernel launch failed               */
+#define GBATTN_ERR_DEVICE (-6)      /* the current device is not compute capability 10.3     */
+#define GBATTN_ERR_SCALE (-7)       /* scale is not a finite number > 0                      */
+#define GBATTN_ERR_ALIAS (-8)       /* an output overlaps an input or the other output       */
+#define GBATTN_ERR_TENSORMAP (-9)   /* the driver rejected a TMA descriptor                  */
+
+/* Device-side status codes reported by attn_last_device_error() (positive). */
+#define GBATTN_DEV_TIMEOUT_LOAD 1    /* the TMA producer's wait for a free buffer timed out  */
+#define GBATTN_DEV_TIMEOUT_MMA 2     /* the MMA issuer's wait for data or P timed out        */
+#define GBATTN_DEV_TIMEOUT_SOFTMAX 3 /* the softmax warps' wait for S or O timed out         */
+#define GBATTN_DEV_TIMEOUT_EPILOGUE 4 /* the epilogue's wait for its staging tile timed out   */
+#define GBATTN_DEV_TIMEOUT_PROBE 5   /* the self-test wait of attn_debug_wait_probe ran out */
+
+/*
+ * attn_fwd -- the fused forward pass.
+ *   q, k, v : const fp16 [B, H, L, d], device, 16-byte aligned.
+ *   o       : fp16 [B, H, L, d] output, device, 16-byte aligned.
+ *   lse     : fp32 [B, H, L] output (natural-log LSE of the scaled, masked logits).
+ *   B, H, L : > 0.  d : 64, 128, 256 or 512.  causal : 0 or 1 (nonzero = 1).
+ *   scale   : the logit scale (usually 1/sqrt(d)), finite and > 0.
+ * Rounding: O is rounded to fp16 to nearest even; P (the softmax weights) is rounded to
+ * fp16 before the PV product, as the FP16-in/FP32-accumulate convention implies.
+ * A wait inside the kernel that exceeds about two seconds (a fault, never expected)
+ * ends the kernel early with a code readable through attn_last_device_error().
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+             int L, int d, int causal, float scale, void *stream);
+
+/*
+ * attn_fwd_ex -- attn_fwd with design options (same arguments, same errors).
+ *   flags bit 0 (GBATTN_FLAG_P_SMEM): stage P through shared memory instead of tensor
+ *     memory before the PV product (the SMEM-P path of the STAGE_D.md notes, section 4);
+ *     only for d <= 128, otherwise GBATTN_ERR_HEAD_DIM.  Same results up to rounding.
+ *   grid_limit: 0 = one persistent CTA per SM; n > 0 = at most n CTAs (scheduler tests).
+ */
+#define GBATTN_FLAG_P_SMEM 1
+int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                int H, int L, int d, int causal, float scale, void *stream, int flags,
+                int grid_limit);
+
+/*
+ * attn_debug_scores -- test hook: the raw scaled logits s[b,h,i,j] = scale * q_i . k_j
+ * (fp32 [B, H, L, L], no mask), with the head_dim reduction done the same way as in
+ * attn_fwd (tensor-core products accumulated over every 64-wide slice of d before any
+ * read-out).  It exists to check the QK stage alone ("no-softmax mode", STAGE_D.md,
+ * option 2 of the closing list).  Not a production path.
+ */
+int attn_debug_scores(const void *q, const void *k, float *s, int B, int H, int L, int d,
+                      float scale, void *stream);
+
+/*
+ * attn_last_device_error -- read and clear the device status word of the current
+ * device.  Returns 0 if every kernel since the last call finished normally, otherwise
+ * the first GBATTN_DEV_* code recorded.  Synchronises the current device first (it is
+ * a host-blocking call); returns GBATTN_ERR_LAUNCH if that fails.
+ */
+int attn_last_device_error(void);
+
+/*
+ * attn_debug_wait_probe -- self-test of the bounded waits: launches one tiny kernel
+ * that waits on a shared-memory barrier that nothing completes, giving up after
+ * `limit_cycles` SM clock cycles (clamped to [1000, 100000000]) and recording
+ * GBATTN_DEV_TIMEOUT_PROBE.  Lets a test check, without hanging the GPU, that a wait
+ * that runs out turns into a status the host can read.
+ */
+int attn_debug_wait_probe(long long limit_cycles, void *stream);
+
+/* Human-readable text for a GBATTN_ERR_* or GBATTN_DEV_* code (static storage). */
+const char *attn_strerror(int code);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GBATTN_H */

@@ -1,0 +1,12 @@
+"""GB300-native (sm_103a) exact scaled-dot-product attention forward.
+
+O = softmax(scale * Q K^T + causal mask) V with FP16 inputs, FP32 accumulation, FP16 O
+and FP32 row log-sum-exp, computed by one fused persistent CUDA kernel (TMA, tcgen05
+tensor cores, tensor memory) behind the C ABI of include/gbattn.h.  This package is the
+thin Python binding of that library; every step of the computation runs on the GPU.
+"""
+from ._binding import (FLAG_P_SMEM, GbattnError, attn_debug_scores, attn_debug_wait_probe, attn_fwd,
+                       attn_last_device_error, attn_strerror, attn_version, load_library, LIB_PATH)
+
+__all__ = ["attn_fwd", "attn_debug_scores", "attn_debug_wait_probe", "attn_last_device_error",
+           "attn_strerror", "attn_version", "load_library", "GbattnError", "FLAG_P_SMEM", "LIB_PATH"]

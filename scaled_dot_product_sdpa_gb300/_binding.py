@@ -1,0 +1,135 @@
+"""ctypes binding of libgbattn.so: argument marshalling only.
+
+Every function here converts torch tensors to raw device pointers and sizes, calls the
+C entry point of the same name (include/gbattn.h), and turns a nonzero return code into
+a GbattnError.  There is no fallback: if the library is missing or the tensors are not
+on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgbattn.so")
+_lib = None
+
+FLAG_P_SMEM = 1
+
+
+class GbattnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: gbattn error {code}: {attn_strerror(code)}")
+
+
+def load_library(path: str | None = None):
+    """Load libgbattn.so (built by scaled_dot_product_sdpa_gb300.build).  Raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"libgbattn.so not built ({path} missing); run "
+                           "`python -m scaled_dot_product_sdpa_gb300.build` or __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.attn_fwd.restype = i
+    lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, i, i]
+    lib.attn_fwd_ex.restype = i
+    lib.attn_debug_scores.argtypes = [vp, vp, vp, i, i, i, i, f, vp]
+    lib.attn_debug_scores.restype = i
+    lib.attn_last_device_error.argtypes = []
+    lib.attn_last_device_error.restype = i
+    lib.attn_debug_wait_probe.argtypes = [ctypes.c_longlong, vp]
+    lib.attn_debug_wait_probe.restype = i
+    lib.attn_strerror.argtypes = [i]
+    lib.attn_strerror.restype = ctypes.c_char_p
+    lib.attn_version.argtypes = []
+    lib.attn_version.restype = i
+    _lib = lib
+    return lib
+
+
+def attn_strerror(code: int) -> str:
+    return load_library().attn_strerror(int(code)).decode()
+
+
+def attn_version() -> int:
+    return load_library().attn_version()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check_qkv(q, k, v=None):
+    ts = [q, k] + ([v] if v is not None else [])
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("gbattn: tensors must be on a CUDA device (no CPU path exists)")
+        if t.dtype != torch.float16:
+            raise ValueError("gbattn: q, k, v must be float16")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError("gbattn: q, k, v must be contiguous [B, H, L, d]")
+        if t.shape != q.shape:
+            raise ValueError("gbattn: q, k, v must have the same shape")
+    return q.shape
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None, stream=None,
+             flags: int = 0, grid_limit: int = 0):
+    """O, LSE = SDPA forward of fp16 [B, H, L, d] q, k, v.  Outputs are allocated by torch
+    on q's device unless given.  Enqueued on `stream` (default: torch's current stream)."""
+    B, H, L, d = _check_qkv(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    if o.shape != q.shape or o.dtype != torch.float16 or not o.is_contiguous():
+        raise ValueError("gbattn: o must be contiguous float16 like q")
+    if lse.shape != (B, H, L) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("gbattn: lse must be contiguous float32 [B, H, L]")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                             B, H, L, d, int(bool(causal)), float(scale), _stream_handle(stream),
+                             int(flags), int(grid_limit))
+    if rc != 0:
+        raise GbattnError(rc, "attn_fwd")
+    return o, lse
+
+
+def attn_debug_scores(q, k, scale: float | None = None, s=None, stream=None):
+    """Raw scaled logits scale * Q K^T as fp32 [B, H, L, L] (test hook, no mask)."""
+    B, H, L, d = _check_qkv(q, k)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if s is None:
+        s = torch.empty((B, H, L, L), dtype=torch.float32, device=q.device)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_debug_scores(q.data_ptr(), k.data_ptr(), s.data_ptr(), B, H, L, d, float(scale),
+                                   _stream_handle(stream))
+    if rc != 0:
+        raise GbattnError(rc, "attn_debug_scores")
+    return s
+
+
+def attn_last_device_error() -> int:
+    """Synchronise the current device, then read and clear its device status word."""
+    return load_library().attn_last_device_error()
+
+
+def attn_debug_wait_probe(limit_cycles: int, stream=None) -> None:
+    rc = load_library().attn_debug_wait_probe(int(limit_cycles), _stream_handle(stream))
+    if rc != 0:
+        raise GbattnError(rc, "attn_debug_wait_probe")

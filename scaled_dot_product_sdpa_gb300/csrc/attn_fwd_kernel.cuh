@@ -1,0 +1,542 @@
+// attn_fwd_kernel.cuh -- fused, persistent, warp-specialised SDPA forward for sm_103a.
+//
+// What it computes ("An Optimal Mapper Meets a Real GPU", "Ground rules" / "Experiment
+// one"; STAGE_D.md of nvfp4-megamoe-kernel, sections 2, 3, 4 and 6):
+//   O = softmax(scale * Q K^T + causal mask) V  and  LSE = log-sum-exp of each row,
+// in ONE kernel: scores and weights live in tensor memory only, never in DRAM (the
+// single-kernel fusion the first page finds missing from the mapper's search space).
+//
+// Work item = (batch*head bh, 128-row query tile qt, value-column half): head_dim 512
+// splits the 512 output columns into two 256-wide items (tensor memory holds S twice
+// plus a 256-column O).  Items are ordered longest first (causal: most key tiles first)
+// and dealt to a persistent grid in a snake order; every CTA walks its own list, so no
+// scheduler state lives in global memory.
+//
+// Warp roles (256 threads):
+//   warp 0      TMA producer: Q tile per item, then K / V tiles through an mbarrier ring in
+//               exactly the order the MMA issuer consumes them.
+//   warp 1      TMEM owner + MMA issuer (one thread): S = Q K^T into one of two S buffers
+//               (head_dim summed over every 64-wide slice before the softmax sees S),
+//               then O += P V.  QK of the next key tile is issued before PV of the current
+//               one, so the tensor core works while the softmax runs.
+//   warps 4..7  softmax + epilogue, one query row per thread: row max, exp2, row sum,
+//               lazy O rescale (only when the running max grows by more than 2^8), P as
+//               fp16 back into tensor memory (aliasing S) or into shared memory; then
+//               O / l -> fp16 -> swizzled staging tile -> TMA store, and LSE.
+//   warps 2,3   idle.
+//
+// Every wait is bounded (about two seconds of SM clock); a wait that runs out records a
+// status code, raises a CTA-wide abort flag, and the CTA drains its in-flight copies and
+// MMAs, frees tensor memory and exits.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace gbattn {
+
+constexpr unsigned kDevTimeoutLoad = 1;
+constexpr unsigned kDevTimeoutMma = 2;
+constexpr unsigned kDevTimeoutSoftmax = 3;
+constexpr unsigned kDevTimeoutEpilogue = 4;
+constexpr unsigned kDevTimeoutProbe = 5;
+
+struct FwdParams {
+  float *lse;              // [BH, L] fp32
+  unsigned *status;        // device status word (first error code wins)
+  long long wait_limit;    // SM clock cycles a single wait may take before it gives up
+  int BH, L, nQ, n_items;  // nQ = ceil(L / 128)
+  float c2;                // scale * log2(e)
+};
+
+template <int D, bool P_TMEM>
+struct FwdCfg {
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int DVS = D > 256 ? D / 256 : 1;  // value-column splits per (bh, qt)
+  static constexpr int DV = D / DVS;                 // O columns owned by one item
+  static constexpr int NCH = D / 64;                 // 64-column chunks of a Q / K tile
+  static constexpr int NCHV = DV / 64;               // 64-column chunks of an item's V tile
+  static constexpr int SC = D == 64 ? 1 : 2;         // chunks per ring stage
+  static constexpr int KST = NCH / SC;               // ring stages per K tile
+  static constexpr int VST = NCHV / SC;              // ring stages per V tile
+  static constexpr int NQB = D <= 128 ? 2 : 1;       // Q buffers (also the O staging tiles)
+  static constexpr bool LOOKAHEAD = NQB >= 2;        // next item's first QK before last PV
+  static constexpr int CHUNK = 128 * 128;            // bytes of a 128-row x 64-col fp16 box
+  static constexpr int STAGE = SC * CHUNK;
+  static constexpr int QBYTES = NCH * CHUNK;
+  static constexpr int NPB = P_TMEM ? 0 : 2;         // shared-memory P buffers
+  static constexpr int PBYTES = 2 * CHUNK;           // 128 x 128 fp16
+  static constexpr int TILE_BUDGET = 224 * 1024;
+  static constexpr int NST_FIT = (TILE_BUDGET - NQB * QBYTES - NPB * PBYTES) / STAGE;
+  static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
+  // barrier indices
+  static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_FULL = 4, B_EMPTY = 4 + NST;
+  static constexpr int B_SFULL = 4 + 2 * NST, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2;
+  static constexpr int B_OFREE = B_ODONE + 1, B_EPI = B_OFREE + 1, B_DRAIN = B_EPI + 1;
+  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr int TILE_BYTES = NQB * QBYTES + NPB * PBYTES + NST * STAGE;
+  static constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + TILE_BYTES + 8 * NBAR + 16;
+  // tensor memory columns: S buffers at [0,128) and [128,256), O at [256, 256 + DV)
+  static constexpr int O_COL = 256;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr uint32_t IDESC_QK = idesc_f16_f32(128, 128, 0, 0);
+  static constexpr uint32_t IDESC_PV = idesc_f16_f32(128, SC * 64, 0, 1);
+  static_assert(NST >= 2, "ring too shallow");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(O_COL + DV <= TMEM_COLS, "tensor memory budget");
+  static_assert(NCH % SC == 0 && NCHV % SC == 0, "stage split");
+};
+
+// Snake-order static schedule: pass p hands items [p*G, p*G+G) to CTAs 0..G-1, reversed
+// on odd passes, so the longest items (first in the order) are spread over all CTAs and
+// each CTA's total is balanced.
+struct Sched {
+  int cta, G, NI, pass, npass;
+  __device__ Sched(int c, int g, int ni) : cta(c), G(g), NI(ni), pass(0), npass((ni + g - 1) / g) {}
+  __device__ bool next(int &item) {
+    while (pass < npass) {
+      const int p = pass++;
+      const int r = p * G + ((p & 1) ? (G - 1 - cta) : cta);
+      if (r < NI) {
+        item = r;
+        return true;
+      }
+    }
+    return false;
+  }
+};
+
+template <int DVS, bool CAUSAL>
+__device__ __forceinline__ void decode_item(int r, const FwdParams &p, int &bh, int &qt, int &half,
+                                            int &ntiles) {
+  const int per = p.BH * DVS;
+  const int grp = r / per, rem = r - grp * per;
+  qt = CAUSAL ? (p.nQ - 1 - grp) : grp;
+  bh = rem / DVS;
+  half = rem - bh * DVS;
+  ntiles = CAUSAL ? qt + 1 : p.nQ;
+}
+
+// Bounded wait.  Gives up when the abort flag is raised or after `limit` cycles; in the
+// latter case records `code` (first error wins) and raises the abort flag.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                             unsigned *status, unsigned code, long long limit) {
+  if (mbar_try(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      atomicCAS(status, 0u, code);
+      *abort_flag = 1u;
+      return false;
+    }
+  }
+}
+// Same but ignoring the abort flag: used only while draining in-flight work at exit.
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, long long limit) {
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity)) {
+    if (clock64() - t0 > limit) return false;
+  }
+  return true;
+}
+
+template <int D, bool CAUSAL, bool P_TMEM>
+__global__ void __launch_bounds__(256, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const FwdParams p) {
+  using C = FwdCfg<D, P_TMEM>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *const base_ptr = smem_raw + (base - raw);
+  // The ring comes first: every tensor-core operand read that starts in a ring stage
+  // stays inside this CTA's tiles even at its farthest stride.
+  const uint32_t ring_s = base;                             // NST x STAGE
+  const uint32_t q_s = ring_s + C::NST * C::STAGE;          // NQB x QBYTES
+  const uint32_t p_s = q_s + C::NQB * C::QBYTES;            // NPB x PBYTES
+  const uint32_t bar_s = p_s + C::NPB * C::PBYTES;          // NBAR x 8
+  uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + (bar_s - base) + 8 * C::NBAR);
+  volatile uint32_t *const abort_flag = tmem_slot + 1;
+  auto BAR = [&](int i) -> uint32_t { return bar_s + 8u * static_cast<uint32_t>(i); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NQB; ++i) {
+      mbar_init(BAR(C::B_QFULL + i), 1);
+      mbar_init(BAR(C::B_QEMPTY + i), 1);
+    }
+    for (int i = 0; i < C::NST; ++i) {
+      mbar_init(BAR(C::B_FULL + i), 1);
+      mbar_init(BAR(C::B_EMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(BAR(C::B_SFULL + i), 1);
+      mbar_init(BAR(C::B_PFULL + i), 128);
+    }
+    mbar_init(BAR(C::B_ODONE), 1);
+    mbar_init(BAR(C::B_OFREE), 128);
+    mbar_init(BAR(C::B_EPI), 128);
+    mbar_init(BAR(C::B_DRAIN), 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const long long LIM = p.wait_limit;
+
+  if (warp == 0) {
+    // =============================================================== TMA producer
+    if (lane == 0) {
+      Sched sc(blockIdx.x, gridDim.x, p.n_items);
+      uint32_t it = 0;
+      int il = 0, item;
+      bool ok = true, have_v = false;
+      int v_bh = 0, v_kt = 0, v_half = 0;
+      const uint64_t pol_kv = policy_evict_last();
+      auto load_stage = [&](const CUtensorMap *tm, int chunk0, int y, int z) -> bool {
+        const uint32_t s = it % C::NST, ph = (it / C::NST) & 1u;
+        if (!wait_bounded(BAR(C::B_EMPTY + s), ph ^ 1u, abort_flag, p.status, kDevTimeoutLoad, LIM))
+          return false;
+        mbar_arrive_expect_tx(BAR(C::B_FULL + s), C::STAGE);
+#pragma unroll
+        for (int j = 0; j < C::SC; ++j)
+          tma_load_3d_hint(ring_s + s * C::STAGE + j * C::CHUNK, tm, (chunk0 + j) * 64, y, z,
+                           BAR(C::B_FULL + s), pol_kv);
+        ++it;
+        return true;
+      };
+      auto load_v = [&]() -> bool {
+        for (int vs = 0; vs < C::VST; ++vs)
+          if (!load_stage(&tm_v, v_half * C::NCHV + vs * C::SC, v_kt * C::BN, v_bh)) return false;
+        return true;
+      };
+      while (ok && sc.next(item)) {
+        int bh, qt, half, n;
+        decode_item<C::DVS, CAUSAL>(item, p, bh, qt, half, n);
+        if (!C::LOOKAHEAD && have_v) {
+          have_v = false;
+          if (!(ok = load_v())) break;
+        }
+        const int qb = il % C::NQB;
+        const uint32_t qph = (il / C::NQB) & 1;
+        if (!(ok = wait_bounded(BAR(C::B_QEMPTY + qb), qph ^ 1u, abort_flag, p.status, kDevTimeoutLoad, LIM)))
+          break;
+        mbar_arrive_expect_tx(BAR(C::B_QFULL + qb), C::QBYTES);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(q_s + qb * C::QBYTES + c * C::CHUNK, &tm_q, c * 64, qt * C::BM, bh, BAR(C::B_QFULL + qb));
+        for (int t = 0; t < n && ok; ++t) {
+          for (int ks = 0; ks < C::KST && ok; ++ks) ok = load_stage(&tm_k, ks * C::SC, t * C::BN, bh);
+          if (ok && have_v) ok = load_v();
+          have_v = true;
+          v_bh = bh;
+          v_kt = t;
+          v_half = half;
+        }
+        ++il;
+      }
+      if (ok && have_v) ok = load_v();
+      // Drain: every load issued must have landed before the CTA may exit.
+      const uint32_t first = it > static_cast<uint32_t>(C::NST) ? it - C::NST : 0u;
+      for (uint32_t i = first; i < it; ++i)
+        wait_drain(BAR(C::B_FULL + (i % C::NST)), (i / C::NST) & 1u, LIM);
+      for (int i = (il > C::NQB ? il - C::NQB : 0); i < il; ++i)
+        wait_drain(BAR(C::B_QFULL + (i % C::NQB)), (i / C::NQB) & 1, LIM);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // =============================================================== MMA issuer
+    if (lane == 0) {
+      Sched sc(blockIdx.x, gridDim.x, p.n_items);
+      uint32_t it = 0, g = 0;
+      int il = 0, item;
+      bool ok = true, have_pv = false;
+      uint32_t pv_g = 0;
+      bool pv_first = false;
+      int pv_il = 0;
+      auto wait = [&](uint32_t bar, uint32_t ph) -> bool {
+        return wait_bounded(bar, ph, abort_flag, p.status, kDevTimeoutMma, LIM);
+      };
+      auto issue_qk = [&](uint32_t gg, int qb) -> bool {
+        const uint32_t d_tmem = tmem + (gg & 1u) * 128u;
+        for (int ks = 0; ks < C::KST; ++ks) {
+          const uint32_t s = it % C::NST;
+          if (!wait(BAR(C::B_FULL + s), (it / C::NST) & 1u)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int j = 0; j < C::SC; ++j) {
+            const int cidx = ks * C::SC + j;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t a = sdesc_sw128(q_s + qb * C::QBYTES + cidx * C::CHUNK + kk * 32, 16, 1024);
+              const uint64_t b = sdesc_sw128(ring_s + s * C::STAGE + j * C::CHUNK + kk * 32, 16, 1024);
+              umma_ss(d_tmem, a, b, C::IDESC_QK, (cidx | kk) != 0 ? 1u : 0u);
+            }
+          }
+          umma_commit(BAR(C::B_EMPTY + s));
+          ++it;
+        }
+        umma_commit(BAR(C::B_SFULL + (gg & 1u)));
+        return true;
+      };
+      auto issue_pv = [&]() -> bool {
+        const uint32_t sb = pv_g & 1u;
+        if (!wait(BAR(C::B_PFULL + sb), (pv_g >> 1) & 1u)) return false;
+        if (pv_first && pv_il > 0 && !wait(BAR(C::B_OFREE), (pv_il - 1) & 1)) return false;
+        tc_fence_after();
+        for (int vs = 0; vs < C::VST; ++vs) {
+          const uint32_t s = it % C::NST;
+          if (!wait(BAR(C::B_FULL + s), (it / C::NST) & 1u)) return false;
+          tc_fence_after();
+          const uint32_t o_tmem = tmem + C::O_COL + vs * C::SC * 64;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t b = sdesc_sw128(ring_s + s * C::STAGE + kk * 2048, C::CHUNK, 1024);
+            const uint32_t acc = (pv_first && kk == 0) ? 0u : 1u;
+            if constexpr (P_TMEM) {
+              umma_ts(o_tmem, tmem + sb * 128u + kk * 8u, b, C::IDESC_PV, acc);
+            } else {
+              const uint64_t a =
+                  sdesc_sw128(p_s + sb * C::PBYTES + (kk >> 2) * C::CHUNK + (kk & 3) * 32, 16, 1024);
+              umma_ss(o_tmem, a, b, C::IDESC_PV, acc);
+            }
+          }
+          umma_commit(BAR(C::B_EMPTY + s));
+          ++it;
+        }
+        umma_commit(BAR(C::B_ODONE));
+        return true;
+      };
+      while (ok && sc.next(item)) {
+        int bh, qt, half, n;
+        decode_item<C::DVS, CAUSAL>(item, p, bh, qt, half, n);
+        if (!C::LOOKAHEAD && have_pv) {
+          have_pv = false;
+          if (!(ok = issue_pv())) break;
+        }
+        const int qb = il % C::NQB;
+        if (!(ok = wait(BAR(C::B_QFULL + qb), (il / C::NQB) & 1))) break;
+        tc_fence_after();
+        for (int t = 0; t < n && ok; ++t) {
+          ok = issue_qk(g, qb);
+          if (ok && have_pv) ok = issue_pv();
+          have_pv = true;
+          pv_g = g;
+          pv_first = (t == 0);
+          pv_il = il;
+          ++g;
+        }
+        ++il;
+      }
+      if (ok && have_pv) ok = issue_pv();
+      // Drain: all MMAs issued by this thread complete before tensor memory is freed.
+      umma_commit(BAR(C::B_DRAIN));
+      wait_drain(BAR(C::B_DRAIN), 0, LIM);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // =============================================================== softmax + epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // query row within the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const float c2 = p.c2;
+    Sched sc(blockIdx.x, gridDim.x, p.n_items);
+    uint32_t g = 0;
+    int il = 0, item;
+    bool ok = true;
+    auto wait_warp = [&](uint32_t bar, uint32_t ph) -> bool {
+      const bool r = wait_bounded(bar, ph, abort_flag, p.status, kDevTimeoutSoftmax, LIM);
+      return __all_sync(0xffffffffu, r);
+    };
+    while (ok && sc.next(item)) {
+      int bh, qt, half, n;
+      decode_item<C::DVS, CAUSAL>(item, p, bh, qt, half, n);
+      float m_used = 0.f, l = 0.f;
+      for (int t = 0; t < n; ++t, ++g) {
+        const uint32_t sb = g & 1u;
+        if (!(ok = wait_warp(BAR(C::B_SFULL + sb), (g >> 1) & 1u))) break;
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld32x128(tmem + lane_base + sb * 128u, sr);
+        float *s = reinterpret_cast<float *>(sr);
+        if (CAUSAL) {
+          if (t == qt) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c > row) s[c] = -INFINITY;
+          }
+        } else {
+          const int lim = p.L - t * C::BN;
+          if (lim < C::BN) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c >= lim) s[c] = -INFINITY;
+          }
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        float m_tile = mx * c2;
+        if (t == 0) {
+          m_used = (m_tile == -INFINITY) ? 0.f : m_tile;
+        } else {
+          // PV of the previous key tile must be complete before O may be rescaled.
+          if (!(ok = wait_warp(BAR(C::B_ODONE), (g - 1) & 1u))) break;
+          tc_fence_after();
+          const bool need = m_tile > m_used + 8.0f;
+          if (__any_sync(0xffffffffu, need)) {
+            const float m_new = fmaxf(m_used, m_tile);
+            const float alpha = ex2_approx(m_used - m_new);
+            m_used = m_new;
+            l *= alpha;
+#pragma unroll 1
+            for (int c32 = 0; c32 < C::DV / 32; ++c32) {
+              uint32_t orr[32];
+              const uint32_t ta = tmem + lane_base + C::O_COL + c32 * 32;
+              tmem_ld32x32(ta, orr);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+              tmem_st32x32(ta, orr);
+            }
+          }
+        }
+        const float neg = -m_used;
+        float sum = 0.f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float p0 = ex2_approx(fmaf(s[2 * c], c2, neg));
+          const float p1 = ex2_approx(fmaf(s[2 * c + 1], c2, neg));
+          sum += p0 + p1;
+          pk[c] = pack_f16x2(p0, p1);
+        }
+        l += sum;
+        if constexpr (P_TMEM) {
+          tmem_st32x64(tmem + lane_base + sb * 128u, pk);
+        } else {
+          const uint32_t pb = p_s + sb * C::PBYTES + row * 128;
+#pragma unroll
+          for (int ch = 0; ch < 16; ++ch) {
+            const uint32_t addr = pb + (ch >> 3) * C::CHUNK + ((((ch & 7) ^ (row & 7))) << 4);
+            st_shared_v4(addr, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+          }
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        mbar_arrive(BAR(C::B_PFULL + sb));
+      }
+      if (!ok) break;
+      // ------------------------------------------------------------- epilogue
+      if (!(ok = wait_warp(BAR(C::B_ODONE), (g - 1) & 1u))) break;
+      tc_fence_after();
+      const int qb = il % C::NQB;
+      const uint32_t stage = q_s + qb * C::QBYTES;  // the item's Q tile is no longer read
+      const float inv_l = 1.0f / l;
+#pragma unroll 1
+      for (int c32 = 0; c32 < C::DV / 32; ++c32) {
+        uint32_t orr[32];
+        tmem_ld32x32(tmem + lane_base + C::O_COL + c32 * 32, orr);
+        uint32_t h[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          h[i] = pack_f16x2(__uint_as_float(orr[2 * i]) * inv_l, __uint_as_float(orr[2 * i + 1]) * inv_l);
+        const uint32_t rowaddr = stage + (c32 >> 1) * C::CHUNK + row * 128;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int chunk = (c32 & 1) * 4 + q4;
+          st_shared_v4(rowaddr + ((chunk ^ (row & 7)) << 4), h[4 * q4], h[4 * q4 + 1], h[4 * q4 + 2],
+                       h[4 * q4 + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(BAR(C::B_OFREE));
+      const int grow = qt * C::BM + row;
+      if (half == 0 && grow < p.L)
+        p.lse[static_cast<long long>(bh) * p.L + grow] = (m_used + __log2f(l)) * 0.69314718055994531f;
+      fence_proxy_async_smem();
+      mbar_arrive(BAR(C::B_EPI));
+      if (warp == 4 && lane == 0) {
+        if (wait_bounded(BAR(C::B_EPI), il & 1, abort_flag, p.status, kDevTimeoutEpilogue, LIM)) {
+          for (int j = 0; j < C::NCHV; ++j)
+            tma_store_3d(&tm_o, stage + j * C::CHUNK, half * C::DV + j * 64, qt * C::BM, bh);
+          bulk_commit();
+          bulk_wait_read0();
+          mbar_arrive(BAR(C::B_QEMPTY + qb));
+        }
+      }
+      __syncwarp();
+      ++il;
+    }
+    if (warp == 4 && lane == 0) bulk_wait0();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// Launch description shared by the per-head-dim translation units and the ABI.
+struct FwdLaunch {
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;
+  FwdParams p;
+  int grid;
+  bool causal;
+  bool p_smem;
+  cudaStream_t stream;
+};
+
+template <int D, bool CAUSAL, bool P_TMEM>
+cudaError_t launch_fwd_variant(const FwdLaunch &a) {
+  using C = FwdCfg<D, P_TMEM>;
+  auto *kern = attn_fwd_kernel<D, CAUSAL, P_TMEM>;
+  static int configured_mask = 0;  // one bit per device ordinal < 31
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 31 || !(configured_mask & (1 << dev))) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev < 31) configured_mask |= (1 << dev);
+  }
+  kern<<<a.grid, 256, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdLaunch &a) {
+  if constexpr (D <= 128) {
+    if (a.p_smem)
+      return a.causal ? launch_fwd_variant<D, true, false>(a) : launch_fwd_variant<D, false, false>(a);
+  }
+  return a.causal ? launch_fwd_variant<D, true, true>(a) : launch_fwd_variant<D, false, true>(a);
+}
+
+template <int D>
+constexpr int fwd_items_per_tile() {
+  return FwdCfg<D, true>::DVS;
+}
+
+cudaError_t launch_fwd_64(const FwdLaunch &a);
+cudaError_t launch_fwd_128(const FwdLaunch &a);
+cudaError_t launch_fwd_256(const FwdLaunch &a);
+cudaError_t launch_fwd_512(const FwdLaunch &a);
+
+}  // namespace gbattn

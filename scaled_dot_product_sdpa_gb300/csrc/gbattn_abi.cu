@@ -1,0 +1,239 @@
+// gbattn_abi.cu -- the C ABI of libgbattn.so (declared in include/gbattn.h): argument
+// checks, per-device setup, TMA descriptor encoding and kernel launch.  No entry point
+// allocates device memory or synchronises (except attn_last_device_error, which is a
+// documented host-blocking read of the device status word).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_fwd_kernel.cuh"
+#include "gbattn.h"
+
+namespace gbattn {
+
+// One status word per device (each device that loads the module gets its own copy).
+// Kernels receive its device address as a parameter; the first error code wins.
+__device__ unsigned g_status;
+
+cudaError_t launch_debug_scores(int d, const CUtensorMap &tq, const CUtensorMap &tk, float *s, int BH, int L,
+                                float scale, unsigned *status, long long limit, cudaStream_t st);
+cudaError_t launch_wait_probe(unsigned *status, long long limit, cudaStream_t st);
+
+namespace {
+
+constexpr long long kWaitLimitCycles = 1LL << 32;  // about two seconds of SM clock
+constexpr int kMaxDevices = 64;
+
+struct DevInfo {
+  bool init = false;
+  int cc_major = 0, cc_minor = 0, sm_count = 0;
+  unsigned *status = nullptr;
+};
+DevInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Per-device setup on first use: capability, SM count, status-word address, and the
+// driver's tensor-map encoder (fetched through the runtime, so no -lcuda link).
+int device_info(DevInfo **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GBATTN_ERR_LAUNCH;
+  if (dev < 0 || dev >= kMaxDevices) return GBATTN_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo &d = g_dev[dev];
+  if (!d.init) {
+    if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return GBATTN_ERR_LAUNCH;
+    if (d.cc_major != 10 || d.cc_minor != 3) return GBATTN_ERR_DEVICE;
+    void *addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status) != cudaSuccess || addr == nullptr) return GBATTN_ERR_LAUNCH;
+    d.status = static_cast<unsigned *>(addr);
+    if (g_encode == nullptr) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return GBATTN_ERR_TENSORMAP;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    d.init = true;
+  }
+  *out = &d;
+  return GBATTN_OK;
+}
+
+// [BH, L, D] fp16 viewed as a 3-D tensor (D innermost); box = 64 columns (128 B, the
+// swizzle span) x 128 rows x 1 head.  Rows past L read as zero and are never written.
+int encode_bhld(CUtensorMap *tm, const void *ptr, int BH, int L, int D) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2u,
+                                 static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(D) * 2u};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+                              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GBATTN_OK : GBATTN_ERR_TENSORMAP;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int B, int H, int L, int d) {
+  if (B <= 0 || H <= 0 || L <= 0) return GBATTN_ERR_DIMS;
+  const long long rows = static_cast<long long>(B) * H * L;
+  if (rows > INT_MAX || static_cast<long long>(B) * H > INT_MAX) return GBATTN_ERR_DIMS;
+  if (d != 64 && d != 128 && d != 256 && d != 512) return GBATTN_ERR_HEAD_DIM;
+  return GBATTN_OK;
+}
+
+}  // namespace
+}  // namespace gbattn
+
+using namespace gbattn;
+
+extern "C" int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int L,
+                           int d, int causal, float scale, void *stream, int flags, int grid_limit) {
+  if (!q || !k || !v || !o || !lse) return GBATTN_ERR_NULL;
+  int rc = check_shape(B, H, L, d);
+  if (rc != GBATTN_OK) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return GBATTN_ERR_ALIGN;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return GBATTN_ERR_SCALE;
+  const bool p_smem = (flags & GBATTN_FLAG_P_SMEM) != 0;
+  if (p_smem && d > 128) return GBATTN_ERR_HEAD_DIM;
+  if (grid_limit < 0) return GBATTN_ERR_DIMS;
+  const long long rows = static_cast<long long>(B) * H * L;
+  const size_t tbytes = static_cast<size_t>(rows) * static_cast<size_t>(d) * 2u;
+  const size_t lbytes = static_cast<size_t>(rows) * 4u;
+  if (overlaps(o, tbytes, q, tbytes) || overlaps(o, tbytes, k, tbytes) || overlaps(o, tbytes, v, tbytes) ||
+      overlaps(lse, lbytes, q, tbytes) || overlaps(lse, lbytes, k, tbytes) || overlaps(lse, lbytes, v, tbytes) ||
+      overlaps(lse, lbytes, o, tbytes))
+    return GBATTN_ERR_ALIAS;
+
+  DevInfo *di = nullptr;
+  if ((rc = device_info(&di)) != GBATTN_OK) return rc;
+
+  const int BH = B * H;
+  const int nQ = (L + 127) / 128;
+  const int dvs = d > 256 ? d / 256 : 1;
+  const long long n_items = static_cast<long long>(BH) * nQ * dvs;
+  if (n_items > INT_MAX) return GBATTN_ERR_DIMS;
+
+  FwdLaunch a;
+  if (encode_bhld(&a.tm_q, q, BH, L, d) || encode_bhld(&a.tm_k, k, BH, L, d) || encode_bhld(&a.tm_v, v, BH, L, d) ||
+      encode_bhld(&a.tm_o, o, BH, L, d))
+    return GBATTN_ERR_TENSORMAP;
+  int grid = di->sm_count;
+  if (grid_limit > 0 && grid_limit < grid) grid = grid_limit;
+  if (n_items < grid) grid = static_cast<int>(n_items);
+  a.grid = grid;
+  a.causal = causal != 0;
+  a.p_smem = p_smem;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.p.lse = lse;
+  a.p.status = di->status;
+  a.p.wait_limit = kWaitLimitCycles;
+  a.p.BH = BH;
+  a.p.L = L;
+  a.p.nQ = nQ;
+  a.p.n_items = static_cast<int>(n_items);
+  a.p.c2 = scale * 1.4426950408889634f;
+
+  cudaError_t e;
+  switch (d) {
+    case 64: e = launch_fwd_64(a); break;
+    case 128: e = launch_fwd_128(a); break;
+    case 256: e = launch_fwd_256(a); break;
+    default: e = launch_fwd_512(a); break;
+  }
+  return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_LAUNCH;
+}
+
+extern "C" int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int L, int d,
+                        int causal, float scale, void *stream) {
+  return attn_fwd_ex(q, k, v, o, lse, B, H, L, d, causal, scale, stream, 0, 0);
+}
+
+extern "C" int attn_debug_scores(const void *q, const void *k, float *s, int B, int H, int L, int d, float scale,
+                                 void *stream) {
+  if (!q || !k || !s) return GBATTN_ERR_NULL;
+  int rc = check_shape(B, H, L, d);
+  if (rc != GBATTN_OK) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(s)) return GBATTN_ERR_ALIGN;
+  if (!std::isfinite(scale)) return GBATTN_ERR_SCALE;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long nQ = (L + 127) / 128;
+  if (BH > 65535 || nQ * nQ > INT_MAX) return GBATTN_ERR_DIMS;
+  const size_t tbytes = static_cast<size_t>(BH) * L * d * 2u;
+  const size_t sbytes = static_cast<size_t>(BH) * L * L * 4u;
+  if (overlaps(s, sbytes, q, tbytes) || overlaps(s, sbytes, k, tbytes)) return GBATTN_ERR_ALIAS;
+  DevInfo *di = nullptr;
+  if ((rc = device_info(&di)) != GBATTN_OK) return rc;
+  CUtensorMap tq, tk;
+  if (encode_bhld(&tq, q, static_cast<int>(BH), L, d) || encode_bhld(&tk, k, static_cast<int>(BH), L, d))
+    return GBATTN_ERR_TENSORMAP;
+  const cudaError_t e = launch_debug_scores(d, tq, tk, s, static_cast<int>(BH), L, scale, di->status,
+                                            kWaitLimitCycles, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_LAUNCH;
+}
+
+extern "C" int attn_debug_wait_probe(long long limit_cycles, void *stream) {
+  DevInfo *di = nullptr;
+  const int rc = device_info(&di);
+  if (rc != GBATTN_OK) return rc;
+  long long lim = limit_cycles < 1000 ? 1000 : limit_cycles;
+  if (lim > 100000000LL) lim = 100000000LL;
+  return launch_wait_probe(di->status, lim, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GBATTN_OK
+                                                                                               : GBATTN_ERR_LAUNCH;
+}
+
+extern "C" int attn_last_device_error(void) {
+  DevInfo *di = nullptr;
+  const int rc = device_info(&di);
+  if (rc != GBATTN_OK) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return GBATTN_ERR_LAUNCH;
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(v)) != cudaSuccess) return GBATTN_ERR_LAUNCH;
+  if (cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess) return GBATTN_ERR_LAUNCH;
+  return static_cast<int>(v);
+}
+
+extern "C" const char *attn_strerror(int code) {
+  switch (code) {
+    case GBATTN_OK: return "success";
+    case GBATTN_ERR_NULL: return "a required pointer is NULL";
+    case GBATTN_ERR_DIMS: return "bad dimensions (B, H, L must be > 0 and B*H*L must fit in int32)";
+    case GBATTN_ERR_HEAD_DIM: return "unsupported head_dim (64, 128, 256 or 512; shared-memory P only for <= 128)";
+    case GBATTN_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case GBATTN_ERR_LAUNCH: return "a CUDA call or the kernel launch failed";
+    case GBATTN_ERR_DEVICE: return "the current device is not compute capability 10.3 (sm_103)";
+    case GBATTN_ERR_SCALE: return "scale must be finite and > 0";
+    case GBATTN_ERR_ALIAS: return "an output overlaps an input or the other output";
+    case GBATTN_ERR_TENSORMAP: return "the driver rejected a TMA tensor-map descriptor";
+    case GBATTN_DEV_TIMEOUT_LOAD: return "device: the TMA producer's wait timed out";
+    case GBATTN_DEV_TIMEOUT_MMA: return "device: the MMA issuer's wait timed out";
+    case GBATTN_DEV_TIMEOUT_SOFTMAX: return "device: a softmax warp's wait timed out";
+    case GBATTN_DEV_TIMEOUT_EPILOGUE: return "device: the epilogue's wait timed out";
+    case GBATTN_DEV_TIMEOUT_PROBE: return "device: the wait-probe barrier timed out (expected)";
+    default: return "unknown gbattn status code";
+  }
+}
+
+extern "C" int attn_version(void) { return 100; }

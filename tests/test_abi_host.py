@@ -1,0 +1,122 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds for sm_103a, loads,
+exports every entry point include/gbattn.h declares, and rejects bad arguments with the
+documented codes before touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gbattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from scaled_dot_product_sdpa_gb300 import build as b
+    path = b.build()
+    import scaled_dot_product_sdpa_gb300 as g
+    return g.load_library(path)
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^(?:int|const char \*)\s*(\w+)\(", text, re.M)))
+
+
+def _codes():
+    text = open(HEADER).read()
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"#define (GBATTN_\w+) \(?(-?\d+)\)?", text)}
+
+
+def test_header_declares_the_scope_entry_points():
+    names = _declared()
+    for required in ("attn_fwd", "attn_last_device_error", "attn_strerror", "attn_debug_scores"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = os.path.join(ROOT, "scaled_dot_product_sdpa_gb300", "libgbattn.so")
+    out = subprocess.run(["nm", "-D", "--defined-only", so], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r" T (\w+)$", out, re.M))
+    missing = [n for n in _declared() if n not in exported]
+    assert not missing, missing
+    for n in _declared():
+        assert hasattr(lib, n)
+
+
+def test_strerror_covers_every_code(lib):
+    for name, code in _codes().items():
+        if name.startswith("GBATTN_FLAG"):
+            continue
+        msg = lib.attn_strerror(code).decode()
+        assert msg and "unknown" not in msg, (name, code)
+    assert "unknown" in lib.attn_strerror(12345).decode()
+    assert lib.attn_version() >= 100
+
+
+# Fake, 16-byte-aligned, non-overlapping "device" addresses: validation rejects the call
+# before any CUDA API is reached, so nothing is dereferenced.
+Q, K, V, O, LSE = 0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000
+
+
+def _fwd(lib, q=Q, k=K, v=V, o=O, lse=LSE, B=1, H=2, L=128, d=64, causal=0, scale=0.125, flags=0, grid=0):
+    return lib.attn_fwd_ex(q, k, v, o, lse, B, H, L, d, causal, scale, None, flags, grid)
+
+
+def test_rejects_null_pointers(lib):
+    codes = _codes()
+    for kw in ("q", "k", "v", "o", "lse"):
+        assert _fwd(lib, **{kw: 0}) == codes["GBATTN_ERR_NULL"]
+
+
+@pytest.mark.parametrize("B,H,L", [(0, 1, 1), (1, 0, 1), (1, 1, 0), (-1, 1, 1), (1 << 16, 1 << 16, 1)])
+def test_rejects_bad_dims(lib, B, H, L):
+    assert _fwd(lib, B=B, H=H, L=L) == _codes()["GBATTN_ERR_DIMS"]
+
+
+@pytest.mark.parametrize("d", [0, 16, 32, 96, 100, 192, 1024])
+def test_rejects_unsupported_head_dim(lib, d):
+    assert _fwd(lib, d=d) == _codes()["GBATTN_ERR_HEAD_DIM"]
+
+
+def test_smem_p_only_up_to_128(lib):
+    assert _fwd(lib, d=256, flags=1) == _codes()["GBATTN_ERR_HEAD_DIM"]
+
+
+@pytest.mark.parametrize("kw", ["q", "k", "v", "o", "lse"])
+def test_rejects_misaligned(lib, kw):
+    base = {"q": Q, "k": K, "v": V, "o": O, "lse": LSE}[kw]
+    assert _fwd(lib, **{kw: base + 8}) == _codes()["GBATTN_ERR_ALIGN"]
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.5, float("inf"), float("nan")])
+def test_rejects_bad_scale(lib, scale):
+    assert _fwd(lib, scale=scale) == _codes()["GBATTN_ERR_SCALE"]
+
+
+def test_rejects_aliased_outputs(lib):
+    a = _codes()["GBATTN_ERR_ALIAS"]
+    assert _fwd(lib, o=Q) == a
+    assert _fwd(lib, o=V + 256) == a          # overlaps the tail of v
+    assert _fwd(lib, lse=O + 1024) == a       # lse inside o
+    assert _fwd(lib, lse=K) == a
+
+
+def test_valid_call_without_gpu_fails_cleanly(lib):
+    """Past validation, a machine without a usable sm_103 device gets an error code.
+    Only run where no GPU is visible: the addresses above are fake."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; the fake addresses must never reach a launch")
+    rc = _fwd(lib)
+    assert rc in (_codes()["GBATTN_ERR_LAUNCH"], _codes()["GBATTN_ERR_DEVICE"])
+
+
+def test_debug_scores_validation(lib):
+    c = _codes()
+    assert lib.attn_debug_scores(0, K, O, 1, 1, 128, 64, 0.1, None) == c["GBATTN_ERR_NULL"]
+    assert lib.attn_debug_scores(Q, K, O, 1, 1, 128, 48, 0.1, None) == c["GBATTN_ERR_HEAD_DIM"]
+    assert lib.attn_debug_scores(Q, K, O + 4, 1, 1, 128, 64, 0.1, None) == c["GBATTN_ERR_ALIGN"]
+    assert lib.attn_debug_scores(Q, K, Q, 1, 1, 128, 64, 0.1, None) == c["GBATTN_ERR_ALIAS"]

@@ -1,0 +1,188 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the float64 oracle.
+
+Tolerances: O within atol = rtol = 2e-2 elementwise, the numerics gate of "An Optimal
+Mapper Meets a Real GPU" ("Ground rules": FP16 in, FP32 accumulate, atol/rtol 2e-2);
+LSE within 1e-3 absolute.  The raw-score hook is held to the worst-case float32
+summation bound d * 2^-23 * scale * sum_t |q_t k_t| (fp16 products are exact in fp32),
+which a half-length dot product (STAGE_D.md's QK bug) or a wrong descriptor breaks by
+orders of magnitude.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import scaled_dot_product_sdpa_gb300 as gb
+from scaled_dot_product_sdpa_gb300 import inputs
+from scaled_dot_product_sdpa_gb300.configs import WORKLOADS
+
+pytestmark = pytest.mark.gpu
+
+O_ATOL = O_RTOL = 2e-2
+LSE_ATOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from scaled_dot_product_sdpa_gb300 import build
+    gb.load_library(build.build())
+    assert gb.attn_last_device_error() == 0
+    yield
+    assert gb.attn_last_device_error() == 0, "a kernel recorded a device-side timeout"
+
+
+def _dev(*ts):
+    return [t.cuda() for t in ts]
+
+
+def _check(o, lse, o_ref, lse_ref, what=""):
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+    assert np.isfinite(o).all() and np.isfinite(lse).all(), f"{what}: non-finite output"
+    err = np.abs(o - o_ref)
+    bound = O_ATOL + O_RTOL * np.abs(o_ref)
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert (err <= bound).all(), (f"{what}: O mismatch at {worst}: got {o[worst]}, want {o_ref[worst]}; "
+                                  f"max|err| {err.max():.3e}, {(err > bound).sum()} elements out of tolerance")
+    lerr = np.abs(lse - lse_ref)
+    assert lerr.max() <= LSE_ATOL, f"{what}: LSE max err {lerr.max():.3e} at {np.unravel_index(lerr.argmax(), lerr.shape)}"
+    return err.max(), lerr.max()
+
+
+def _run(q, k, v, causal, scale, **kw):
+    o, lse = gb.attn_fwd(q, k, v, causal=causal, scale=scale, **kw)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+# ------------------------------------------------------------------ failure path
+def test_wait_probe_turns_a_stuck_wait_into_a_status():
+    """A wait on a barrier that nothing completes gives up and reports its code."""
+    gb.attn_debug_wait_probe(200_000)
+    assert gb.attn_last_device_error() == 5
+    assert gb.attn_last_device_error() == 0  # read-and-clear
+
+
+# ------------------------------------------------------------------ QK stage alone
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+@pytest.mark.parametrize("L", [128, 200])
+def test_debug_scores_match_oracle(d, L):
+    q, k, _ = inputs.qkv(1, 2, L, d, seed=1000 + d + L, sigma=0.5 if d == 512 else 1.0)
+    scale = 1.0 / math.sqrt(d)
+    s = gb.attn_debug_scores(*_dev(q, k), scale=scale)
+    torch.cuda.synchronize()
+    s_ref = oracle.scores(q, k, float(np.float32(scale)))
+    qa, ka = (np.abs(x.double().numpy()) for x in (q, k))
+    mag = np.einsum("bhid,bhjd->bhij", qa, ka) * float(np.float32(scale))
+    bound = d * 2.0 ** -23 * mag + 1e-6
+    err = np.abs(s.cpu().numpy().astype(np.float64) - s_ref)
+    assert (err <= bound).all(), f"max err {err.max():.3e}, max excess {(err - bound).max():.3e}"
+
+
+# ------------------------------------------------------------------ fused forward, small
+SMALL = [(L, d) for d in (64, 128) for L in (1, 17, 127, 128, 129, 200, 256, 384)] + \
+        [(L, d) for d in (256, 512) for L in (1, 100, 128, 300)]
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("L,d", SMALL)
+def test_fwd_small_matches_oracle(L, d, causal):
+    q, k, v = inputs.qkv(2, 3, L, d, seed=7 * L + d + int(causal), sigma=0.5 if d == 512 else 1.0)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(*_dev(q, k, v), causal, scale)
+    o_ref, lse_ref = oracle.sdpa_fwd(q, k, v, causal, float(np.float32(scale)))
+    _check(o, lse, o_ref, lse_ref, f"L={L} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("L,d", [(200, 64), (384, 64), (129, 128), (384, 128)])
+def test_fwd_smem_p_variant_matches_oracle(L, d, causal):
+    """P staged through shared memory instead of tensor memory: same results."""
+    q, k, v = inputs.qkv(1, 4, L, d, seed=31 * L + d)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(*_dev(q, k, v), causal, scale, flags=gb.FLAG_P_SMEM)
+    o_ref, lse_ref = oracle.sdpa_fwd(q, k, v, causal, float(np.float32(scale)))
+    _check(o, lse, o_ref, lse_ref, "smem-P")
+
+
+@pytest.mark.parametrize("grid", [1, 2, 3, 7])
+@pytest.mark.parametrize("d", [64, 128, 512])
+def test_fwd_persistent_loop_with_few_ctas(grid, d):
+    """Few CTAs => many items per CTA: exercises the cross-item pipeline and the phase
+    bookkeeping of every barrier over long runs."""
+    L = 640 if d < 512 else 384
+    q, k, v = inputs.qkv(1, 3, L, d, seed=grid * 100 + d, sigma=0.5 if d == 512 else 1.0)
+    scale = 1.0 / math.sqrt(d)
+    for causal in (False, True):
+        o, lse = _run(*_dev(q, k, v), causal, scale, grid_limit=grid)
+        o_ref, lse_ref = oracle.sdpa_fwd(q, k, v, causal, float(np.float32(scale)))
+        _check(o, lse, o_ref, lse_ref, f"grid={grid} causal={causal}")
+
+
+def test_fwd_large_logits_force_rescale():
+    """Keys whose logits grow along the sequence force the lazy O rescale path."""
+    B, H, L, d = 1, 2, 512, 64
+    q, k, v = inputs.qkv(B, H, L, d, seed=77)
+    q = q.abs()  # every q_i . 1 > 0, so logits grow with the ramp added to every key
+    ramp = torch.linspace(0, 6, L).view(1, 1, L, 1)
+    k = (k.float() * 0.2 + ramp).half()
+    scale = 1.0 / math.sqrt(d)
+    for causal in (False, True):
+        o, lse = _run(*_dev(q, k, v), causal, scale)
+        o_ref, lse_ref = oracle.sdpa_fwd(q, k, v, causal, float(np.float32(scale)))
+        _check(o, lse, o_ref, lse_ref, "rescale")
+
+
+# ------------------------------------------------------------------ the five workloads
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_workload_full_size_matches_oracle(name):
+    w = WORKLOADS[name]
+    q, k, v = inputs.qkv(w.B, w.H, w.L, w.d, w.seed, w.sigma)
+    o, lse = _run(*_dev(q, k, v), w.causal, w.scale)
+    o_ref, lse_ref = oracle.sdpa_fwd(q, k, v, w.causal, float(np.float32(w.scale)))
+    e_o, e_l = _check(o, lse, o_ref, lse_ref, name)
+    print(f"{name}: max|dO| {e_o:.3e}  max|dLSE| {e_l:.3e}")
+
+
+# ------------------------------------------------------------------ guards and determinism
+@pytest.mark.parametrize("L,d,causal", [(200, 64, True), (129, 128, False), (300, 512, True)])
+def test_outputs_stay_inside_their_buffers(L, d, causal):
+    B, H = 1, 2
+    q, k, v = _dev(*inputs.qkv(B, H, L, d, seed=5))
+    n_o, n_l, pad = B * H * L * d, B * H * L, 4096
+    o_buf = torch.full((n_o + 2 * pad,), 1234.0, dtype=torch.float16, device="cuda")
+    l_buf = torch.full((n_l + 2 * pad,), -777.0, dtype=torch.float32, device="cuda")
+    o = o_buf[pad:pad + n_o].view(B, H, L, d)
+    lse = l_buf[pad:pad + n_l].view(B, H, L)
+    gb.attn_fwd(q, k, v, causal=causal, o=o, lse=lse)
+    torch.cuda.synchronize()
+    assert (o_buf[:pad] == 1234.0).all() and (o_buf[pad + n_o:] == 1234.0).all()
+    assert (l_buf[:pad] == -777.0).all() and (l_buf[pad + n_l:] == -777.0).all()
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+def test_repeated_calls_are_bitwise_identical():
+    w = WORKLOADS["caseC"]
+    q, k, v = _dev(*inputs.qkv(w.B, w.H, w.L, w.d, w.seed, w.sigma))
+    o1, l1 = _run(q, k, v, w.causal, w.scale)
+    o2, l2 = _run(q, k, v, w.causal, w.scale)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_runs_on_a_side_stream():
+    w = WORKLOADS["caseB"]
+    q, k, v = _dev(*inputs.qkv(w.B, w.H, w.L, w.d, w.seed, w.sigma))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o, lse = gb.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, stream=s)
+    s.synchronize()
+    o_ref, lse_ref = oracle.sdpa_fwd(*(t.cpu() for t in (q, k, v)), w.causal, float(np.float32(w.scale)))
+    _check(o, lse, o_ref, lse_ref, "side stream")
+
+
+def test_cpu_tensors_are_rejected_loudly():
+    q, k, v = inputs.qkv(1, 1, 128, 64, seed=1)
+    with pytest.raises(ValueError):
+        gb.attn_fwd(q, k, v)
