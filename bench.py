@@ -68,10 +68,15 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def stored_traffic(workload: str):
+def kernel_name(d: int) -> str:
+    """The kernel attn_fwd runs for head_dim d (two-tile kernel for d <= 128)."""
+    return "attn_fwd_pp_kernel" if d <= 128 else "attn_fwd_kernel"
+
+
+def stored_traffic(workload: str, d: int):
     """dram read+write bytes per launch from the committed ncu summary of this workload,
     if it was taken on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"attn_fwd_kernel_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel_name(d)}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -327,7 +332,7 @@ def bench_ours(args):
     hbm_peak = peaks["hbm_gbs"]
     achieved_gbs = w.bytes() / t_max / 1e9
     bound = "hbm" if w.flops() / w.bytes() < fp16_peak * 1e12 / (hbm_peak * 1e9) else "tensor"
-    traffic = stored_traffic(w.name)
+    traffic = stored_traffic(w.name, w.d)
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved_gbs / hbm_peak, 4)}
@@ -335,6 +340,7 @@ def bench_ours(args):
         roof = {"bound": "tensor", "achieved": round(w.flops() / t_max / 1e12, 1), "peak": fp16_peak,
                 "unit": "TFLOP/s", "frac": round(w.flops() / t_max / 1e12 / fp16_peak, 4)}
     roof["traffic"] = traffic
+    roof["kernel"] = kernel_name(w.d)
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
     roof["algorithmic_bytes_per_launch"] = w.bytes()
     roof["algorithmic_flops_per_launch"] = w.flops()

@@ -43,6 +43,7 @@ extern "C" {
 #define GBATTN_ERR_SCALE (-7)       /* scale is not a finite number > 0                      */
 #define GBATTN_ERR_ALIAS (-8)       /* an output overlaps an input or the other output       */
 #define GBATTN_ERR_TENSORMAP (-9)   /* the driver rejected a TMA descriptor                  */
+#define GBATTN_ERR_FLAGS (-10)      /* attn_fwd_ex: unknown bits in flags                    */
 
 /* Device-side status codes reported by attn_last_device_error() (positive). */
 #define GBATTN_DEV_TIMEOUT_LOAD 1    /* the TMA producer's wait for a free buffer timed out  */
@@ -67,13 +68,20 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
              int L, int d, int causal, float scale, void *stream);
 
 /*
- * attn_fwd_ex -- attn_fwd with design options (same arguments, same errors).
- *   flags bit 0 (GBATTN_FLAG_P_SMEM): stage P through shared memory instead of tensor
- *     memory before the PV product (the SMEM-P path of the STAGE_D.md notes, section 4);
- *     only for d <= 128, otherwise GBATTN_ERR_HEAD_DIM.  Same results up to rounding.
+ * attn_fwd_ex -- attn_fwd with design options (same arguments, same errors, plus
+ * GBATTN_ERR_FLAGS for unknown flag bits).  For d <= 128 attn_fwd runs the two-tile
+ * kernel: each work item is a 256-row query block whose two 128-row halves share every
+ * K/V tile and have their own softmax warpgroup.  The options select the single-tile
+ * kernel (one 128-row query tile per item, the only kernel for d = 256 and 512):
+ *   flags bit 0 (GBATTN_FLAG_P_SMEM): single-tile kernel, with P staged through shared
+ *     memory instead of tensor memory before the PV product (the SMEM-P path of the
+ *     STAGE_D.md notes, section 4); only for d <= 128, otherwise GBATTN_ERR_HEAD_DIM.
+ *   flags bit 1 (GBATTN_FLAG_SINGLE_TILE): single-tile kernel, P in tensor memory.
  *   grid_limit: 0 = one persistent CTA per SM; n > 0 = at most n CTAs (scheduler tests).
+ * Every option gives the same results up to rounding.
  */
 #define GBATTN_FLAG_P_SMEM 1
+#define GBATTN_FLAG_SINGLE_TILE 2
 int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                 int H, int L, int d, int causal, float scale, void *stream, int flags,
                 int grid_limit);

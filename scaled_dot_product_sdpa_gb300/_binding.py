@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libgbattn.so")
 _lib = None
 
 FLAG_P_SMEM = 1
+FLAG_SINGLE_TILE = 2
 
 
 class GbattnError(RuntimeError):

@@ -47,6 +47,7 @@ struct FwdParams {
   unsigned *status;        // device status word (first error code wins)
   long long wait_limit;    // SM clock cycles a single wait may take before it gives up
   int BH, L, nQ, n_items;  // nQ = ceil(L / 128)
+  int nQB;                 // ceil(L / 256): query blocks of the two-tile kernel
   float c2;                // scale * log2(e)
 };
 

@@ -1,0 +1,492 @@
+// attn_fwd_pp.cuh -- ping-pong SDPA forward for head_dim 64 and 128 on sm_103a.
+//
+// Same mathematics as attn_fwd_kernel.cuh ("An Optimal Mapper Meets a Real GPU",
+// "Ground rules" / "Experiment one"): O = softmax(scale * Q K^T + causal mask) V and the
+// row LSE, fused into one persistent kernel.  The work item is a 256-row query block
+// split into two 128-row tiles Q0 and Q1 that share every K/V tile the producer loads
+// (half the K/V traffic per query row of the single-tile kernel), each with its own
+// softmax warpgroup, S buffer and O accumulator in tensor memory:
+//   TMEM columns  S0 [0,128)  S1 [128,256)  O0 [256, 256+D)  O1 [256+D, 256+2D).
+//
+// The MMA issuer runs one fixed stream of tensor-core operations per item:
+//   QK0_0, QK1_0, then for each key tile j:  PV0_j, QK0_{j+1}, PV1_j, QK1_{j+1}
+// where QKa_{j+1} at the end of an item is already the first QK of the next item.  PVa_j
+// always comes right before QKa_{j+1} from the same thread, so when softmax warpgroup a
+// sees S_a of tile j+1 complete, PV_a of tile j is complete too (tcgen05 operations of
+// one thread complete in order): the lazy O rescale never waits for a PV, and while
+// warpgroup a exponentiates tile j the tensor core runs the other tile's PV and QK.
+// Under the causal mask Q0 needs key tiles 0..2qb and Q1 needs 0..2qb+1; the last one
+// is run for Q1 alone.
+//
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
+// warps 4-7 softmax + epilogue of Q0, warps 8-11 softmax + epilogue of Q1, warps 2-3 idle.
+// Producer and MMA issuer walk the same operation stream (run_pp_stream), so the
+// producer loads each K or V tile into the ring in the order of its first use.
+#pragma once
+
+#include "attn_fwd_kernel.cuh"
+
+namespace gbattn {
+
+template <int D>
+struct PPCfg {
+  static constexpr int NCH = D / 64;
+  static constexpr int CHUNK = 128 * 128;            // bytes of a 128-row x 64-col fp16 box
+  static constexpr int TILE = NCH * CHUNK;           // one 128 x D tile
+  static constexpr int NQB = 2;                      // Q pairs (items) in flight
+  static constexpr int QPAIR = 2 * TILE;
+  static constexpr int TILE_BUDGET = 224 * 1024;
+  static constexpr int NST_FIT = (TILE_BUDGET - NQB * QPAIR) / TILE;
+  static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
+  static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_FULL = 4, B_EMPTY = 4 + NST;
+  static constexpr int B_SFULL = 4 + 2 * NST, B_PFULL = B_SFULL + 2, B_OFINAL = B_PFULL + 2;
+  static constexpr int B_OFREE = B_OFINAL + 2, B_EPI = B_OFREE + 2, B_DRAIN = B_EPI + 2;
+  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr int TILE_BYTES = NST * TILE + NQB * QPAIR;
+  static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + 8 * NBAR + 16;
+  static constexpr int O_COL = 256;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr uint32_t IDESC_QK = idesc_f16_f32(128, 128, 0, 0);
+  static constexpr uint32_t IDESC_PV = idesc_f16_f32(128, D, 0, 1);
+  static constexpr int kLaunchRegs = 168;  // 65536 / 384 rounded down to a multiple of 8
+  static constexpr int kRegsLow = 104, kRegsHigh = 192;
+  static_assert(NST >= 3, "ring too shallow");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(O_COL + 2 * D <= TMEM_COLS, "tensor memory budget");
+};
+
+struct PPItem {
+  int bh, qb, n0, n1;  // key tiles needed by Q0 and Q1 (n1 >= n0 >= 1)
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ PPItem pp_decode(int r, const FwdParams &p) {
+  PPItem it;
+  const int grp = r / p.BH;
+  it.bh = r - grp * p.BH;
+  it.qb = CAUSAL ? (p.nQB - 1 - grp) : grp;
+  if (CAUSAL) {
+    it.n0 = 2 * it.qb + 1;
+    it.n1 = min(2 * it.qb + 2, p.nQ);
+  } else {
+    it.n0 = it.n1 = p.nQ;
+  }
+  return it;
+}
+
+// Walk this CTA's operation stream, calling v.qk(slot, j, il, item) and
+// v.pv(slot, j, il, item) in issue order.  Returns false as soon as a visitor does.
+template <bool CAUSAL, class Visitor>
+__device__ __forceinline__ bool run_pp_stream(const FwdParams &p, Visitor &v) {
+  Sched sc(blockIdx.x, gridDim.x, p.n_items);
+  int r;
+  if (!sc.next(r)) return true;
+  PPItem cur = pp_decode<CAUSAL>(r, p);
+  bool pre0 = false, pre1 = false;
+  for (int il = 0;; ++il) {
+    Sched peek = sc;
+    int rn;
+    const bool has_next = peek.next(rn);
+    const PPItem nxt = has_next ? pp_decode<CAUSAL>(rn, p) : cur;
+    if (!pre0 && !v.qk(0, 0, il, cur)) return false;
+    if (!pre1 && !v.qk(1, 0, il, cur)) return false;
+    bool npre0 = false, npre1 = false;
+    for (int j = 0; j < cur.n1; ++j) {
+      if (j < cur.n0) {
+        if (!v.pv(0, j, il, cur)) return false;
+        if (j + 1 < cur.n0) {
+          if (!v.qk(0, j + 1, il, cur)) return false;
+        } else if (has_next) {
+          if (!v.qk(0, 0, il + 1, nxt)) return false;
+          npre0 = true;
+        }
+      }
+      if (!v.pv(1, j, il, cur)) return false;
+      if (j + 1 < cur.n1) {
+        if (!v.qk(1, j + 1, il, cur)) return false;
+      } else if (has_next) {
+        if (!v.qk(1, 0, il + 1, nxt)) return false;
+        npre1 = true;
+      }
+    }
+    if (!has_next) break;
+    sc = peek;
+    cur = nxt;
+    pre0 = npre0;
+    pre1 = npre1;
+  }
+  return true;
+}
+
+// A K tile j is first used by QK0_j (or by QK1_j when j >= n0) and last used by QK1_j;
+// likewise V tile j by PV0_j / PV1_j.
+__device__ __forceinline__ bool pp_first_use(int slot, int j, const PPItem &it) {
+  return slot == 0 || j >= it.n0;
+}
+
+template <int D, bool CAUSAL>
+struct PPProducer {
+  using C = PPCfg<D>;
+  const CUtensorMap *tq, *tk, *tv;
+  const FwdParams *p;
+  uint32_t ring_s, q_s, bar_s;
+  volatile uint32_t *abort_flag;
+  uint32_t it = 0;  // ring positions issued
+  int q_loads = 0;
+  uint64_t pol;
+  __device__ uint32_t bar(int i) const { return bar_s + 8u * static_cast<uint32_t>(i); }
+  __device__ bool load_tile(const CUtensorMap *tm, int j, int bh) {
+    const uint32_t s = it % C::NST, ph = (it / C::NST) & 1u;
+    if (!wait_bounded(bar(C::B_EMPTY + s), ph ^ 1u, abort_flag, p->status, kDevTimeoutLoad, p->wait_limit))
+      return false;
+    mbar_arrive_expect_tx(bar(C::B_FULL + s), C::TILE);
+#pragma unroll
+    for (int c = 0; c < C::NCH; ++c)
+      tma_load_3d_hint(ring_s + s * C::TILE + c * C::CHUNK, tm, c * 64, j * 128, bh, bar(C::B_FULL + s), pol);
+    ++it;
+    return true;
+  }
+  __device__ bool qk(int slot, int j, int il, const PPItem &item) {
+    if (slot == 0 && j == 0) {  // first operation of an item: bring its two Q tiles
+      const int b = il & 1;
+      if (!wait_bounded(bar(C::B_QEMPTY + b), ((il >> 1) & 1) ^ 1u, abort_flag, p->status, kDevTimeoutLoad,
+                        p->wait_limit))
+        return false;
+      mbar_arrive_expect_tx(bar(C::B_QFULL + b), C::QPAIR);
+      for (int a = 0; a < 2; ++a)
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(q_s + b * C::QPAIR + a * C::TILE + c * C::CHUNK, tq, c * 64, item.qb * 256 + a * 128,
+                      item.bh, bar(C::B_QFULL + b));
+      q_loads = il + 1;
+    }
+    return pp_first_use(slot, j, item) ? load_tile(tk, j, item.bh) : true;
+  }
+  __device__ bool pv(int slot, int j, int il, const PPItem &item) {
+    return pp_first_use(slot, j, item) ? load_tile(tv, j, item.bh) : true;
+  }
+};
+
+template <int D, bool CAUSAL>
+struct PPIssuer {
+  using C = PPCfg<D>;
+  const FwdParams *p;
+  uint32_t ring_s, q_s, bar_s, tmem;
+  volatile uint32_t *abort_flag;
+  uint32_t it = 0;                 // ring positions consumed (first uses)
+  uint32_t kpos = 0, vpos = 0;     // ring position of the K / V tile awaiting its last use
+  uint32_t n_qk[2] = {0, 0}, n_pv[2] = {0, 0};
+  __device__ uint32_t bar(int i) const { return bar_s + 8u * static_cast<uint32_t>(i); }
+  __device__ bool wait(int b, uint32_t ph) {
+    return wait_bounded(bar(b), ph, abort_flag, p->status, kDevTimeoutMma, p->wait_limit);
+  }
+  __device__ bool acquire(uint32_t &pos) {
+    pos = it++;
+    if (!wait(C::B_FULL + pos % C::NST, (pos / C::NST) & 1u)) return false;
+    tc_fence_after();
+    return true;
+  }
+  __device__ bool qk(int slot, int j, int il, const PPItem &item) {
+    if (slot == 0 && j == 0) {
+      if (!wait(C::B_QFULL + (il & 1), (il >> 1) & 1)) return false;
+      tc_fence_after();
+    }
+    uint32_t pos;
+    if (pp_first_use(slot, j, item)) {
+      if (!acquire(pos)) return false;
+      if (slot == 0) kpos = pos;
+    } else {
+      pos = kpos;
+    }
+    const uint32_t q_tile = q_s + (il & 1) * C::QPAIR + slot * C::TILE;
+    const uint32_t k_tile = ring_s + (pos % C::NST) * C::TILE;
+    const uint32_t d_tmem = tmem + slot * 128u;
+#pragma unroll
+    for (int c = 0; c < C::NCH; ++c)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        umma_ss(d_tmem, sdesc_sw128(q_tile + c * C::CHUNK + kk * 32, 16, 1024),
+                sdesc_sw128(k_tile + c * C::CHUNK + kk * 32, 16, 1024), C::IDESC_QK, (c | kk) != 0 ? 1u : 0u);
+    umma_commit(bar(C::B_SFULL + slot));
+    if (slot == 1) umma_commit(bar(C::B_EMPTY + pos % C::NST));  // last use of this K tile
+    ++n_qk[slot];
+    return true;
+  }
+  __device__ bool pv(int slot, int j, int il, const PPItem &item) {
+    if (!wait(C::B_PFULL + slot, n_pv[slot] & 1u)) return false;
+    if (j == 0 && il > 0 && !wait(C::B_OFREE + slot, (il - 1) & 1)) return false;
+    tc_fence_after();
+    uint32_t pos;
+    if (pp_first_use(slot, j, item)) {
+      if (!acquire(pos)) return false;
+      if (slot == 0) vpos = pos;
+    } else {
+      pos = vpos;
+    }
+    const uint32_t v_tile = ring_s + (pos % C::NST) * C::TILE;
+    const uint32_t o_tmem = tmem + C::O_COL + slot * D;
+    const uint32_t p_tmem = tmem + slot * 128u;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      umma_ts(o_tmem, p_tmem + kk * 8u, sdesc_sw128(v_tile + kk * 2048, C::CHUNK, 1024), C::IDESC_PV,
+              (j == 0 && kk == 0) ? 0u : 1u);
+    if (slot == 1) umma_commit(bar(C::B_EMPTY + pos % C::NST));  // last use of this V tile
+    if (j == (slot == 0 ? item.n0 : item.n1) - 1) umma_commit(bar(C::B_OFINAL + slot));
+    ++n_pv[slot];
+    return true;
+  }
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+    attn_fwd_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                       const FwdParams p) {
+  using C = PPCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *const base_ptr = smem_raw + (base - raw);
+  const uint32_t ring_s = base;                     // NST x TILE (first: see attn_fwd_kernel.cuh)
+  const uint32_t q_s = ring_s + C::NST * C::TILE;   // NQB x (Q0, Q1)
+  const uint32_t bar_s = q_s + C::NQB * C::QPAIR;   // NBAR x 8
+  uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + (bar_s - base) + 8 * C::NBAR);
+  volatile uint32_t *const abort_flag = tmem_slot + 1;
+  auto BAR = [&](int i) -> uint32_t { return bar_s + 8u * static_cast<uint32_t>(i); };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(BAR(C::B_QFULL + i), 1);
+      mbar_init(BAR(C::B_QEMPTY + i), 2);
+      mbar_init(BAR(C::B_SFULL + i), 1);
+      mbar_init(BAR(C::B_PFULL + i), 128);
+      mbar_init(BAR(C::B_OFINAL + i), 1);
+      mbar_init(BAR(C::B_OFREE + i), 128);
+      mbar_init(BAR(C::B_EPI + i), 128);
+    }
+    for (int i = 0; i < C::NST; ++i) {
+      mbar_init(BAR(C::B_FULL + i), 1);
+      mbar_init(BAR(C::B_EMPTY + i), 1);
+    }
+    mbar_init(BAR(C::B_DRAIN), 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // Register split: the launch gives every thread kLaunchRegs; the producer/MMA warpgroup
+  // (warps 0-3) gives up registers that the two softmax warpgroups take:
+  // 128 * kRegsLow + 256 * kRegsHigh <= 384 * kLaunchRegs.
+  static_assert(128 * PPCfg<D>::kRegsLow + 256 * PPCfg<D>::kRegsHigh <= 384 * PPCfg<D>::kLaunchRegs,
+                "register split exceeds the launch allocation");
+  if (warp < 4) {
+    setmaxnreg_dec<PPCfg<D>::kRegsLow>();
+    if (warp == 0 && lane == 0) {
+      PPProducer<D, CAUSAL> pr;
+      pr.tq = &tm_q;
+      pr.tk = &tm_k;
+      pr.tv = &tm_v;
+      pr.p = &p;
+      pr.ring_s = ring_s;
+      pr.q_s = q_s;
+      pr.bar_s = bar_s;
+      pr.abort_flag = abort_flag;
+      pr.pol = policy_evict_last();
+      run_pp_stream<CAUSAL>(p, pr);
+      // Drain: every load issued must have landed before the CTA may exit.
+      const uint32_t first = pr.it > static_cast<uint32_t>(C::NST) ? pr.it - C::NST : 0u;
+      for (uint32_t i = first; i < pr.it; ++i)
+        wait_drain(BAR(C::B_FULL + (i % C::NST)), (i / C::NST) & 1u, p.wait_limit);
+      for (int i = (pr.q_loads > 2 ? pr.q_loads - 2 : 0); i < pr.q_loads; ++i)
+        wait_drain(BAR(C::B_QFULL + (i & 1)), (i >> 1) & 1, p.wait_limit);
+    } else if (warp == 1 && lane == 0) {
+      PPIssuer<D, CAUSAL> is;
+      is.p = &p;
+      is.ring_s = ring_s;
+      is.q_s = q_s;
+      is.bar_s = bar_s;
+      is.tmem = tmem;
+      is.abort_flag = abort_flag;
+      run_pp_stream<CAUSAL>(p, is);
+      umma_commit(BAR(C::B_DRAIN));
+      wait_drain(BAR(C::B_DRAIN), 0, p.wait_limit);
+    }
+    __syncwarp();
+  } else {
+    setmaxnreg_inc<PPCfg<D>::kRegsHigh>();
+    // ================================================= softmax + epilogue of one Q tile
+    const int slot = (warp - 4) >> 2;  // warps 4-7: Q0, warps 8-11: Q1
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t s_tmem = tmem + lane_base + slot * 128u;
+    const uint32_t o_tmem = tmem + lane_base + C::O_COL + slot * D;
+    const float c2 = p.c2;
+    const long long LIM = p.wait_limit;
+    Sched sc(blockIdx.x, gridDim.x, p.n_items);
+    uint32_t g = 0;  // S tiles of this slot so far
+    int il = 0, r;
+    bool ok = true;
+    auto wait_warp = [&](uint32_t b, uint32_t ph) -> bool {
+      const bool w = wait_bounded(b, ph, abort_flag, p.status, kDevTimeoutSoftmax, LIM);
+      return __all_sync(0xffffffffu, w);
+    };
+    while (ok && sc.next(r)) {
+      const PPItem item = pp_decode<CAUSAL>(r, p);
+      const int n = slot == 0 ? item.n0 : item.n1;
+      const int qrow0 = item.qb * 256 + slot * 128;  // first query row of this tile
+      const int diag = 2 * item.qb + slot;           // causal: the key tile holding the diagonal
+      float m_used = 0.f, l = 0.f;
+      for (int j = 0; j < n; ++j, ++g) {
+        if (!(ok = wait_warp(BAR(C::B_SFULL + slot), g & 1u))) break;
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld32x128(s_tmem, sr);
+        float *s = reinterpret_cast<float *>(sr);
+        if (CAUSAL) {
+          if (j == diag) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c > row) s[c] = -INFINITY;
+          }
+        } else {
+          const int lim = p.L - j * 128;
+          if (lim < 128) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c >= lim) s[c] = -INFINITY;
+          }
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        const float m_tile = mx * c2;
+        if (j == 0) {
+          m_used = (m_tile == -INFINITY) ? 0.f : m_tile;
+        } else if (__any_sync(0xffffffffu, m_tile > m_used + 8.0f)) {
+          // PV of the previous tile is complete (it precedes this QK in the issue order).
+          const float m_new = fmaxf(m_used, m_tile);
+          const float alpha = ex2_approx(m_used - m_new);
+          m_used = m_new;
+          l *= alpha;
+#pragma unroll 1
+          for (int c32 = 0; c32 < D / 32; ++c32) {
+            uint32_t orr[32];
+            tmem_ld32x32(o_tmem + c32 * 32, orr);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+            tmem_st32x32(o_tmem + c32 * 32, orr);
+          }
+        }
+        const float neg = -m_used;
+        float sum = 0.f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float p0 = ex2_approx(fmaf(s[2 * c], c2, neg));
+          const float p1 = ex2_approx(fmaf(s[2 * c + 1], c2, neg));
+          sum += p0 + p1;
+          pk[c] = pack_f16x2(p0, p1);
+        }
+        l += sum;
+        tmem_st32x64(s_tmem, pk);
+        tc_fence_before();
+        mbar_arrive(BAR(C::B_PFULL + slot));
+      }
+      if (!ok) break;
+      // --------------------------------------------------------------- epilogue
+      if (!(ok = wait_warp(BAR(C::B_OFINAL + slot), il & 1))) break;
+      tc_fence_after();
+      const uint32_t stage = q_s + (il & 1) * C::QPAIR + slot * C::TILE;  // this tile's Q, no longer read
+      const float inv_l = 1.0f / l;
+#pragma unroll 1
+      for (int c32 = 0; c32 < D / 32; ++c32) {
+        uint32_t orr[32];
+        tmem_ld32x32(o_tmem + c32 * 32, orr);
+        uint32_t h[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          h[i] = pack_f16x2(__uint_as_float(orr[2 * i]) * inv_l, __uint_as_float(orr[2 * i + 1]) * inv_l);
+        const uint32_t rowaddr = stage + (c32 >> 1) * C::CHUNK + row * 128;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int chunk = (c32 & 1) * 4 + q4;
+          st_shared_v4(rowaddr + ((chunk ^ (row & 7)) << 4), h[4 * q4], h[4 * q4 + 1], h[4 * q4 + 2],
+                       h[4 * q4 + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(BAR(C::B_OFREE + slot));
+      const int grow = qrow0 + row;
+      if (grow < p.L)
+        p.lse[static_cast<long long>(item.bh) * p.L + grow] = (m_used + __log2f(l)) * 0.69314718055994531f;
+      fence_proxy_async_smem();
+      mbar_arrive(BAR(C::B_EPI + slot));
+      if (quarter == 0 && lane == 0) {
+        if (wait_bounded(BAR(C::B_EPI + slot), il & 1, abort_flag, p.status, kDevTimeoutEpilogue, LIM)) {
+          if (qrow0 < p.L) {
+            for (int c = 0; c < C::NCH; ++c) tma_store_3d(&tm_o, stage + c * C::CHUNK, c * 64, qrow0, item.bh);
+            bulk_commit();
+            bulk_wait_read0();
+          }
+          mbar_arrive(BAR(C::B_QEMPTY + (il & 1)));
+        }
+      }
+      __syncwarp();
+      ++il;
+    }
+    if (quarter == 0 && lane == 0) bulk_wait0();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_pp_variant(const FwdLaunch &a) {
+  using C = PPCfg<D>;
+  auto *kern = attn_fwd_pp_kernel<D, CAUSAL>;
+  static int configured_mask = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 31 || !(configured_mask & (1 << dev))) {
+    // The warpgroup register split assumes the kernel is launched with kLaunchRegs
+    // registers per thread; with fewer, setmaxnreg.inc could never be satisfied.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < C::kLaunchRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev < 31) configured_mask |= (1 << dev);
+  }
+  kern<<<a.grid, 384, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fwd_pp_d(const FwdLaunch &a) {
+  return a.causal ? launch_fwd_pp_variant<D, true>(a) : launch_fwd_pp_variant<D, false>(a);
+}
+
+cudaError_t launch_fwd_pp_64(const FwdLaunch &a);
+cudaError_t launch_fwd_pp_128(const FwdLaunch &a);
+
+}  // namespace gbattn

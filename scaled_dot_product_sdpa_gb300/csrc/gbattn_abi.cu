@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "attn_fwd_kernel.cuh"
+#include "attn_fwd_pp.cuh"
 #include "gbattn.h"
 
 namespace gbattn {
@@ -118,6 +119,10 @@ extern "C" int attn_fwd_ex(const void *q, const void *k, const void *v, void *o,
   if (!std::isfinite(scale) || !(scale > 0.f)) return GBATTN_ERR_SCALE;
   const bool p_smem = (flags & GBATTN_FLAG_P_SMEM) != 0;
   if (p_smem && d > 128) return GBATTN_ERR_HEAD_DIM;
+  if (flags & ~(GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE)) return GBATTN_ERR_FLAGS;
+  // Two 128-row query tiles per item (ping-pong kernel) for d <= 128 unless a
+  // single-tile option is asked for.
+  const bool two_tile = d <= 128 && !p_smem && !(flags & GBATTN_FLAG_SINGLE_TILE);
   if (grid_limit < 0) return GBATTN_ERR_DIMS;
   const long long rows = static_cast<long long>(B) * H * L;
   const size_t tbytes = static_cast<size_t>(rows) * static_cast<size_t>(d) * 2u;
@@ -132,8 +137,9 @@ extern "C" int attn_fwd_ex(const void *q, const void *k, const void *v, void *o,
 
   const int BH = B * H;
   const int nQ = (L + 127) / 128;
+  const int nQB = (L + 255) / 256;
   const int dvs = d > 256 ? d / 256 : 1;
-  const long long n_items = static_cast<long long>(BH) * nQ * dvs;
+  const long long n_items = two_tile ? static_cast<long long>(BH) * nQB : static_cast<long long>(BH) * nQ * dvs;
   if (n_items > INT_MAX) return GBATTN_ERR_DIMS;
 
   FwdLaunch a;
@@ -153,10 +159,15 @@ extern "C" int attn_fwd_ex(const void *q, const void *k, const void *v, void *o,
   a.p.BH = BH;
   a.p.L = L;
   a.p.nQ = nQ;
+  a.p.nQB = nQB;
   a.p.n_items = static_cast<int>(n_items);
   a.p.c2 = scale * 1.4426950408889634f;
 
   cudaError_t e;
+  if (two_tile) {
+    e = d == 64 ? launch_fwd_pp_64(a) : launch_fwd_pp_128(a);
+    return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_LAUNCH;
+  }
   switch (d) {
     case 64: e = launch_fwd_64(a); break;
     case 128: e = launch_fwd_128(a); break;
@@ -227,6 +238,7 @@ extern "C" const char *attn_strerror(int code) {
     case GBATTN_ERR_SCALE: return "scale must be finite and > 0";
     case GBATTN_ERR_ALIAS: return "an output overlaps an input or the other output";
     case GBATTN_ERR_TENSORMAP: return "the driver rejected a TMA tensor-map descriptor";
+    case GBATTN_ERR_FLAGS: return "flags holds bits that name no option";
     case GBATTN_DEV_TIMEOUT_LOAD: return "device: the TMA producer's wait timed out";
     case GBATTN_DEV_TIMEOUT_MMA: return "device: the MMA issuer's wait timed out";
     case GBATTN_DEV_TIMEOUT_SOFTMAX: return "device: a softmax warp's wait timed out";

@@ -168,6 +168,17 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
                : "memory");
 }
 
+// ----------------------------------------------------------------------------- registers
+// Warpgroup-wide register re-allocation (every thread of the 4 warps executes it).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ----------------------------------------------------------------------------- math
 // 2^x on the special-function unit (flush-to-zero; 2^-inf = +0).
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -97,6 +97,17 @@ def test_fwd_small_matches_oracle(L, d, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("L,d", [(L, d) for d in (64, 128) for L in (1, 129, 200, 256, 384, 640)])
+def test_fwd_single_tile_kernel_matches_oracle(L, d, causal):
+    """The single-tile kernel (one 128-row query tile per item) for d <= 128."""
+    q, k, v = inputs.qkv(2, 3, L, d, seed=11 * L + d + int(causal))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(*_dev(q, k, v), causal, scale, flags=gb.FLAG_SINGLE_TILE)
+    o_ref, lse_ref = oracle.sdpa_fwd(q, k, v, causal, float(np.float32(scale)))
+    _check(o, lse, o_ref, lse_ref, f"single-tile L={L} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 @pytest.mark.parametrize("L,d", [(200, 64), (384, 64), (129, 128), (384, 128)])
 def test_fwd_smem_p_variant_matches_oracle(L, d, causal):
     """P staged through shared memory instead of tensor memory: same results."""
@@ -107,30 +118,34 @@ def test_fwd_smem_p_variant_matches_oracle(L, d, causal):
     _check(o, lse, o_ref, lse_ref, "smem-P")
 
 
+@pytest.mark.parametrize("flags", [0, 2], ids=["default", "single_tile"])
 @pytest.mark.parametrize("grid", [1, 2, 3, 7])
 @pytest.mark.parametrize("d", [64, 128, 512])
-def test_fwd_persistent_loop_with_few_ctas(grid, d):
+def test_fwd_persistent_loop_with_few_ctas(grid, d, flags):
     """Few CTAs => many items per CTA: exercises the cross-item pipeline and the phase
     bookkeeping of every barrier over long runs."""
+    if d > 128 and flags:
+        pytest.skip("head_dim 512 has only the single-tile kernel")
     L = 640 if d < 512 else 384
     q, k, v = inputs.qkv(1, 3, L, d, seed=grid * 100 + d, sigma=0.5 if d == 512 else 1.0)
     scale = 1.0 / math.sqrt(d)
     for causal in (False, True):
-        o, lse = _run(*_dev(q, k, v), causal, scale, grid_limit=grid)
+        o, lse = _run(*_dev(q, k, v), causal, scale, grid_limit=grid, flags=flags)
         o_ref, lse_ref = oracle.sdpa_fwd(q, k, v, causal, float(np.float32(scale)))
         _check(o, lse, o_ref, lse_ref, f"grid={grid} causal={causal}")
 
 
-def test_fwd_large_logits_force_rescale():
+@pytest.mark.parametrize("d,flags", [(64, 0), (64, 2), (128, 0), (128, 2), (512, 0)])
+def test_fwd_large_logits_force_rescale(d, flags):
     """Keys whose logits grow along the sequence force the lazy O rescale path."""
-    B, H, L, d = 1, 2, 512, 64
+    B, H, L = 1, 2, 512
     q, k, v = inputs.qkv(B, H, L, d, seed=77)
     q = q.abs()  # every q_i . 1 > 0, so logits grow with the ramp added to every key
-    ramp = torch.linspace(0, 6, L).view(1, 1, L, 1)
+    ramp = torch.linspace(0, 6 * math.sqrt(64 / d), L).view(1, 1, L, 1)
     k = (k.float() * 0.2 + ramp).half()
     scale = 1.0 / math.sqrt(d)
     for causal in (False, True):
-        o, lse = _run(*_dev(q, k, v), causal, scale)
+        o, lse = _run(*_dev(q, k, v), causal, scale, flags=flags)
         o_ref, lse_ref = oracle.sdpa_fwd(q, k, v, causal, float(np.float32(scale)))
         _check(o, lse, o_ref, lse_ref, "rescale")
 
