@@ -69,19 +69,24 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
 
 /*
  * attn_fwd_ex -- attn_fwd with design options (same arguments, same errors, plus
- * GBATTN_ERR_FLAGS for unknown flag bits).  For d <= 128 attn_fwd runs the two-tile
- * kernel: each work item is a 256-row query block whose two 128-row halves share every
- * K/V tile and have their own softmax warpgroup.  The options select the single-tile
- * kernel (one 128-row query tile per item, the only kernel for d = 256 and 512):
+ * GBATTN_ERR_FLAGS for unknown or conflicting flag bits).  Two kernels exist:
+ *   two-tile kernel (d <= 128 only): each work item is a 256-row query block whose two
+ *     128-row halves share every K/V tile and have their own softmax warpgroup;
+ *   single-tile kernel (every d): each work item is one 128-row query tile.
+ * With flags = 0, attn_fwd picks the two-tile kernel for d <= 128 when it has at least
+ * two items per SM, else the single-tile kernel.  Options:
  *   flags bit 0 (GBATTN_FLAG_P_SMEM): single-tile kernel, with P staged through shared
  *     memory instead of tensor memory before the PV product (the SMEM-P path of the
  *     STAGE_D.md notes, section 4); only for d <= 128, otherwise GBATTN_ERR_HEAD_DIM.
  *   flags bit 1 (GBATTN_FLAG_SINGLE_TILE): single-tile kernel, P in tensor memory.
+ *   flags bit 2 (GBATTN_FLAG_TWO_TILE): two-tile kernel whatever the item count; only for
+ *     d <= 128 (else GBATTN_ERR_HEAD_DIM) and not with bits 0 or 1 (GBATTN_ERR_FLAGS).
  *   grid_limit: 0 = one persistent CTA per SM; n > 0 = at most n CTAs (scheduler tests).
  * Every option gives the same results up to rounding.
  */
 #define GBATTN_FLAG_P_SMEM 1
 #define GBATTN_FLAG_SINGLE_TILE 2
+#define GBATTN_FLAG_TWO_TILE 4
 int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                 int H, int L, int d, int causal, float scale, void *stream, int flags,
                 int grid_limit);
@@ -112,6 +117,17 @@ int attn_last_device_error(void);
  * that runs out turns into a status the host can read.
  */
 int attn_debug_wait_probe(long long limit_cycles, void *stream);
+
+/*
+ * attn_debug_schedule -- test hook: the static work schedule attn_fwd_ex would use for
+ * this shape, `grid` CTAs and `flags`.  Returns the number of work items n and fills
+ * start[0..grid] (CTA c runs items[start[c] .. start[c+1]) in order) and items[0..n), or
+ * returns 0 when the problem is too large for a table (the kernels then use a fixed
+ * snake order), or a negative GBATTN_ERR_* code (GBATTN_ERR_DIMS if n > max_items).
+ * Host-only; needs no GPU.  Not thread-safe.
+ */
+int attn_debug_schedule(int B, int H, int L, int d, int causal, int grid, int flags, int *start, int *items,
+                        int max_items);
 
 /* Human-readable text for a GBATTN_ERR_* or GBATTN_DEV_* code (static storage). */
 const char *attn_strerror(int code);

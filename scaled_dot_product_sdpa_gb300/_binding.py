@@ -19,6 +19,7 @@ _lib = None
 
 FLAG_P_SMEM = 1
 FLAG_SINGLE_TILE = 2
+FLAG_TWO_TILE = 4
 
 
 class GbattnError(RuntimeError):
@@ -50,6 +51,9 @@ def load_library(path: str | None = None):
     lib.attn_debug_wait_probe.restype = i
     lib.attn_strerror.argtypes = [i]
     lib.attn_strerror.restype = ctypes.c_char_p
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.attn_debug_schedule.argtypes = [i, i, i, i, i, i, i, ip, ip, i]
+    lib.attn_debug_schedule.restype = i
     lib.attn_version.argtypes = []
     lib.attn_version.restype = i
     _lib = lib
@@ -134,3 +138,17 @@ def attn_debug_wait_probe(limit_cycles: int, stream=None) -> None:
     rc = load_library().attn_debug_wait_probe(int(limit_cycles), _stream_handle(stream))
     if rc != 0:
         raise GbattnError(rc, "attn_debug_wait_probe")
+
+
+def attn_debug_schedule(B: int, H: int, L: int, d: int, causal: bool, grid: int, flags: int = 0):
+    """The static work schedule attn_fwd would use (host-only): a list with, per CTA, the
+    work-item indices it runs in order; None when the kernels use their fixed order."""
+    max_items = 1 << 16
+    start = (ctypes.c_int * (grid + 1))()
+    items = (ctypes.c_int * max_items)()
+    n = load_library().attn_debug_schedule(B, H, L, d, int(bool(causal)), grid, flags, start, items, max_items)
+    if n < 0:
+        raise GbattnError(n, "attn_debug_schedule")
+    if n == 0:
+        return None
+    return [list(items[start[c]:start[c + 1]]) for c in range(grid)]

@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
+#include "softmax_tile.cuh"
 
 namespace gbattn {
 
@@ -43,6 +44,7 @@ constexpr unsigned kDevTimeoutEpilogue = 4;
 constexpr unsigned kDevTimeoutProbe = 5;
 
 struct FwdParams {
+  void *o;                 // [BH, L, D] fp16 (written directly by the two-tile kernel)
   float *lse;              // [BH, L] fp32
   unsigned *status;        // device status word (first error code wins)
   long long wait_limit;    // SM clock cycles a single wait may take before it gives up
@@ -89,13 +91,35 @@ struct FwdCfg {
   static_assert(NCH % SC == 0 && NCHV % SC == 0, "stage split");
 };
 
-// Snake-order static schedule: pass p hands items [p*G, p*G+G) to CTAs 0..G-1, reversed
-// on odd passes, so the longest items (first in the order) are spread over all CTAs and
-// each CTA's total is balanced.
+// Static schedule.  With a table (n > 0), CTA c processes items[start[c] .. start[c+1]):
+// the host fills it by longest-processing-time-first assignment of item costs (work units
+// plus a per-item overhead).  It travels in the kernel parameters, so no device memory is
+// involved.  Without a table (problems with more items than it holds), a snake order:
+// pass p hands items [p*G, p*G+G) to CTAs 0..G-1, reversed on odd passes.
+constexpr int kSchedMaxCtas = 256;
+constexpr int kSchedMaxItems = 3072;
+struct SchedTable {
+  int n;  // items in the table; 0 = snake order
+  uint16_t start[kSchedMaxCtas + 1];
+  uint16_t items[kSchedMaxItems];
+};
+
 struct Sched {
   int cta, G, NI, pass, npass;
-  __device__ Sched(int c, int g, int ni) : cta(c), G(g), NI(ni), pass(0), npass((ni + g - 1) / g) {}
+  const SchedTable *tbl;
+  __device__ Sched(int c, int g, int ni, const SchedTable *t)
+      : cta(c), G(g), NI(ni), pass(0), npass((ni + g - 1) / g), tbl(t) {
+    if (tbl->n > 0) {
+      pass = tbl->start[c];
+      npass = tbl->start[c + 1];
+    }
+  }
   __device__ bool next(int &item) {
+    if (tbl->n > 0) {
+      if (pass >= npass) return false;
+      item = tbl->items[pass++];
+      return true;
+    }
     while (pass < npass) {
       const int p = pass++;
       const int r = p * G + ((p & 1) ? (G - 1 - cta) : cta);
@@ -148,7 +172,7 @@ template <int D, bool CAUSAL, bool P_TMEM>
 __global__ void __launch_bounds__(256, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                    const FwdParams p) {
+                    const FwdParams p, const __grid_constant__ SchedTable tbl) {
   using C = FwdCfg<D, P_TMEM>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -203,7 +227,7 @@ __global__ void __launch_bounds__(256, 1)
   if (warp == 0) {
     // =============================================================== TMA producer
     if (lane == 0) {
-      Sched sc(blockIdx.x, gridDim.x, p.n_items);
+      Sched sc(blockIdx.x, gridDim.x, p.n_items, &tbl);
       uint32_t it = 0;
       int il = 0, item;
       bool ok = true, have_v = false;
@@ -262,7 +286,7 @@ __global__ void __launch_bounds__(256, 1)
   } else if (warp == 1) {
     // =============================================================== MMA issuer
     if (lane == 0) {
-      Sched sc(blockIdx.x, gridDim.x, p.n_items);
+      Sched sc(blockIdx.x, gridDim.x, p.n_items, &tbl);
       uint32_t it = 0, g = 0;
       int il = 0, item;
       bool ok = true, have_pv = false;
@@ -278,15 +302,15 @@ __global__ void __launch_bounds__(256, 1)
           const uint32_t s = it % C::NST;
           if (!wait(BAR(C::B_FULL + s), (it / C::NST) & 1u)) return false;
           tc_fence_after();
+          const SDesc a = sdesc_split(sdesc_sw128(q_s + qb * C::QBYTES + ks * C::STAGE, 16, 1024));
+          const SDesc b = sdesc_split(sdesc_sw128(ring_s + s * C::STAGE, 16, 1024));
 #pragma unroll
           for (int j = 0; j < C::SC; ++j) {
             const int cidx = ks * C::SC + j;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = sdesc_sw128(q_s + qb * C::QBYTES + cidx * C::CHUNK + kk * 32, 16, 1024);
-              const uint64_t b = sdesc_sw128(ring_s + s * C::STAGE + j * C::CHUNK + kk * 32, 16, 1024);
-              umma_ss(d_tmem, a, b, C::IDESC_QK, (cidx | kk) != 0 ? 1u : 0u);
-            }
+            for (int kk = 0; kk < 4; ++kk)
+              umma_ss_off(d_tmem, a, j * C::CHUNK + kk * 32, b, j * C::CHUNK + kk * 32, C::IDESC_QK,
+                          (cidx | kk) != 0 ? 1u : 0u);
           }
           umma_commit(BAR(C::B_EMPTY + s));
           ++it;
@@ -304,16 +328,15 @@ __global__ void __launch_bounds__(256, 1)
           if (!wait(BAR(C::B_FULL + s), (it / C::NST) & 1u)) return false;
           tc_fence_after();
           const uint32_t o_tmem = tmem + C::O_COL + vs * C::SC * 64;
+          const SDesc b = sdesc_split(sdesc_sw128(ring_s + s * C::STAGE, C::CHUNK, 1024));
+          const SDesc a = sdesc_split(sdesc_sw128(p_s + sb * C::PBYTES, 16, 1024));
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t b = sdesc_sw128(ring_s + s * C::STAGE + kk * 2048, C::CHUNK, 1024);
             const uint32_t acc = (pv_first && kk == 0) ? 0u : 1u;
             if constexpr (P_TMEM) {
-              umma_ts(o_tmem, tmem + sb * 128u + kk * 8u, b, C::IDESC_PV, acc);
+              umma_ts_off(o_tmem, tmem + sb * 128u + kk * 8u, b, kk * 2048, C::IDESC_PV, acc);
             } else {
-              const uint64_t a =
-                  sdesc_sw128(p_s + sb * C::PBYTES + (kk >> 2) * C::CHUNK + (kk & 3) * 32, 16, 1024);
-              umma_ss(o_tmem, a, b, C::IDESC_PV, acc);
+              umma_ss_off(o_tmem, a, (kk >> 2) * C::CHUNK + (kk & 3) * 32, b, kk * 2048, C::IDESC_PV, acc);
             }
           }
           umma_commit(BAR(C::B_EMPTY + s));
@@ -355,7 +378,7 @@ __global__ void __launch_bounds__(256, 1)
     const int row = quarter * 32 + lane;  // query row within the tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const float c2 = p.c2;
-    Sched sc(blockIdx.x, gridDim.x, p.n_items);
+    Sched sc(blockIdx.x, gridDim.x, p.n_items, &tbl);
     uint32_t g = 0;
     int il = 0, item;
     bool ok = true;
@@ -371,64 +394,27 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t sb = g & 1u;
         if (!(ok = wait_warp(BAR(C::B_SFULL + sb), (g >> 1) & 1u))) break;
         tc_fence_after();
-        uint32_t sr[128];
-        tmem_ld32x128(tmem + lane_base + sb * 128u, sr);
-        float *s = reinterpret_cast<float *>(sr);
-        if (CAUSAL) {
-          if (t == qt) {
-#pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (c > row) s[c] = -INFINITY;
-          }
-        } else {
-          const int lim = p.L - t * C::BN;
-          if (lim < C::BN) {
-#pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (c >= lim) s[c] = -INFINITY;
-          }
-        }
-        float mx = s[0];
-#pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-        float m_tile = mx * c2;
-        if (t == 0) {
-          m_used = (m_tile == -INFINITY) ? 0.f : m_tile;
-        } else {
-          // PV of the previous key tile must be complete before O may be rescaled.
-          if (!(ok = wait_warp(BAR(C::B_ODONE), (g - 1) & 1u))) break;
+        const int lim = CAUSAL ? (t == qt ? row + 1 : 128) : min(128, p.L - t * C::BN);
+        // PV of the previous key tile must be complete before O may be rescaled: wait for
+        // it once the tile maximum is known (every tile but the first, to keep the
+        // barrier's phases in step).
+        auto wait_prev_pv = [&]() -> bool {
+          if (!wait_warp(BAR(C::B_ODONE), (g - 1) & 1u)) return false;
           tc_fence_after();
-          const bool need = m_tile > m_used + 8.0f;
-          if (__any_sync(0xffffffffu, need)) {
-            const float m_new = fmaxf(m_used, m_tile);
-            const float alpha = ex2_approx(m_used - m_new);
-            m_used = m_new;
-            l *= alpha;
-#pragma unroll 1
-            for (int c32 = 0; c32 < C::DV / 32; ++c32) {
-              uint32_t orr[32];
-              const uint32_t ta = tmem + lane_base + C::O_COL + c32 * 32;
-              tmem_ld32x32(ta, orr);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-              tmem_st32x32(ta, orr);
-            }
-          }
-        }
-        const float neg = -m_used;
-        float sum = 0.f;
-        uint32_t pk[64];
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float p0 = ex2_approx(fmaf(s[2 * c], c2, neg));
-          const float p1 = ex2_approx(fmaf(s[2 * c + 1], c2, neg));
-          sum += p0 + p1;
-          pk[c] = pack_f16x2(p0, p1);
-        }
-        l += sum;
+          return true;
+        };
         if constexpr (P_TMEM) {
-          tmem_st32x64(tmem + lane_base + sb * 128u, pk);
+          if (!(ok = softmax_tile<C::DV>(tmem + lane_base + sb * 128u, tmem + lane_base + C::O_COL, lim, c2, t == 0,
+                                         m_used, l, wait_prev_pv)))
+            break;
         } else {
+          // P through shared memory: run the step into tensor memory, then move the fp16
+          // P from the S columns into the swizzled shared-memory operand tile.
+          if (!(ok = softmax_tile<C::DV>(tmem + lane_base + sb * 128u, tmem + lane_base + C::O_COL, lim, c2, t == 0,
+                                         m_used, l, wait_prev_pv)))
+            break;
+          uint32_t pk[64];
+          tmem_ld32x64(tmem + lane_base + sb * 128u, pk);
           const uint32_t pb = p_s + sb * C::PBYTES + row * 128;
 #pragma unroll
           for (int ch = 0; ch < 16; ++ch) {
@@ -498,6 +484,7 @@ __global__ void __launch_bounds__(256, 1)
 struct FwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_o;
   FwdParams p;
+  const SchedTable *tbl;
   int grid;
   bool causal;
   bool p_smem;
@@ -517,7 +504,7 @@ cudaError_t launch_fwd_variant(const FwdLaunch &a) {
     if (e != cudaSuccess) return e;
     if (dev < 31) configured_mask |= (1 << dev);
   }
-  kern<<<a.grid, 256, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
+  kern<<<a.grid, 256, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p, *a.tbl);
   return cudaGetLastError();
 }
 

@@ -1,4 +1,4 @@
-// attn_fwd_pp.cuh -- ping-pong SDPA forward for head_dim 64 and 128 on sm_103a.
+// attn_fwd_pp.cuh -- two-tile ("ping-pong") SDPA forward for head_dim 64 and 128 on sm_103a.
 //
 // Same mathematics as attn_fwd_kernel.cuh ("An Optimal Mapper Meets a Real GPU",
 // "Ground rules" / "Experiment one"): O = softmax(scale * Q K^T + causal mask) V and the
@@ -18,13 +18,21 @@
 // Under the causal mask Q0 needs key tiles 0..2qb and Q1 needs 0..2qb+1; the last one
 // is run for Q1 alone.
 //
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
-// warps 4-7 softmax + epilogue of Q0, warps 8-11 softmax + epilogue of Q1, warps 2-3 idle.
-// Producer and MMA issuer walk the same operation stream (run_pp_stream), so the
-// producer loads each K or V tile into the ring in the order of its first use.
+// Warp roles (384 threads):
+//   warp 0      K/V producer: walks the same operation stream as the MMA issuer
+//               (run_pp_stream) and loads each K or V tile into the ring at its first use.
+//   warp 1      TMEM owner + MMA issuer.
+//   warp 2      Q loader: each slot has two Q buffers, so the next item's Q tiles arrive
+//               while the current item runs; the K/V stream never waits for them.
+//   warp 3      O store issuer: TMA-stores each finished O tile from its staging buffer
+//               and then frees that Q buffer.
+//   warps 4-7   softmax + epilogue of Q0;  warps 8-11  softmax + epilogue of Q1.
+// The epilogue writes O / l as fp16 into the item's own Q buffer (no longer read once the
+// slot's last QK has completed) in the 128-byte-swizzled layout the TMA store reads.
 #pragma once
 
 #include "attn_fwd_kernel.cuh"
+#include "softmax_tile.cuh"
 
 namespace gbattn {
 
@@ -33,16 +41,18 @@ struct PPCfg {
   static constexpr int NCH = D / 64;
   static constexpr int CHUNK = 128 * 128;            // bytes of a 128-row x 64-col fp16 box
   static constexpr int TILE = NCH * CHUNK;           // one 128 x D tile
-  static constexpr int NQB = 2;                      // Q pairs (items) in flight
-  static constexpr int QPAIR = 2 * TILE;
   static constexpr int TILE_BUDGET = 224 * 1024;
-  static constexpr int NST_FIT = (TILE_BUDGET - NQB * QPAIR) / TILE;
-  static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
-  static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_FULL = 4, B_EMPTY = 4 + NST;
-  static constexpr int B_SFULL = 4 + 2 * NST, B_PFULL = B_SFULL + 2, B_OFINAL = B_PFULL + 2;
-  static constexpr int B_OFREE = B_OFINAL + 2, B_EPI = B_OFREE + 2, B_DRAIN = B_EPI + 2;
+  static constexpr int NQBUF = 4;                    // Q buffers: 2 slots x 2 items
+  static constexpr int NST_FIT = (TILE_BUDGET - NQBUF * TILE) / TILE;
+  static constexpr int NST = NST_FIT > 12 ? 12 : NST_FIT;
+  // barrier indices (per slot a and buffer b: index a * 2 + b)
+  static constexpr int B_QFULL = 0, B_QEMPTY = 4, B_FULL = 8, B_EMPTY = 8 + NST;
+  static constexpr int B_SFULL = 8 + 2 * NST, B_PFULL = B_SFULL + 2, B_OFINAL = B_PFULL + 2;
+  // EPI is per (slot, Q buffer): an epilogue can only finish into a buffer after the store
+  // of that buffer's previous tile freed it, so its phases cannot run ahead of the issuer.
+  static constexpr int B_OFREE = B_OFINAL + 2, B_EPI = B_OFREE + 2, B_DRAIN = B_EPI + 4;
   static constexpr int NBAR = B_DRAIN + 1;
-  static constexpr int TILE_BYTES = NST * TILE + NQB * QPAIR;
+  static constexpr int TILE_BYTES = NST * TILE + NQBUF * TILE;
   static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + 8 * NBAR + 16;
   static constexpr int O_COL = 256;
   static constexpr int TMEM_COLS = 512;
@@ -77,8 +87,8 @@ __device__ __forceinline__ PPItem pp_decode(int r, const FwdParams &p) {
 // Walk this CTA's operation stream, calling v.qk(slot, j, il, item) and
 // v.pv(slot, j, il, item) in issue order.  Returns false as soon as a visitor does.
 template <bool CAUSAL, class Visitor>
-__device__ __forceinline__ bool run_pp_stream(const FwdParams &p, Visitor &v) {
-  Sched sc(blockIdx.x, gridDim.x, p.n_items);
+__device__ __forceinline__ bool run_pp_stream(const FwdParams &p, const SchedTable *tbl, Visitor &v) {
+  Sched sc(blockIdx.x, gridDim.x, p.n_items, tbl);
   int r;
   if (!sc.next(r)) return true;
   PPItem cur = pp_decode<CAUSAL>(r, p);
@@ -124,16 +134,20 @@ __device__ __forceinline__ bool pp_first_use(int slot, int j, const PPItem &it) 
   return slot == 0 || j >= it.n0;
 }
 
+template <int D>
+__device__ __forceinline__ uint32_t pp_q_tile(uint32_t q_s, int slot, int il) {
+  return q_s + static_cast<uint32_t>(slot * 2 + (il & 1)) * PPCfg<D>::TILE;
+}
+
 template <int D, bool CAUSAL>
-struct PPProducer {
+struct PPProducer {  // K/V only
   using C = PPCfg<D>;
-  const CUtensorMap *tq, *tk, *tv;
+  const CUtensorMap *tk, *tv;
   const FwdParams *p;
-  uint32_t ring_s, q_s, bar_s;
+  uint32_t ring_s, bar_s;
   volatile uint32_t *abort_flag;
   uint32_t it = 0;  // ring positions issued
-  int q_loads = 0;
-  uint64_t pol;
+  uint64_t pol_kv;
   __device__ uint32_t bar(int i) const { return bar_s + 8u * static_cast<uint32_t>(i); }
   __device__ bool load_tile(const CUtensorMap *tm, int j, int bh) {
     const uint32_t s = it % C::NST, ph = (it / C::NST) & 1u;
@@ -142,26 +156,14 @@ struct PPProducer {
     mbar_arrive_expect_tx(bar(C::B_FULL + s), C::TILE);
 #pragma unroll
     for (int c = 0; c < C::NCH; ++c)
-      tma_load_3d_hint(ring_s + s * C::TILE + c * C::CHUNK, tm, c * 64, j * 128, bh, bar(C::B_FULL + s), pol);
+      tma_load_3d_hint(ring_s + s * C::TILE + c * C::CHUNK, tm, c * 64, j * 128, bh, bar(C::B_FULL + s), pol_kv);
     ++it;
     return true;
   }
-  __device__ bool qk(int slot, int j, int il, const PPItem &item) {
-    if (slot == 0 && j == 0) {  // first operation of an item: bring its two Q tiles
-      const int b = il & 1;
-      if (!wait_bounded(bar(C::B_QEMPTY + b), ((il >> 1) & 1) ^ 1u, abort_flag, p->status, kDevTimeoutLoad,
-                        p->wait_limit))
-        return false;
-      mbar_arrive_expect_tx(bar(C::B_QFULL + b), C::QPAIR);
-      for (int a = 0; a < 2; ++a)
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_3d(q_s + b * C::QPAIR + a * C::TILE + c * C::CHUNK, tq, c * 64, item.qb * 256 + a * 128,
-                      item.bh, bar(C::B_QFULL + b));
-      q_loads = il + 1;
-    }
+  __device__ bool qk(int slot, int j, int, const PPItem &item) {
     return pp_first_use(slot, j, item) ? load_tile(tk, j, item.bh) : true;
   }
-  __device__ bool pv(int slot, int j, int il, const PPItem &item) {
+  __device__ bool pv(int slot, int j, int, const PPItem &item) {
     return pp_first_use(slot, j, item) ? load_tile(tv, j, item.bh) : true;
   }
 };
@@ -174,7 +176,7 @@ struct PPIssuer {
   volatile uint32_t *abort_flag;
   uint32_t it = 0;                 // ring positions consumed (first uses)
   uint32_t kpos = 0, vpos = 0;     // ring position of the K / V tile awaiting its last use
-  uint32_t n_qk[2] = {0, 0}, n_pv[2] = {0, 0};
+  uint32_t n_pv[2] = {0, 0};
   __device__ uint32_t bar(int i) const { return bar_s + 8u * static_cast<uint32_t>(i); }
   __device__ bool wait(int b, uint32_t ph) {
     return wait_bounded(bar(b), ph, abort_flag, p->status, kDevTimeoutMma, p->wait_limit);
@@ -186,8 +188,8 @@ struct PPIssuer {
     return true;
   }
   __device__ bool qk(int slot, int j, int il, const PPItem &item) {
-    if (slot == 0 && j == 0) {
-      if (!wait(C::B_QFULL + (il & 1), (il >> 1) & 1)) return false;
+    if (j == 0) {
+      if (!wait(C::B_QFULL + slot * 2 + (il & 1), (il >> 1) & 1)) return false;
       tc_fence_after();
     }
     uint32_t pos;
@@ -197,18 +199,17 @@ struct PPIssuer {
     } else {
       pos = kpos;
     }
-    const uint32_t q_tile = q_s + (il & 1) * C::QPAIR + slot * C::TILE;
-    const uint32_t k_tile = ring_s + (pos % C::NST) * C::TILE;
+    const SDesc a = sdesc_split(sdesc_sw128(pp_q_tile<D>(q_s, slot, il), 16, 1024));
+    const SDesc b = sdesc_split(sdesc_sw128(ring_s + (pos % C::NST) * C::TILE, 16, 1024));
     const uint32_t d_tmem = tmem + slot * 128u;
 #pragma unroll
     for (int c = 0; c < C::NCH; ++c)
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        umma_ss(d_tmem, sdesc_sw128(q_tile + c * C::CHUNK + kk * 32, 16, 1024),
-                sdesc_sw128(k_tile + c * C::CHUNK + kk * 32, 16, 1024), C::IDESC_QK, (c | kk) != 0 ? 1u : 0u);
+        umma_ss_off(d_tmem, a, c * C::CHUNK + kk * 32, b, c * C::CHUNK + kk * 32, C::IDESC_QK,
+                    (c | kk) != 0 ? 1u : 0u);
     umma_commit(bar(C::B_SFULL + slot));
     if (slot == 1) umma_commit(bar(C::B_EMPTY + pos % C::NST));  // last use of this K tile
-    ++n_qk[slot];
     return true;
   }
   __device__ bool pv(int slot, int j, int il, const PPItem &item) {
@@ -222,13 +223,12 @@ struct PPIssuer {
     } else {
       pos = vpos;
     }
-    const uint32_t v_tile = ring_s + (pos % C::NST) * C::TILE;
+    const SDesc b = sdesc_split(sdesc_sw128(ring_s + (pos % C::NST) * C::TILE, C::CHUNK, 1024));
     const uint32_t o_tmem = tmem + C::O_COL + slot * D;
     const uint32_t p_tmem = tmem + slot * 128u;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-      umma_ts(o_tmem, p_tmem + kk * 8u, sdesc_sw128(v_tile + kk * 2048, C::CHUNK, 1024), C::IDESC_PV,
-              (j == 0 && kk == 0) ? 0u : 1u);
+      umma_ts_off(o_tmem, p_tmem + kk * 8u, b, kk * 2048, C::IDESC_PV, (j == 0 && kk == 0) ? 0u : 1u);
     if (slot == 1) umma_commit(bar(C::B_EMPTY + pos % C::NST));  // last use of this V tile
     if (j == (slot == 0 ? item.n0 : item.n1) - 1) umma_commit(bar(C::B_OFINAL + slot));
     ++n_pv[slot];
@@ -240,29 +240,32 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                       const FwdParams p) {
+                       const FwdParams p, const __grid_constant__ SchedTable tbl) {
   using C = PPCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *const base_ptr = smem_raw + (base - raw);
   const uint32_t ring_s = base;                     // NST x TILE (first: see attn_fwd_kernel.cuh)
-  const uint32_t q_s = ring_s + C::NST * C::TILE;   // NQB x (Q0, Q1)
-  const uint32_t bar_s = q_s + C::NQB * C::QPAIR;   // NBAR x 8
+  const uint32_t q_s = ring_s + C::NST * C::TILE;   // Q[slot][item parity], also O staging
+  const uint32_t bar_s = q_s + C::NQBUF * C::TILE;  // NBAR x 8
   uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + (bar_s - base) + 8 * C::NBAR);
   volatile uint32_t *const abort_flag = tmem_slot + 1;
   auto BAR = [&](int i) -> uint32_t { return bar_s + 8u * static_cast<uint32_t>(i); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long LIM = p.wait_limit;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
       mbar_init(BAR(C::B_QFULL + i), 1);
-      mbar_init(BAR(C::B_QEMPTY + i), 2);
+      mbar_init(BAR(C::B_QEMPTY + i), 1);
+      mbar_init(BAR(C::B_EPI + i), 128);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(BAR(C::B_SFULL + i), 1);
       mbar_init(BAR(C::B_PFULL + i), 128);
       mbar_init(BAR(C::B_OFINAL + i), 1);
       mbar_init(BAR(C::B_OFREE + i), 128);
-      mbar_init(BAR(C::B_EPI + i), 128);
     }
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(BAR(C::B_FULL + i), 1);
@@ -285,32 +288,29 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Register split: the launch gives every thread kLaunchRegs; the producer/MMA warpgroup
-  // (warps 0-3) gives up registers that the two softmax warpgroups take:
-  // 128 * kRegsLow + 256 * kRegsHigh <= 384 * kLaunchRegs.
+  // Register split: the launch gives every thread kLaunchRegs; the warpgroup of the four
+  // single-thread roles (warps 0-3) gives up registers that the two softmax warpgroups
+  // take: 128 * kRegsLow + 256 * kRegsHigh <= 384 * kLaunchRegs.
   static_assert(128 * PPCfg<D>::kRegsLow + 256 * PPCfg<D>::kRegsHigh <= 384 * PPCfg<D>::kLaunchRegs,
                 "register split exceeds the launch allocation");
   if (warp < 4) {
     setmaxnreg_dec<PPCfg<D>::kRegsLow>();
     if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- K/V producer
       PPProducer<D, CAUSAL> pr;
-      pr.tq = &tm_q;
       pr.tk = &tm_k;
       pr.tv = &tm_v;
       pr.p = &p;
       pr.ring_s = ring_s;
-      pr.q_s = q_s;
       pr.bar_s = bar_s;
       pr.abort_flag = abort_flag;
-      pr.pol = policy_evict_last();
-      run_pp_stream<CAUSAL>(p, pr);
+      pr.pol_kv = policy_evict_last();
+      run_pp_stream<CAUSAL>(p, &tbl, pr);
       // Drain: every load issued must have landed before the CTA may exit.
       const uint32_t first = pr.it > static_cast<uint32_t>(C::NST) ? pr.it - C::NST : 0u;
-      for (uint32_t i = first; i < pr.it; ++i)
-        wait_drain(BAR(C::B_FULL + (i % C::NST)), (i / C::NST) & 1u, p.wait_limit);
-      for (int i = (pr.q_loads > 2 ? pr.q_loads - 2 : 0); i < pr.q_loads; ++i)
-        wait_drain(BAR(C::B_QFULL + (i & 1)), (i >> 1) & 1, p.wait_limit);
+      for (uint32_t i = first; i < pr.it; ++i) wait_drain(BAR(C::B_FULL + (i % C::NST)), (i / C::NST) & 1u, LIM);
     } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       PPIssuer<D, CAUSAL> is;
       is.p = &p;
       is.ring_s = ring_s;
@@ -318,9 +318,56 @@ __global__ void __launch_bounds__(384, 1)
       is.bar_s = bar_s;
       is.tmem = tmem;
       is.abort_flag = abort_flag;
-      run_pp_stream<CAUSAL>(p, is);
+      run_pp_stream<CAUSAL>(p, &tbl, is);
       umma_commit(BAR(C::B_DRAIN));
-      wait_drain(BAR(C::B_DRAIN), 0, p.wait_limit);
+      wait_drain(BAR(C::B_DRAIN), 0, LIM);
+    } else if (warp == 2 && lane == 0) {
+      // ---------------------------------------------------------- Q loader
+      const uint64_t pol_q = policy_evict_first();
+      Sched sc(blockIdx.x, gridDim.x, p.n_items, &tbl);
+      int il = 0, r;
+      bool ok = true;
+      while (ok && sc.next(r)) {
+        const PPItem item = pp_decode<CAUSAL>(r, p);
+        for (int a = 0; a < 2 && ok; ++a) {
+          const int b = a * 2 + (il & 1);
+          if (!(ok = wait_bounded(BAR(C::B_QEMPTY + b), ((il >> 1) & 1) ^ 1u, abort_flag, p.status,
+                                  kDevTimeoutLoad, LIM)))
+            break;
+          mbar_arrive_expect_tx(BAR(C::B_QFULL + b), C::TILE);
+          const uint32_t dst = pp_q_tile<D>(q_s, a, il);
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d_hint(dst + c * C::CHUNK, &tm_q, c * 64, item.qb * 256 + a * 128, item.bh,
+                             BAR(C::B_QFULL + b), pol_q);
+        }
+        ++il;
+      }
+      // Drain the Q loads of the last two items.
+      for (int i = (il > 2 ? il - 2 : 0); i < il; ++i)
+        for (int a = 0; a < 2; ++a) wait_drain(BAR(C::B_QFULL + a * 2 + (i & 1)), (i >> 1) & 1, LIM);
+    } else if (warp == 3 && lane == 0) {
+      // ---------------------------------------------------------- O store issuer
+      Sched sc(blockIdx.x, gridDim.x, p.n_items, &tbl);
+      int il = 0, r;
+      bool ok = true;
+      while (ok && sc.next(r)) {
+        const PPItem item = pp_decode<CAUSAL>(r, p);
+        for (int a = 0; a < 2 && ok; ++a) {
+          if (!(ok = wait_bounded(BAR(C::B_EPI + a * 2 + (il & 1)), (il >> 1) & 1, abort_flag, p.status,
+                                  kDevTimeoutEpilogue, LIM)))
+            break;
+          const int qrow0 = item.qb * 256 + a * 128;
+          if (qrow0 < p.L) {
+            const uint32_t src = pp_q_tile<D>(q_s, a, il);
+            for (int c = 0; c < C::NCH; ++c) tma_store_3d(&tm_o, src + c * C::CHUNK, c * 64, qrow0, item.bh);
+            bulk_commit();
+            bulk_wait_read0();
+          }
+          mbar_arrive(BAR(C::B_QEMPTY + a * 2 + (il & 1)));  // the staging buffer may be refilled
+        }
+        ++il;
+      }
+      bulk_wait0();
     }
     __syncwarp();
   } else {
@@ -333,8 +380,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t s_tmem = tmem + lane_base + slot * 128u;
     const uint32_t o_tmem = tmem + lane_base + C::O_COL + slot * D;
     const float c2 = p.c2;
-    const long long LIM = p.wait_limit;
-    Sched sc(blockIdx.x, gridDim.x, p.n_items);
+    Sched sc(blockIdx.x, gridDim.x, p.n_items, &tbl);
     uint32_t g = 0;  // S tiles of this slot so far
     int il = 0, r;
     bool ok = true;
@@ -351,69 +397,29 @@ __global__ void __launch_bounds__(384, 1)
       for (int j = 0; j < n; ++j, ++g) {
         if (!(ok = wait_warp(BAR(C::B_SFULL + slot), g & 1u))) break;
         tc_fence_after();
-        uint32_t sr[128];
-        tmem_ld32x128(s_tmem, sr);
-        float *s = reinterpret_cast<float *>(sr);
-        if (CAUSAL) {
-          if (j == diag) {
-#pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (c > row) s[c] = -INFINITY;
-          }
-        } else {
-          const int lim = p.L - j * 128;
-          if (lim < 128) {
-#pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (c >= lim) s[c] = -INFINITY;
-          }
-        }
-        float mx = s[0];
-#pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-        const float m_tile = mx * c2;
-        if (j == 0) {
-          m_used = (m_tile == -INFINITY) ? 0.f : m_tile;
-        } else if (__any_sync(0xffffffffu, m_tile > m_used + 8.0f)) {
-          // PV of the previous tile is complete (it precedes this QK in the issue order).
-          const float m_new = fmaxf(m_used, m_tile);
-          const float alpha = ex2_approx(m_used - m_new);
-          m_used = m_new;
-          l *= alpha;
-#pragma unroll 1
-          for (int c32 = 0; c32 < D / 32; ++c32) {
-            uint32_t orr[32];
-            tmem_ld32x32(o_tmem + c32 * 32, orr);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-            tmem_st32x32(o_tmem + c32 * 32, orr);
-          }
-        }
-        const float neg = -m_used;
-        float sum = 0.f;
-        uint32_t pk[64];
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float p0 = ex2_approx(fmaf(s[2 * c], c2, neg));
-          const float p1 = ex2_approx(fmaf(s[2 * c + 1], c2, neg));
-          sum += p0 + p1;
-          pk[c] = pack_f16x2(p0, p1);
-        }
-        l += sum;
-        tmem_st32x64(s_tmem, pk);
+        // Keys past the diagonal (causal) or past L (ragged last tile) are masked.  PV of
+        // the previous tile is complete here: it precedes this QK in the issue order.
+        const int lim = CAUSAL ? (j == diag ? row + 1 : 128) : min(128, p.L - j * 128);
+        softmax_tile<D>(s_tmem, o_tmem, lim, c2, j == 0, m_used, l);
         tc_fence_before();
         mbar_arrive(BAR(C::B_PFULL + slot));
       }
       if (!ok) break;
       // --------------------------------------------------------------- epilogue
+      // O / l as fp16 into this tile's Q buffer (swizzled like a TMA box), then the store
+      // issuer writes it out; LSE goes straight to global memory.
       if (!(ok = wait_warp(BAR(C::B_OFINAL + slot), il & 1))) break;
       tc_fence_after();
-      const uint32_t stage = q_s + (il & 1) * C::QPAIR + slot * C::TILE;  // this tile's Q, no longer read
+      const uint32_t stage = pp_q_tile<D>(q_s, slot, il);
       const float inv_l = 1.0f / l;
 #pragma unroll 1
       for (int c32 = 0; c32 < D / 32; ++c32) {
         uint32_t orr[32];
         tmem_ld32x32(o_tmem + c32 * 32, orr);
+        if (c32 == D / 32 - 1) {  // O fully read: the next item's first PV may overwrite it
+          tc_fence_before();
+          mbar_arrive(BAR(C::B_OFREE + slot));
+        }
         uint32_t h[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -426,28 +432,13 @@ __global__ void __launch_bounds__(384, 1)
                        h[4 * q4 + 3]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(BAR(C::B_OFREE + slot));
       const int grow = qrow0 + row;
       if (grow < p.L)
         p.lse[static_cast<long long>(item.bh) * p.L + grow] = (m_used + __log2f(l)) * 0.69314718055994531f;
       fence_proxy_async_smem();
-      mbar_arrive(BAR(C::B_EPI + slot));
-      if (quarter == 0 && lane == 0) {
-        if (wait_bounded(BAR(C::B_EPI + slot), il & 1, abort_flag, p.status, kDevTimeoutEpilogue, LIM)) {
-          if (qrow0 < p.L) {
-            for (int c = 0; c < C::NCH; ++c) tma_store_3d(&tm_o, stage + c * C::CHUNK, c * 64, qrow0, item.bh);
-            bulk_commit();
-            bulk_wait_read0();
-          }
-          mbar_arrive(BAR(C::B_QEMPTY + (il & 1)));
-        }
-      }
-      __syncwarp();
+      mbar_arrive(BAR(C::B_EPI + slot * 2 + (il & 1)));
       ++il;
     }
-    if (quarter == 0 && lane == 0) bulk_wait0();
-    __syncwarp();
   }
 
   tc_fence_before();
@@ -477,7 +468,7 @@ cudaError_t launch_fwd_pp_variant(const FwdLaunch &a) {
     if (e != cudaSuccess) return e;
     if (dev < 31) configured_mask |= (1 << dev);
   }
-  kern<<<a.grid, 384, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
+  kern<<<a.grid, 384, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p, *a.tbl);
   return cudaGetLastError();
 }
 

@@ -5,10 +5,15 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
+#include <numeric>
+#include <queue>
+#include <vector>
 
 #include "attn_fwd_kernel.cuh"
 #include "attn_fwd_pp.cuh"
@@ -90,6 +95,90 @@ int encode_bhld(CUtensorMap *tm, const void *ptr, int BH, int L, int D) {
   return r == CUDA_SUCCESS ? GBATTN_OK : GBATTN_ERR_TENSORMAP;
 }
 
+// ------------------------------------------------------------------ work schedule
+// Cost of a work item in 128 x 128 tile units plus a per-item overhead (fill, drain and
+// epilogue of the item's pipeline), the latter measured on GB300 for each kernel.
+constexpr double kItemOverheadTwoTile = 1.7;
+constexpr double kItemOverheadSingle = 1.0;
+
+struct SchedKey {
+  int two_tile, BH, nQ, nQB, dvs, causal, grid;
+  bool operator==(const SchedKey &o) const {
+    return two_tile == o.two_tile && BH == o.BH && nQ == o.nQ && nQB == o.nQB && dvs == o.dvs &&
+           causal == o.causal && grid == o.grid;
+  }
+};
+
+// Work units of item r, mirroring the kernels' item decoding (pp_decode / decode_item).
+int item_units(const SchedKey &k, int r) {
+  if (k.two_tile) {
+    if (!k.causal) return 2 * k.nQ;
+    const int qb = k.nQB - 1 - r / k.BH;
+    return (2 * qb + 1) + std::min(2 * qb + 2, k.nQ);
+  }
+  if (!k.causal) return k.nQ;
+  const int qt = k.nQ - 1 - r / (k.BH * k.dvs);
+  return qt + 1;
+}
+
+// Longest-processing-time-first: take items by decreasing cost, give each to the CTA with
+// the least accumulated cost (ties: lowest CTA).  Each CTA's list keeps assignment order.
+void build_lpt(const SchedKey &k, int n_items, SchedTable &t) {
+  std::memset(&t, 0, sizeof(t));
+  if (n_items > kSchedMaxItems || k.grid > kSchedMaxCtas || k.grid <= 0) return;  // snake order
+  const double over = k.two_tile ? kItemOverheadTwoTile : kItemOverheadSingle;
+  std::vector<int> order(n_items);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int a, int b) { return item_units(k, a) > item_units(k, b); });
+  using Slot = std::pair<double, int>;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int c = 0; c < k.grid; ++c) heap.push({0.0, c});
+  std::vector<std::vector<uint16_t>> lists(k.grid);
+  for (int r : order) {
+    const Slot s = heap.top();
+    heap.pop();
+    lists[s.second].push_back(static_cast<uint16_t>(r));
+    heap.push({s.first + item_units(k, r) + over, s.second});
+  }
+  int pos = 0;
+  for (int c = 0; c < k.grid; ++c) {
+    t.start[c] = static_cast<uint16_t>(pos);
+    for (uint16_t r : lists[c]) t.items[pos++] = r;
+  }
+  t.start[k.grid] = static_cast<uint16_t>(pos);
+  t.n = n_items;
+}
+
+struct SchedEntry {
+  bool valid = false;
+  unsigned long long stamp = 0;
+  SchedKey key{};
+  SchedTable tbl;
+};
+SchedEntry g_sched_cache[8];
+unsigned long long g_sched_clock = 0;
+std::mutex g_sched_mu;
+
+// Copy the schedule for `k` into `out`, building and caching it on a miss.
+void get_schedule(const SchedKey &k, int n_items, SchedTable &out) {
+  std::lock_guard<std::mutex> lock(g_sched_mu);
+  SchedEntry *victim = &g_sched_cache[0];
+  for (SchedEntry &e : g_sched_cache) {
+    if (e.valid && e.key == k) {
+      e.stamp = ++g_sched_clock;
+      out = e.tbl;
+      return;
+    }
+    if (!e.valid || e.stamp < victim->stamp) victim = &e;
+  }
+  build_lpt(k, n_items, victim->tbl);
+  victim->key = k;
+  victim->valid = true;
+  victim->stamp = ++g_sched_clock;
+  out = victim->tbl;
+}
+
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
@@ -119,10 +208,16 @@ extern "C" int attn_fwd_ex(const void *q, const void *k, const void *v, void *o,
   if (!std::isfinite(scale) || !(scale > 0.f)) return GBATTN_ERR_SCALE;
   const bool p_smem = (flags & GBATTN_FLAG_P_SMEM) != 0;
   if (p_smem && d > 128) return GBATTN_ERR_HEAD_DIM;
-  if (flags & ~(GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE)) return GBATTN_ERR_FLAGS;
-  // Two 128-row query tiles per item (ping-pong kernel) for d <= 128 unless a
-  // single-tile option is asked for.
-  const bool two_tile = d <= 128 && !p_smem && !(flags & GBATTN_FLAG_SINGLE_TILE);
+  if (flags & ~(GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE | GBATTN_FLAG_TWO_TILE)) return GBATTN_ERR_FLAGS;
+  if ((flags & GBATTN_FLAG_TWO_TILE) && (flags & (GBATTN_FLAG_SINGLE_TILE | GBATTN_FLAG_P_SMEM)))
+    return GBATTN_ERR_FLAGS;
+  if ((flags & GBATTN_FLAG_TWO_TILE) && d > 128) return GBATTN_ERR_HEAD_DIM;
+  // d <= 128: the two-tile kernel (two 128-row query tiles per item) unless an option asks
+  // for the single-tile kernel, or unless it would get fewer than two items per SM: then
+  // the single-tile kernel's twice-as-many, half-as-long items balance the SMs better
+  // (measured on GB300: 1x16x512x64 causal 7.7 vs 10.5 us, 1x32x1024x128 causal 15.0 vs
+  // 19.2 us), while the two-tile kernel is faster once every SM has several items.
+  bool two_tile = d <= 128 && !(flags & (GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE));
   if (grid_limit < 0) return GBATTN_ERR_DIMS;
   const long long rows = static_cast<long long>(B) * H * L;
   const size_t tbytes = static_cast<size_t>(rows) * static_cast<size_t>(d) * 2u;
@@ -139,10 +234,14 @@ extern "C" int attn_fwd_ex(const void *q, const void *k, const void *v, void *o,
   const int nQ = (L + 127) / 128;
   const int nQB = (L + 255) / 256;
   const int dvs = d > 256 ? d / 256 : 1;
+  if (two_tile && !(flags & GBATTN_FLAG_TWO_TILE) && static_cast<long long>(BH) * nQB < 2LL * di->sm_count)
+    two_tile = false;
   const long long n_items = two_tile ? static_cast<long long>(BH) * nQB : static_cast<long long>(BH) * nQ * dvs;
   if (n_items > INT_MAX) return GBATTN_ERR_DIMS;
 
   FwdLaunch a;
+  SchedTable tbl;
+  a.tbl = &tbl;
   if (encode_bhld(&a.tm_q, q, BH, L, d) || encode_bhld(&a.tm_k, k, BH, L, d) || encode_bhld(&a.tm_v, v, BH, L, d) ||
       encode_bhld(&a.tm_o, o, BH, L, d))
     return GBATTN_ERR_TENSORMAP;
@@ -150,9 +249,12 @@ extern "C" int attn_fwd_ex(const void *q, const void *k, const void *v, void *o,
   if (grid_limit > 0 && grid_limit < grid) grid = grid_limit;
   if (n_items < grid) grid = static_cast<int>(n_items);
   a.grid = grid;
+  get_schedule(SchedKey{two_tile ? 1 : 0, BH, nQ, nQB, two_tile ? 1 : dvs, causal != 0 ? 1 : 0, grid},
+               static_cast<int>(n_items), tbl);
   a.causal = causal != 0;
   a.p_smem = p_smem;
   a.stream = static_cast<cudaStream_t>(stream);
+  a.p.o = o;
   a.p.lse = lse;
   a.p.status = di->status;
   a.p.wait_limit = kWaitLimitCycles;
@@ -246,6 +348,28 @@ extern "C" const char *attn_strerror(int code) {
     case GBATTN_DEV_TIMEOUT_PROBE: return "device: the wait-probe barrier timed out (expected)";
     default: return "unknown gbattn status code";
   }
+}
+
+extern "C" int attn_debug_schedule(int B, int H, int L, int d, int causal, int grid, int flags, int *start,
+                                   int *items, int max_items) {
+  int rc = check_shape(B, H, L, d);
+  if (rc != GBATTN_OK) return rc;
+  if (grid <= 0 || grid > kSchedMaxCtas) return GBATTN_ERR_DIMS;
+  if (!start || !items) return GBATTN_ERR_NULL;
+  // The schedule of the kernel the flags name: the two-tile kernel when d <= 128 and no
+  // single-tile option is set (the automatic choice of attn_fwd is not applied here).
+  const bool two_tile = d <= 128 && !(flags & (GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE));
+  const int BH = B * H, nQ = (L + 127) / 128, nQB = (L + 255) / 256, dvs = d > 256 ? d / 256 : 1;
+  const long long n_items = two_tile ? static_cast<long long>(BH) * nQB : static_cast<long long>(BH) * nQ * dvs;
+  if (n_items > INT_MAX) return GBATTN_ERR_DIMS;
+  static SchedTable t;  // large; this is a test hook, not thread-safe
+  get_schedule(SchedKey{two_tile ? 1 : 0, BH, nQ, nQB, two_tile ? 1 : dvs, causal != 0 ? 1 : 0, grid},
+               static_cast<int>(n_items), t);
+  if (t.n == 0) return 0;
+  if (t.n > max_items) return GBATTN_ERR_DIMS;
+  for (int c = 0; c <= grid; ++c) start[c] = t.start[c];
+  for (int i = 0; i < t.n; ++i) items[i] = t.items[i];
+  return t.n;
 }
 
 extern "C" int attn_version(void) { return 100; }

@@ -1,0 +1,118 @@
+// softmax_tile.cuh -- one online-softmax step over a 128-column S tile held in tensor
+// memory, one query row per thread (the softmax stage of "An Optimal Mapper Meets a Real
+// GPU", "Experiment one", item (3): a real row max, exponent, sum and divide).
+//
+// In base 2: with c2 = scale * log2(e), the running maximum m (log2 units) and the
+// running sum l satisfy, after every tile,
+//     l = sum_j 2^(s_j * c2 - m)   over the keys seen so far,
+// and O (in tensor memory) = sum_j 2^(s_j * c2 - m) v_j.  m is raised lazily: only when a
+// tile's maximum exceeds it by more than 8 (a factor 256, harmless in fp16 P and fp32
+// sums); then O and l are multiplied by 2^(m_old - m_new).  The final O / l and
+// LSE = (m + log2 l) * ln 2 do not depend on when m was raised.
+//
+// Latency, not arithmetic, bounds this step (one warp per scheduler per Q tile), so:
+// the second half of S is loaded while the max over the first half runs; the max uses
+// eight independent chains of three-input max; s * c2 - m uses packed f32x2 FMA; the row
+// sum uses four packed f32x2 partial sums.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace gbattn {
+
+// s_tmem / o_tmem: this warp's lane base plus the S / O column.  Columns >= lim are
+// masked to -inf (lim = row + 1 on a causal diagonal tile, L - first key on a ragged last
+// tile, 128 otherwise).  P (fp16) is written over the first 64 columns of the S tile.
+// Warp-collective (tcgen05.ld/st): all 32 lanes must call it together.
+// `before_rescale()` runs on every tile but the first, after the tile maximum is known
+// and before O may be touched (the single-tile kernel waits there for the previous PV);
+// if it returns false the step stops and returns false.
+struct NoWait {
+  __device__ bool operator()() const { return true; }
+};
+template <int DV, class Hook = NoWait>
+__device__ __forceinline__ bool softmax_tile(uint32_t s_tmem, uint32_t o_tmem, int lim, float c2, bool first,
+                                             float &m_used, float &l, const Hook &before_rescale = Hook()) {
+  uint32_t ra[64], rb[64];
+  tmem_ld32x64(s_tmem, ra);
+  tmem_ld32x64_async(s_tmem + 64, rb);
+  float *sa = reinterpret_cast<float *>(ra);
+  if (lim < 64) {
+#pragma unroll
+    for (int c = 0; c < 64; ++c)
+      if (c >= lim) sa[c] = -INFINITY;
+  }
+  float mk[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    mk[k] = fmax3(sa[8 * k], sa[8 * k + 1], sa[8 * k + 2]);
+    mk[k] = fmax3(mk[k], sa[8 * k + 3], sa[8 * k + 4]);
+    mk[k] = fmax3(mk[k], sa[8 * k + 5], sa[8 * k + 6]);
+    mk[k] = fmaxf(mk[k], sa[8 * k + 7]);
+  }
+  tmem_wait_ld_fence64(rb);
+  float *sb = reinterpret_cast<float *>(rb);
+  if (lim < 128) {
+#pragma unroll
+    for (int c = 0; c < 64; ++c)
+      if (c + 64 >= lim) sb[c] = -INFINITY;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    mk[k] = fmax3(mk[k], sb[8 * k], sb[8 * k + 1]);
+    mk[k] = fmax3(mk[k], sb[8 * k + 2], sb[8 * k + 3]);
+    mk[k] = fmax3(mk[k], sb[8 * k + 4], sb[8 * k + 5]);
+    mk[k] = fmax3(mk[k], sb[8 * k + 6], sb[8 * k + 7]);
+  }
+  const float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
+  const float m_tile = mx * c2;
+  if (first) {
+    m_used = (m_tile == -INFINITY) ? 0.f : m_tile;
+    l = 0.f;
+  } else if (!before_rescale()) {
+    return false;
+  } else if (__any_sync(0xffffffffu, m_tile > m_used + 8.0f)) {
+    // The caller guarantees that no PV into O is in flight here.
+    const float m_new = fmaxf(m_used, m_tile);
+    const float alpha = ex2_approx(m_used - m_new);
+    m_used = m_new;
+    l *= alpha;
+#pragma unroll 1
+    for (int c32 = 0; c32 < DV / 32; ++c32) {
+      uint32_t orr[32];
+      tmem_ld32x32(o_tmem + c32 * 32, orr);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+      tmem_st32x32(o_tmem + c32 * 32, orr);
+    }
+  }
+  const uint64_t c2x2 = f32x2(c2, c2), negm = f32x2(-m_used, -m_used);
+  uint64_t acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = f32x2(0.f, 0.f);
+  uint32_t pk[64];
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    float x0, x1;
+    f32x2_split(ffma2(f32x2(sa[2 * c], sa[2 * c + 1]), c2x2, negm), x0, x1);
+    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    acc[c & 3] = fadd2(acc[c & 3], f32x2(p0, p1));
+    pk[c] = pack_f16x2(p0, p1);
+  }
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    float x0, x1;
+    f32x2_split(ffma2(f32x2(sb[2 * c], sb[2 * c + 1]), c2x2, negm), x0, x1);
+    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    acc[c & 3] = fadd2(acc[c & 3], f32x2(p0, p1));
+    pk[32 + c] = pack_f16x2(p0, p1);
+  }
+  const uint64_t s01 = fadd2(acc[0], acc[1]), s23 = fadd2(acc[2], acc[3]);
+  float lo, hi;
+  f32x2_split(fadd2(s01, s23), lo, hi);
+  l += lo + hi;
+  tmem_st32x64(s_tmem, pk);
+  return true;
+}
+
+}  // namespace gbattn

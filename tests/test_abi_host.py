@@ -85,6 +85,14 @@ def test_smem_p_only_up_to_128(lib):
     assert _fwd(lib, d=256, flags=1) == _codes()["GBATTN_ERR_HEAD_DIM"]
 
 
+def test_flag_combinations(lib):
+    c = _codes()
+    assert _fwd(lib, d=512, flags=4) == c["GBATTN_ERR_HEAD_DIM"]
+    assert _fwd(lib, flags=4 | 2) == c["GBATTN_ERR_FLAGS"]
+    assert _fwd(lib, flags=4 | 1) == c["GBATTN_ERR_FLAGS"]
+    assert _fwd(lib, flags=8) == c["GBATTN_ERR_FLAGS"]
+
+
 @pytest.mark.parametrize("kw", ["q", "k", "v", "o", "lse"])
 def test_rejects_misaligned(lib, kw):
     base = {"q": Q, "k": K, "v": V, "o": O, "lse": LSE}[kw]

@@ -86,12 +86,15 @@ SMALL = [(L, d) for d in (64, 128) for L in (1, 17, 127, 128, 129, 200, 256, 384
         [(L, d) for d in (256, 512) for L in (1, 100, 128, 300)]
 
 
+@pytest.mark.parametrize("flags", [0, 4], ids=["auto", "two_tile"])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 @pytest.mark.parametrize("L,d", SMALL)
-def test_fwd_small_matches_oracle(L, d, causal):
+def test_fwd_small_matches_oracle(L, d, causal, flags):
+    if d > 128 and flags:
+        pytest.skip("the two-tile kernel exists for head_dim <= 128")
     q, k, v = inputs.qkv(2, 3, L, d, seed=7 * L + d + int(causal), sigma=0.5 if d == 512 else 1.0)
     scale = 1.0 / math.sqrt(d)
-    o, lse = _run(*_dev(q, k, v), causal, scale)
+    o, lse = _run(*_dev(q, k, v), causal, scale, flags=flags)
     o_ref, lse_ref = oracle.sdpa_fwd(q, k, v, causal, float(np.float32(scale)))
     _check(o, lse, o_ref, lse_ref, f"L={L} d={d} causal={causal}")
 
@@ -118,14 +121,16 @@ def test_fwd_smem_p_variant_matches_oracle(L, d, causal):
     _check(o, lse, o_ref, lse_ref, "smem-P")
 
 
-@pytest.mark.parametrize("flags", [0, 2], ids=["default", "single_tile"])
+@pytest.mark.parametrize("flags", [4, 2], ids=["two_tile", "single_tile"])
 @pytest.mark.parametrize("grid", [1, 2, 3, 7])
 @pytest.mark.parametrize("d", [64, 128, 512])
 def test_fwd_persistent_loop_with_few_ctas(grid, d, flags):
     """Few CTAs => many items per CTA: exercises the cross-item pipeline and the phase
     bookkeeping of every barrier over long runs."""
-    if d > 128 and flags:
-        pytest.skip("head_dim 512 has only the single-tile kernel")
+    if d > 128:
+        if flags == 4:
+            pytest.skip("head_dim 512 has only the single-tile kernel")
+        flags = 0
     L = 640 if d < 512 else 384
     q, k, v = inputs.qkv(1, 3, L, d, seed=grid * 100 + d, sigma=0.5 if d == 512 else 1.0)
     scale = 1.0 / math.sqrt(d)
@@ -135,7 +140,7 @@ def test_fwd_persistent_loop_with_few_ctas(grid, d, flags):
         _check(o, lse, o_ref, lse_ref, f"grid={grid} causal={causal}")
 
 
-@pytest.mark.parametrize("d,flags", [(64, 0), (64, 2), (128, 0), (128, 2), (512, 0)])
+@pytest.mark.parametrize("d,flags", [(64, 4), (64, 2), (128, 4), (128, 2), (512, 0)])
 def test_fwd_large_logits_force_rescale(d, flags):
     """Keys whose logits grow along the sequence force the lazy O rescale path."""
     B, H, L = 1, 2, 512
@@ -150,13 +155,32 @@ def test_fwd_large_logits_force_rescale(d, flags):
         _check(o, lse, o_ref, lse_ref, "rescale")
 
 
+def test_fwd_many_items_use_the_fixed_order():
+    """More work items than the schedule table holds: the kernels fall back to their fixed
+    snake order (both kernels)."""
+    B, H, L, d = 1, 3100, 130, 64
+    q, k, v = inputs.qkv(B, H, L, d, seed=3)
+    scale = 1.0 / math.sqrt(d)
+    o_ref, lse_ref = oracle.sdpa_fwd(q, k, v, True, float(np.float32(scale)))
+    for flags in (4, 2):
+        o, lse = _run(*_dev(q, k, v), True, scale, flags=flags)
+        _check(o, lse, o_ref, lse_ref, f"many items flags={flags}")
+
+
 # ------------------------------------------------------------------ the five workloads
+_ORACLE_CACHE = {}
+
+@pytest.mark.parametrize("flags", [0, 4, 2], ids=["auto", "two_tile", "single_tile"])
 @pytest.mark.parametrize("name", list(WORKLOADS))
-def test_workload_full_size_matches_oracle(name):
+def test_workload_full_size_matches_oracle(name, flags):
     w = WORKLOADS[name]
+    if w.d > 128 and flags:
+        pytest.skip("head_dim 512 has only the single-tile kernel")
     q, k, v = inputs.qkv(w.B, w.H, w.L, w.d, w.seed, w.sigma)
-    o, lse = _run(*_dev(q, k, v), w.causal, w.scale)
-    o_ref, lse_ref = oracle.sdpa_fwd(q, k, v, w.causal, float(np.float32(w.scale)))
+    o, lse = _run(*_dev(q, k, v), w.causal, w.scale, flags=flags)
+    if name not in _ORACLE_CACHE:
+        _ORACLE_CACHE[name] = oracle.sdpa_fwd(q, k, v, w.causal, float(np.float32(w.scale)))
+    o_ref, lse_ref = _ORACLE_CACHE[name]
     e_o, e_l = _check(o, lse, o_ref, lse_ref, name)
     print(f"{name}: max|dO| {e_o:.3e}  max|dLSE| {e_l:.3e}")
 

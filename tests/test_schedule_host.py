@@ -1,0 +1,80 @@
+"""Host-side checks of the static work schedule (no GPU): every work item is assigned to
+exactly one CTA, lists run longest item first, and the longest-processing-time-first
+assignment keeps the busiest CTA close to the lower bound."""
+import math
+
+import pytest
+
+import scaled_dot_product_sdpa_gb300 as gb
+
+
+def _units(B, H, L, d, causal, flags, r):
+    """Work units of item r, from the item numbering documented with the kernels."""
+    BH, nQ, nQB = B * H, math.ceil(L / 128), math.ceil(L / 256)
+    two_tile = d <= 128 and not (flags & 3)
+    if two_tile:
+        if not causal:
+            return 2 * nQ
+        qb = nQB - 1 - r // BH
+        return (2 * qb + 1) + min(2 * qb + 2, nQ)
+    dvs = d // 256 if d > 256 else 1
+    if not causal:
+        return nQ
+    return nQ - 1 - r // (BH * dvs) + 1
+
+
+def _n_items(B, H, L, d, flags):
+    BH, nQ, nQB = B * H, math.ceil(L / 128), math.ceil(L / 256)
+    if d <= 128 and not (flags & 3):
+        return BH * nQB
+    return BH * nQ * (d // 256 if d > 256 else 1)
+
+
+CASES = [(8, 32, 512, 128, True, 0), (1, 32, 1024, 128, True, 0), (1, 16, 512, 64, True, 0),
+         (1, 8, 128, 64, False, 0), (1, 8, 2048, 512, True, 0), (8, 32, 512, 128, True, 2),
+         (2, 3, 1000, 64, False, 0), (1, 5, 777, 128, True, 1)]
+
+
+@pytest.mark.parametrize("B,H,L,d,causal,flags", CASES)
+@pytest.mark.parametrize("grid", [1, 7, 152])
+def test_every_item_exactly_once(B, H, L, d, causal, flags, grid):
+    n = _n_items(B, H, L, d, flags)
+    sched = gb.attn_debug_schedule(B, H, L, d, causal, min(grid, n), flags)
+    assert sched is not None
+    flat = sorted(i for lst in sched for i in lst)
+    assert flat == list(range(n))
+
+
+@pytest.mark.parametrize("B,H,L,d,causal,flags", CASES)
+def test_lists_run_longest_first_and_balance(B, H, L, d, causal, flags):
+    n = _n_items(B, H, L, d, flags)
+    grid = min(152, n)
+    sched = gb.attn_debug_schedule(B, H, L, d, causal, grid, flags)
+    cost = [_units(B, H, L, d, causal, flags, r) for r in range(n)]
+    for lst in sched:
+        c = [cost[r] for r in lst]
+        assert c == sorted(c, reverse=True)
+    loads = [sum(cost[r] for r in lst) for lst in sched]
+    lower = max(sum(cost) / grid, max(cost))
+    # LPT is within 4/3 of the optimum on costs; allow the per-item overhead term too.
+    assert max(loads) <= 4.0 / 3.0 * lower + max(cost)
+
+
+def test_single_tile_case_d_balances_to_the_mean():
+    """caseD as single-tile items (1-4 units each): the busiest CTA is within one item
+    of the mean load (2560 units over 152 CTAs = 16.8)."""
+    sched = gb.attn_debug_schedule(8, 32, 512, 128, True, 152, gb.FLAG_SINGLE_TILE)
+    loads = [sum(_units(8, 32, 512, 128, True, 2, r) for r in lst) for lst in sched]
+    assert sum(loads) == 2560
+    assert max(loads) <= 17 + 4
+
+
+def test_too_many_items_falls_back_to_fixed_order():
+    assert gb.attn_debug_schedule(1, 4000, 128, 64, False, 152, 0) is None
+
+
+def test_schedule_rejects_bad_arguments():
+    with pytest.raises(gb.GbattnError):
+        gb.attn_debug_schedule(1, 1, 128, 48, False, 4)
+    with pytest.raises(gb.GbattnError):
+        gb.attn_debug_schedule(1, 1, 128, 64, False, 0)
