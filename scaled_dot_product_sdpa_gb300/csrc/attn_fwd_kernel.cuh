@@ -159,6 +159,43 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     }
   }
 }
+// Wait for up to three barrier phases at once: first test them all back to back (their
+// latencies overlap), and only fall back to bounded waits for those not yet complete.
+struct WaitSet {
+  uint32_t b0 = 0, p0 = 0, b1 = 0, p1 = 0, b2 = 0, p2 = 0;
+  int n = 0;
+  __device__ void add(uint32_t b, uint32_t ph) {
+    if (n == 0) {
+      b0 = b;
+      p0 = ph;
+    } else if (n == 1) {
+      b1 = b;
+      p1 = ph;
+    } else {
+      b2 = b;
+      p2 = ph;
+    }
+    ++n;
+  }
+  // Non-blocking: are all phases complete?
+  __device__ bool test() const {
+    bool all = mbar_test(b0, p0);
+    if (n > 1) all &= mbar_test(b1, p1);
+    if (n > 2) all &= mbar_test(b2, p2);
+    return all;
+  }
+  __device__ bool wait(volatile uint32_t *abort_flag, unsigned *status, unsigned code, long long limit) const {
+    bool all = mbar_test(b0, p0);
+    if (n > 1) all &= mbar_test(b1, p1);
+    if (n > 2) all &= mbar_test(b2, p2);
+    if (all) return true;
+    if (!wait_bounded(b0, p0, abort_flag, status, code, limit)) return false;
+    if (n > 1 && !wait_bounded(b1, p1, abort_flag, status, code, limit)) return false;
+    if (n > 2 && !wait_bounded(b2, p2, abort_flag, status, code, limit)) return false;
+    return true;
+  }
+};
+
 // Same but ignoring the abort flag: used only while draining in-flight work at exit.
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, long long limit) {
   const long long t0 = clock64();

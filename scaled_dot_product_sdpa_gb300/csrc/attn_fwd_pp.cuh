@@ -1,34 +1,32 @@
-// attn_fwd_pp.cuh -- two-tile ("ping-pong") SDPA forward for head_dim 64 and 128 on sm_103a.
+// attn_fwd_pp.cuh -- two-tile SDPA forward for head_dim 64 and 128 on sm_103a.
 //
 // Same mathematics as attn_fwd_kernel.cuh ("An Optimal Mapper Meets a Real GPU",
 // "Ground rules" / "Experiment one"): O = softmax(scale * Q K^T + causal mask) V and the
 // row LSE, fused into one persistent kernel.  The work item is a 256-row query block
-// split into two 128-row tiles Q0 and Q1 that share every K/V tile the producer loads
-// (half the K/V traffic per query row of the single-tile kernel), each with its own
-// softmax warpgroup, S buffer and O accumulator in tensor memory:
+// split into two 128-row tiles Q0 and Q1 ("slots") that share every K/V tile the
+// producer loads (half the K/V traffic per query row of the single-tile kernel).  Each
+// slot has its own S buffer and O accumulator in tensor memory, its own softmax
+// warpgroup and its own MMA-issuing thread:
 //   TMEM columns  S0 [0,128)  S1 [128,256)  O0 [256, 256+D)  O1 [256+D, 256+2D).
 //
-// The MMA issuer runs one fixed stream of tensor-core operations per item:
-//   QK0_0, QK1_0, then for each key tile j:  PV0_j, QK0_{j+1}, PV1_j, QK1_{j+1}
-// where QKa_{j+1} at the end of an item is already the first QK of the next item.  PVa_j
-// always comes right before QKa_{j+1} from the same thread, so when softmax warpgroup a
-// sees S_a of tile j+1 complete, PV_a of tile j is complete too (tcgen05 operations of
-// one thread complete in order): the lazy O rescale never waits for a PV, and while
-// warpgroup a exponentiates tile j the tensor core runs the other tile's PV and QK.
-// Under the causal mask Q0 needs key tiles 0..2qb and Q1 needs 0..2qb+1; the last one
-// is run for Q1 alone.
+// Slot a's issuer runs the chain  QK_0, then for each key tile j:  PV_j, QK_{j+1}
+// (QK_{j+1} after the last tile is the first QK of the next item).  PV_j comes right
+// before QK_{j+1} from the same thread, so when softmax warpgroup a sees S of tile j+1
+// complete, PV of tile j is complete too (tcgen05 operations of one thread complete in
+// order): the lazy O rescale never waits for a PV.  The two issuers' MMAs interleave in
+// the tensor core's queue, so while slot a waits for its softmax the tensor core runs
+// slot b's work and neither slot's wait holds the other back.  Under the causal mask Q0
+// needs key tiles 0..2qb and Q1 needs 0..2qb+1; the last one belongs to Q1 alone.
 //
 // Warp roles (384 threads):
-//   warp 0      K/V producer: walks the same operation stream as the MMA issuer
-//               (run_pp_stream) and loads each K or V tile into the ring at its first use.
-//   warp 1      TMEM owner + MMA issuer.
-//   warp 2      Q loader: each slot has two Q buffers, so the next item's Q tiles arrive
-//               while the current item runs; the K/V stream never waits for them.
-//   warp 3      O store issuer: TMA-stores each finished O tile from its staging buffer
-//               and then frees that Q buffer.
+//   warp 0      K/V producer: per item, K_0, V_0, K_1, V_1, ... into an mbarrier ring; a
+//               stage is free again once both slots released it (the producer itself
+//               gives the release for tiles only Q1 uses).
+//   warp 1      TMEM owner + MMA issuer of slot 0;  warp 2  MMA issuer of slot 1.
+//   warp 3      Q loader and O store issuer: each slot has two Q buffers, so the next
+//               item's Q tiles arrive while the current item runs; a finished O tile is
+//               staged in its item's Q buffer and TMA-stored from there.
 //   warps 4-7   softmax + epilogue of Q0;  warps 8-11  softmax + epilogue of Q1.
-// The epilogue writes O / l as fp16 into the item's own Q buffer (no longer read once the
-// slot's last QK has completed) in the 128-byte-swizzled layout the TMA store reads.
 #pragma once
 
 #include "attn_fwd_kernel.cuh"
@@ -45,13 +43,13 @@ struct PPCfg {
   static constexpr int NQBUF = 4;                    // Q buffers: 2 slots x 2 items
   static constexpr int NST_FIT = (TILE_BUDGET - NQBUF * TILE) / TILE;
   static constexpr int NST = NST_FIT > 12 ? 12 : NST_FIT;
-  // barrier indices (per slot a and buffer b: index a * 2 + b)
+  // barrier indices (per slot a and Q buffer b: index a * 2 + b)
   static constexpr int B_QFULL = 0, B_QEMPTY = 4, B_FULL = 8, B_EMPTY = 8 + NST;
   static constexpr int B_SFULL = 8 + 2 * NST, B_PFULL = B_SFULL + 2, B_OFINAL = B_PFULL + 2;
   // EPI is per (slot, Q buffer): an epilogue can only finish into a buffer after the store
   // of that buffer's previous tile freed it, so its phases cannot run ahead of the issuer.
   static constexpr int B_OFREE = B_OFINAL + 2, B_EPI = B_OFREE + 2, B_DRAIN = B_EPI + 4;
-  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr int NBAR = B_DRAIN + 2;
   static constexpr int TILE_BYTES = NST * TILE + NQBUF * TILE;
   static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + 8 * NBAR + 16;
   static constexpr int O_COL = 256;
@@ -60,7 +58,7 @@ struct PPCfg {
   static constexpr uint32_t IDESC_PV = idesc_f16_f32(128, D, 0, 1);
   static constexpr int kLaunchRegs = 168;  // 65536 / 384 rounded down to a multiple of 8
   static constexpr int kRegsLow = 104, kRegsHigh = 192;
-  static_assert(NST >= 3, "ring too shallow");
+  static_assert(NST >= 2, "ring too shallow");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(O_COL + 2 * D <= TMEM_COLS, "tensor memory budget");
 };
@@ -84,121 +82,35 @@ __device__ __forceinline__ PPItem pp_decode(int r, const FwdParams &p) {
   return it;
 }
 
-// Walk this CTA's operation stream, calling v.qk(slot, j, il, item) and
-// v.pv(slot, j, il, item) in issue order.  Returns false as soon as a visitor does.
-template <bool CAUSAL, class Visitor>
-__device__ __forceinline__ bool run_pp_stream(const FwdParams &p, const SchedTable *tbl, Visitor &v) {
-  Sched sc(blockIdx.x, gridDim.x, p.n_items, tbl);
-  int r;
-  if (!sc.next(r)) return true;
-  PPItem cur = pp_decode<CAUSAL>(r, p);
-  bool pre0 = false, pre1 = false;
-  for (int il = 0;; ++il) {
-    Sched peek = sc;
-    int rn;
-    const bool has_next = peek.next(rn);
-    const PPItem nxt = has_next ? pp_decode<CAUSAL>(rn, p) : cur;
-    if (!pre0 && !v.qk(0, 0, il, cur)) return false;
-    if (!pre1 && !v.qk(1, 0, il, cur)) return false;
-    bool npre0 = false, npre1 = false;
-    for (int j = 0; j < cur.n1; ++j) {
-      if (j < cur.n0) {
-        if (!v.pv(0, j, il, cur)) return false;
-        if (j + 1 < cur.n0) {
-          if (!v.qk(0, j + 1, il, cur)) return false;
-        } else if (has_next) {
-          if (!v.qk(0, 0, il + 1, nxt)) return false;
-          npre0 = true;
-        }
-      }
-      if (!v.pv(1, j, il, cur)) return false;
-      if (j + 1 < cur.n1) {
-        if (!v.qk(1, j + 1, il, cur)) return false;
-      } else if (has_next) {
-        if (!v.qk(1, 0, il + 1, nxt)) return false;
-        npre1 = true;
-      }
-    }
-    if (!has_next) break;
-    sc = peek;
-    cur = nxt;
-    pre0 = npre0;
-    pre1 = npre1;
-  }
-  return true;
-}
-
-// A K tile j is first used by QK0_j (or by QK1_j when j >= n0) and last used by QK1_j;
-// likewise V tile j by PV0_j / PV1_j.
-__device__ __forceinline__ bool pp_first_use(int slot, int j, const PPItem &it) {
-  return slot == 0 || j >= it.n0;
-}
-
 template <int D>
 __device__ __forceinline__ uint32_t pp_q_tile(uint32_t q_s, int slot, int il) {
   return q_s + static_cast<uint32_t>(slot * 2 + (il & 1)) * PPCfg<D>::TILE;
 }
 
-template <int D, bool CAUSAL>
-struct PPProducer {  // K/V only
-  using C = PPCfg<D>;
-  const CUtensorMap *tk, *tv;
-  const FwdParams *p;
-  uint32_t ring_s, bar_s;
-  volatile uint32_t *abort_flag;
-  uint32_t it = 0;  // ring positions issued
-  uint64_t pol_kv;
-  __device__ uint32_t bar(int i) const { return bar_s + 8u * static_cast<uint32_t>(i); }
-  __device__ bool load_tile(const CUtensorMap *tm, int j, int bh) {
-    const uint32_t s = it % C::NST, ph = (it / C::NST) & 1u;
-    if (!wait_bounded(bar(C::B_EMPTY + s), ph ^ 1u, abort_flag, p->status, kDevTimeoutLoad, p->wait_limit))
-      return false;
-    mbar_arrive_expect_tx(bar(C::B_FULL + s), C::TILE);
-#pragma unroll
-    for (int c = 0; c < C::NCH; ++c)
-      tma_load_3d_hint(ring_s + s * C::TILE + c * C::CHUNK, tm, c * 64, j * 128, bh, bar(C::B_FULL + s), pol_kv);
-    ++it;
-    return true;
-  }
-  __device__ bool qk(int slot, int j, int, const PPItem &item) {
-    return pp_first_use(slot, j, item) ? load_tile(tk, j, item.bh) : true;
-  }
-  __device__ bool pv(int slot, int j, int, const PPItem &item) {
-    return pp_first_use(slot, j, item) ? load_tile(tv, j, item.bh) : true;
-  }
-};
-
+// MMA issuer of one slot.  Ring positions follow the producer's load order: item by item,
+// K_0, V_0, K_1, V_1, ... for the n1 key tiles of the item.
 template <int D, bool CAUSAL>
 struct PPIssuer {
   using C = PPCfg<D>;
   const FwdParams *p;
   uint32_t ring_s, q_s, bar_s, tmem;
   volatile uint32_t *abort_flag;
-  uint32_t it = 0;                 // ring positions consumed (first uses)
-  uint32_t kpos = 0, vpos = 0;     // ring position of the K / V tile awaiting its last use
-  uint32_t n_pv[2] = {0, 0};
+  int slot;
+  uint32_t base = 0;  // ring position of K_0 of the current item
+  uint32_t n_pv = 0;  // PVs of this slot so far (phase of its P barrier)
   __device__ uint32_t bar(int i) const { return bar_s + 8u * static_cast<uint32_t>(i); }
-  __device__ bool wait(int b, uint32_t ph) {
-    return wait_bounded(bar(b), ph, abort_flag, p->status, kDevTimeoutMma, p->wait_limit);
-  }
-  __device__ bool acquire(uint32_t &pos) {
-    pos = it++;
-    if (!wait(C::B_FULL + pos % C::NST, (pos / C::NST) & 1u)) return false;
+  __device__ bool wait_all(const WaitSet &ws) {
+    if (!ws.wait(abort_flag, p->status, kDevTimeoutMma, p->wait_limit)) return false;
     tc_fence_after();
     return true;
   }
-  __device__ bool qk(int slot, int j, int il, const PPItem &item) {
-    if (j == 0) {
-      if (!wait(C::B_QFULL + slot * 2 + (il & 1), (il >> 1) & 1)) return false;
-      tc_fence_after();
-    }
-    uint32_t pos;
-    if (pp_first_use(slot, j, item)) {
-      if (!acquire(pos)) return false;
-      if (slot == 0) kpos = pos;
-    } else {
-      pos = kpos;
-    }
+  // S_slot = Q_slot K_j^T, then release K_j's stage and signal the softmax.
+  __device__ bool qk(int j, int il, uint32_t item_base) {
+    const uint32_t pos = item_base + 2u * static_cast<uint32_t>(j);
+    WaitSet ws;
+    if (j == 0) ws.add(bar(C::B_QFULL + slot * 2 + (il & 1)), (il >> 1) & 1);
+    ws.add(bar(C::B_FULL + pos % C::NST), (pos / C::NST) & 1u);
+    if (!wait_all(ws)) return false;
     const SDesc a = sdesc_split(sdesc_sw128(pp_q_tile<D>(q_s, slot, il), 16, 1024));
     const SDesc b = sdesc_split(sdesc_sw128(ring_s + (pos % C::NST) * C::TILE, 16, 1024));
     const uint32_t d_tmem = tmem + slot * 128u;
@@ -209,30 +121,55 @@ struct PPIssuer {
         umma_ss_off(d_tmem, a, c * C::CHUNK + kk * 32, b, c * C::CHUNK + kk * 32, C::IDESC_QK,
                     (c | kk) != 0 ? 1u : 0u);
     umma_commit(bar(C::B_SFULL + slot));
-    if (slot == 1) umma_commit(bar(C::B_EMPTY + pos % C::NST));  // last use of this K tile
+    umma_commit(bar(C::B_EMPTY + pos % C::NST));
     return true;
   }
-  __device__ bool pv(int slot, int j, int il, const PPItem &item) {
-    if (!wait(C::B_PFULL + slot, n_pv[slot] & 1u)) return false;
-    if (j == 0 && il > 0 && !wait(C::B_OFREE + slot, (il - 1) & 1)) return false;
-    tc_fence_after();
-    uint32_t pos;
-    if (pp_first_use(slot, j, item)) {
-      if (!acquire(pos)) return false;
-      if (slot == 0) vpos = pos;
-    } else {
-      pos = vpos;
-    }
+  // O_slot (+)= P_slot V_j, then release V_j's stage (and signal the epilogue after the
+  // slot's last tile of the item).
+  __device__ bool pv(int j, int il, int n_slot) {
+    const uint32_t pos = base + 2u * static_cast<uint32_t>(j) + 1u;
+    WaitSet ws;
+    ws.add(bar(C::B_PFULL + slot), n_pv & 1u);
+    if (j == 0 && il > 0) ws.add(bar(C::B_OFREE + slot), (il - 1) & 1);
+    ws.add(bar(C::B_FULL + pos % C::NST), (pos / C::NST) & 1u);
+    if (!wait_all(ws)) return false;
     const SDesc b = sdesc_split(sdesc_sw128(ring_s + (pos % C::NST) * C::TILE, C::CHUNK, 1024));
     const uint32_t o_tmem = tmem + C::O_COL + slot * D;
     const uint32_t p_tmem = tmem + slot * 128u;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       umma_ts_off(o_tmem, p_tmem + kk * 8u, b, kk * 2048, C::IDESC_PV, (j == 0 && kk == 0) ? 0u : 1u);
-    if (slot == 1) umma_commit(bar(C::B_EMPTY + pos % C::NST));  // last use of this V tile
-    if (j == (slot == 0 ? item.n0 : item.n1) - 1) umma_commit(bar(C::B_OFINAL + slot));
-    ++n_pv[slot];
+    umma_commit(bar(C::B_EMPTY + pos % C::NST));
+    if (j == n_slot - 1) umma_commit(bar(C::B_OFINAL + slot));
+    ++n_pv;
     return true;
+  }
+  __device__ void run(const SchedTable *tbl) {
+    Sched sc(blockIdx.x, gridDim.x, p->n_items, tbl);
+    int r;
+    if (!sc.next(r)) return;
+    PPItem cur = pp_decode<CAUSAL>(r, *p);
+    if (!qk(0, 0, 0)) return;
+    for (int il = 0;; ++il) {
+      Sched peek = sc;
+      int rn;
+      const bool has_next = peek.next(rn);
+      const PPItem nxt = has_next ? pp_decode<CAUSAL>(rn, *p) : cur;
+      const int n = slot == 0 ? cur.n0 : cur.n1;
+      const uint32_t next_base = base + 2u * static_cast<uint32_t>(cur.n1);
+      for (int j = 0; j < n; ++j) {
+        if (!pv(j, il, n)) return;
+        if (j + 1 < n) {
+          if (!qk(j + 1, il, base)) return;
+        } else if (has_next) {
+          if (!qk(0, il + 1, next_base)) return;
+        }
+      }
+      if (!has_next) return;
+      sc = peek;
+      cur = nxt;
+      base = next_base;
+    }
   }
 };
 
@@ -266,12 +203,12 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(BAR(C::B_PFULL + i), 128);
       mbar_init(BAR(C::B_OFINAL + i), 1);
       mbar_init(BAR(C::B_OFREE + i), 128);
+      mbar_init(BAR(C::B_DRAIN + i), 1);
     }
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(BAR(C::B_FULL + i), 1);
-      mbar_init(BAR(C::B_EMPTY + i), 1);
+      mbar_init(BAR(C::B_EMPTY + i), 2);  // one release per slot
     }
-    mbar_init(BAR(C::B_DRAIN), 1);
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -297,20 +234,32 @@ __global__ void __launch_bounds__(384, 1)
     setmaxnreg_dec<PPCfg<D>::kRegsLow>();
     if (warp == 0 && lane == 0) {
       // ---------------------------------------------------------- K/V producer
-      PPProducer<D, CAUSAL> pr;
-      pr.tk = &tm_k;
-      pr.tv = &tm_v;
-      pr.p = &p;
-      pr.ring_s = ring_s;
-      pr.bar_s = bar_s;
-      pr.abort_flag = abort_flag;
-      pr.pol_kv = policy_evict_last();
-      run_pp_stream<CAUSAL>(p, &tbl, pr);
+      const uint64_t pol_kv = policy_evict_last();
+      Sched sc(blockIdx.x, gridDim.x, p.n_items, &tbl);
+      uint32_t it = 0;
+      int r;
+      bool ok = true;
+      while (ok && sc.next(r)) {
+        const PPItem item = pp_decode<CAUSAL>(r, p);
+        for (int j = 0; j < item.n1 && ok; ++j)
+          for (int kv = 0; kv < 2 && ok; ++kv, ++it) {
+            const uint32_t s = it % C::NST, ph = (it / C::NST) & 1u;
+            if (!(ok = wait_bounded(BAR(C::B_EMPTY + s), ph ^ 1u, abort_flag, p.status, kDevTimeoutLoad, LIM)))
+              break;
+            mbar_arrive_expect_tx(BAR(C::B_FULL + s), C::TILE);
+            const CUtensorMap *tm = kv == 0 ? &tm_k : &tm_v;
+#pragma unroll
+            for (int c = 0; c < C::NCH; ++c)
+              tma_load_3d_hint(ring_s + s * C::TILE + c * C::CHUNK, tm, c * 64, j * 128, item.bh, BAR(C::B_FULL + s),
+                               pol_kv);
+            if (j >= item.n0) mbar_arrive(BAR(C::B_EMPTY + s));  // Q0 never uses this tile
+          }
+      }
       // Drain: every load issued must have landed before the CTA may exit.
-      const uint32_t first = pr.it > static_cast<uint32_t>(C::NST) ? pr.it - C::NST : 0u;
-      for (uint32_t i = first; i < pr.it; ++i) wait_drain(BAR(C::B_FULL + (i % C::NST)), (i / C::NST) & 1u, LIM);
-    } else if (warp == 1 && lane == 0) {
-      // ---------------------------------------------------------- MMA issuer
+      const uint32_t first = it > static_cast<uint32_t>(C::NST) ? it - C::NST : 0u;
+      for (uint32_t i = first; i < it; ++i) wait_drain(BAR(C::B_FULL + (i % C::NST)), (i / C::NST) & 1u, LIM);
+    } else if ((warp == 1 || warp == 2) && lane == 0) {
+      // ---------------------------------------------------------- MMA issuers
       PPIssuer<D, CAUSAL> is;
       is.p = &p;
       is.ring_s = ring_s;
@@ -318,56 +267,63 @@ __global__ void __launch_bounds__(384, 1)
       is.bar_s = bar_s;
       is.tmem = tmem;
       is.abort_flag = abort_flag;
-      run_pp_stream<CAUSAL>(p, &tbl, is);
-      umma_commit(BAR(C::B_DRAIN));
-      wait_drain(BAR(C::B_DRAIN), 0, LIM);
-    } else if (warp == 2 && lane == 0) {
-      // ---------------------------------------------------------- Q loader
+      is.slot = warp - 1;
+      is.run(&tbl);
+      // Drain: all MMAs issued by this thread complete before tensor memory is freed.
+      umma_commit(BAR(C::B_DRAIN + is.slot));
+      wait_drain(BAR(C::B_DRAIN + is.slot), 0, LIM);
+    } else if (warp == 3 && lane == 0) {
+      // ---------------------------------------------------------- Q loads and O stores
       const uint64_t pol_q = policy_evict_first();
       Sched sc(blockIdx.x, gridDim.x, p.n_items, &tbl);
-      int il = 0, r;
+      int r, il = 0, q_loads = 0;
       bool ok = true;
-      while (ok && sc.next(r)) {
-        const PPItem item = pp_decode<CAUSAL>(r, p);
-        for (int a = 0; a < 2 && ok; ++a) {
-          const int b = a * 2 + (il & 1);
-          if (!(ok = wait_bounded(BAR(C::B_QEMPTY + b), ((il >> 1) & 1) ^ 1u, abort_flag, p.status,
-                                  kDevTimeoutLoad, LIM)))
-            break;
+      auto load_q = [&](int ql, const PPItem &item) -> bool {
+        for (int a = 0; a < 2; ++a) {
+          const int b = a * 2 + (ql & 1);
+          if (!wait_bounded(BAR(C::B_QEMPTY + b), ((ql >> 1) & 1) ^ 1u, abort_flag, p.status, kDevTimeoutLoad, LIM))
+            return false;
           mbar_arrive_expect_tx(BAR(C::B_QFULL + b), C::TILE);
-          const uint32_t dst = pp_q_tile<D>(q_s, a, il);
+          const uint32_t dst = pp_q_tile<D>(q_s, a, ql);
           for (int c = 0; c < C::NCH; ++c)
             tma_load_3d_hint(dst + c * C::CHUNK, &tm_q, c * 64, item.qb * 256 + a * 128, item.bh,
                              BAR(C::B_QFULL + b), pol_q);
         }
-        ++il;
-      }
-      // Drain the Q loads of the last two items.
-      for (int i = (il > 2 ? il - 2 : 0); i < il; ++i)
-        for (int a = 0; a < 2; ++a) wait_drain(BAR(C::B_QFULL + a * 2 + (i & 1)), (i >> 1) & 1, LIM);
-    } else if (warp == 3 && lane == 0) {
-      // ---------------------------------------------------------- O store issuer
-      Sched sc(blockIdx.x, gridDim.x, p.n_items, &tbl);
-      int il = 0, r;
-      bool ok = true;
-      while (ok && sc.next(r)) {
-        const PPItem item = pp_decode<CAUSAL>(r, p);
-        for (int a = 0; a < 2 && ok; ++a) {
-          if (!(ok = wait_bounded(BAR(C::B_EPI + a * 2 + (il & 1)), (il >> 1) & 1, abort_flag, p.status,
-                                  kDevTimeoutEpilogue, LIM)))
-            break;
-          const int qrow0 = item.qb * 256 + a * 128;
-          if (qrow0 < p.L) {
-            const uint32_t src = pp_q_tile<D>(q_s, a, il);
-            for (int c = 0; c < C::NCH; ++c) tma_store_3d(&tm_o, src + c * C::CHUNK, c * 64, qrow0, item.bh);
-            bulk_commit();
-            bulk_wait_read0();
+        q_loads = ql + 1;
+        return true;
+      };
+      if (sc.next(r)) {
+        PPItem cur = pp_decode<CAUSAL>(r, p);
+        ok = load_q(0, cur);
+        while (ok) {
+          Sched peek = sc;
+          int rn;
+          const bool has_next = peek.next(rn);
+          const PPItem nxt = has_next ? pp_decode<CAUSAL>(rn, p) : cur;
+          if (has_next && !(ok = load_q(il + 1, nxt))) break;  // next item's Q while this one runs
+          for (int a = 0; a < 2 && ok; ++a) {
+            if (!(ok = wait_bounded(BAR(C::B_EPI + a * 2 + (il & 1)), (il >> 1) & 1, abort_flag, p.status,
+                                    kDevTimeoutEpilogue, LIM)))
+              break;
+            const int qrow0 = cur.qb * 256 + a * 128;
+            if (qrow0 < p.L) {
+              const uint32_t src = pp_q_tile<D>(q_s, a, il);
+              for (int c = 0; c < C::NCH; ++c) tma_store_3d(&tm_o, src + c * C::CHUNK, c * 64, qrow0, cur.bh);
+              bulk_commit();
+              bulk_wait_read0();
+            }
+            mbar_arrive(BAR(C::B_QEMPTY + a * 2 + (il & 1)));  // the staging buffer may be refilled
           }
-          mbar_arrive(BAR(C::B_QEMPTY + a * 2 + (il & 1)));  // the staging buffer may be refilled
+          if (!has_next) break;
+          sc = peek;
+          cur = nxt;
+          ++il;
         }
-        ++il;
       }
       bulk_wait0();
+      // Drain the Q loads of the last two items.
+      for (int i = (q_loads > 2 ? q_loads - 2 : 0); i < q_loads; ++i)
+        for (int a = 0; a < 2; ++a) wait_drain(BAR(C::B_QFULL + a * 2 + (i & 1)), (i >> 1) & 1, LIM);
     }
     __syncwarp();
   } else {

@@ -11,9 +11,9 @@
 // LSE = (m + log2 l) * ln 2 do not depend on when m was raised.
 //
 // Latency, not arithmetic, bounds this step (one warp per scheduler per Q tile), so:
-// the second half of S is loaded while the max over the first half runs; the max uses
-// eight independent chains of three-input max; s * c2 - m uses packed f32x2 FMA; the row
-// sum uses four packed f32x2 partial sums.
+// both halves of S are read with one wait; the max uses eight independent chains of
+// three-input max; s * c2 - m uses packed f32x2 FMA; the row sum uses four packed f32x2
+// partial sums; the first half of P is stored while the second half is computed.
 #pragma once
 
 #include "ptx.cuh"
@@ -34,8 +34,11 @@ template <int DV, class Hook = NoWait>
 __device__ __forceinline__ bool softmax_tile(uint32_t s_tmem, uint32_t o_tmem, int lim, float c2, bool first,
                                              float &m_used, float &l, const Hook &before_rescale = Hook()) {
   uint32_t ra[64], rb[64];
-  tmem_ld32x64(s_tmem, ra);
+  // Both halves of S in flight at once, then one wait.
+  tmem_ld32x64_async(s_tmem, ra);
   tmem_ld32x64_async(s_tmem + 64, rb);
+  tmem_wait_ld_fence64(ra);
+  tmem_wait_ld_fence64(rb);
   float *sa = reinterpret_cast<float *>(ra);
   if (lim < 64) {
 #pragma unroll
@@ -50,7 +53,6 @@ __device__ __forceinline__ bool softmax_tile(uint32_t s_tmem, uint32_t o_tmem, i
     mk[k] = fmax3(mk[k], sa[8 * k + 5], sa[8 * k + 6]);
     mk[k] = fmaxf(mk[k], sa[8 * k + 7]);
   }
-  tmem_wait_ld_fence64(rb);
   float *sb = reinterpret_cast<float *>(rb);
   if (lim < 128) {
 #pragma unroll
@@ -90,28 +92,32 @@ __device__ __forceinline__ bool softmax_tile(uint32_t s_tmem, uint32_t o_tmem, i
   uint64_t acc[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = f32x2(0.f, 0.f);
-  uint32_t pk[64];
+  // P in two halves: the first half's store is in flight while the second is computed.
+  uint32_t pa[32], pb[32];
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
     float x0, x1;
     f32x2_split(ffma2(f32x2(sa[2 * c], sa[2 * c + 1]), c2x2, negm), x0, x1);
     const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
     acc[c & 3] = fadd2(acc[c & 3], f32x2(p0, p1));
-    pk[c] = pack_f16x2(p0, p1);
+    pa[c] = pack_f16x2(p0, p1);
   }
+  tmem_st32x32_async(s_tmem, pa);
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
     float x0, x1;
     f32x2_split(ffma2(f32x2(sb[2 * c], sb[2 * c + 1]), c2x2, negm), x0, x1);
     const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
     acc[c & 3] = fadd2(acc[c & 3], f32x2(p0, p1));
-    pk[32 + c] = pack_f16x2(p0, p1);
+    pb[c] = pack_f16x2(p0, p1);
   }
+  tmem_st32x32_async(s_tmem + 32, pb);
   const uint64_t s01 = fadd2(acc[0], acc[1]), s23 = fadd2(acc[2], acc[3]);
   float lo, hi;
   f32x2_split(fadd2(s01, s23), lo, hi);
   l += lo + hi;
-  tmem_st32x64(s_tmem, pk);
+  tmem_wait_st_fence32(pa);
+  tmem_wait_st_fence32(pb);
   return true;
 }
 
