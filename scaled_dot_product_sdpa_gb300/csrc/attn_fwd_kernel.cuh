@@ -259,6 +259,10 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The prologue above touches no global memory: the next kernel may launch now, and this
+  // one waits here for the previous kernel's writes (inputs may be its outputs).
+  grid_launch_dependents();
+  grid_wait_prior();
   const long long LIM = p.wait_limit;
 
   if (warp == 0) {
@@ -517,6 +521,23 @@ __global__ void __launch_bounds__(256, 1)
   }
 }
 
+// Launch with programmatic stream serialization: the kernel may begin (prologue only, see
+// grid_wait_prior) while the previous kernel in the stream is still finishing.
+template <class Kern, class... Args>
+cudaError_t launch_pdl(Kern kern, int grid, int block, int smem, cudaStream_t stream, const Args &...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Launch description shared by the per-head-dim translation units and the ABI.
 struct FwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_o;
@@ -541,8 +562,7 @@ cudaError_t launch_fwd_variant(const FwdLaunch &a) {
     if (e != cudaSuccess) return e;
     if (dev < 31) configured_mask |= (1 << dev);
   }
-  kern<<<a.grid, 256, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p, *a.tbl);
-  return cudaGetLastError();
+  return launch_pdl(kern, a.grid, 256, C::SMEM_BYTES, a.stream, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p, *a.tbl);
 }
 
 template <int D>

@@ -224,6 +224,10 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The prologue above touches no global memory: the next kernel may launch now, and this
+  // one waits here for the previous kernel's writes (inputs may be its outputs).
+  grid_launch_dependents();
+  grid_wait_prior();
 
   // Register split: the launch gives every thread kLaunchRegs; the warpgroup of the four
   // single-thread roles (warps 0-3) gives up registers that the two softmax warpgroups
@@ -424,8 +428,7 @@ cudaError_t launch_fwd_pp_variant(const FwdLaunch &a) {
     if (e != cudaSuccess) return e;
     if (dev < 31) configured_mask |= (1 << dev);
   }
-  kern<<<a.grid, 384, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p, *a.tbl);
-  return cudaGetLastError();
+  return launch_pdl(kern, a.grid, 384, C::SMEM_BYTES, a.stream, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p, *a.tbl);
 }
 
 template <int D>

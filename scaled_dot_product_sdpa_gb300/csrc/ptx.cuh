@@ -215,6 +215,15 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
                : "memory");
 }
 
+// ----------------------------------------------------------------------------- grid dependencies
+// Programmatic dependent launch: let the next kernel in the stream start its launch and
+// prologue now; and wait until the previous kernel in the stream has completed and its
+// memory is visible (a no-op when the launch has no programmatic dependency).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ----------------------------------------------------------------------------- registers
 // Warpgroup-wide register re-allocation (every thread of the 4 warps executes it).
 template <int N>
