@@ -23,10 +23,17 @@
 //               stage is free again once both slots released it (the producer itself
 //               gives the release for tiles only Q1 uses).
 //   warp 1      TMEM owner + MMA issuer of slot 0;  warp 2  MMA issuer of slot 1.
-//   warp 3      Q loader and O store issuer: each slot has two Q buffers, so the next
-//               item's Q tiles arrive while the current item runs; a finished O tile is
-//               staged in its item's Q buffer and TMA-stored from there.
+//   warp 3      Q loader and O store issuer.  Each slot has one Q buffer, released by the
+//               commit of the slot's last QK of an item, so the next item's Q tile lands
+//               while the last softmax and PV of the current one run.  Finished O tiles
+//               go through one staging buffer that the slots take in turn (slot 0, then
+//               slot 1, item by item): the store issuer grants it to a slot, the slot's
+//               epilogue fills it, the issuer TMA-stores it and grants it to the other.
 //   warps 4-7   softmax + epilogue of Q0;  warps 8-11  softmax + epilogue of Q1.
+//
+// Shared memory: [K/V ring: NST tiles][Q0][Q1][O staging][barriers].  One Q buffer per
+// slot and a single staging buffer leave room for a deeper ring (4 stages at D = 128):
+// the ring's depth is what hides the latency of the K/V loads.
 #pragma once
 
 #include "attn_fwd_kernel.cuh"
@@ -40,17 +47,19 @@ struct PPCfg {
   static constexpr int CHUNK = 128 * 128;            // bytes of a 128-row x 64-col fp16 box
   static constexpr int TILE = NCH * CHUNK;           // one 128 x D tile
   static constexpr int TILE_BUDGET = 224 * 1024;
-  static constexpr int NQBUF = 4;                    // Q buffers: 2 slots x 2 items
-  static constexpr int NST_FIT = (TILE_BUDGET - NQBUF * TILE) / TILE;
+  static constexpr int NQBUF = 2;                    // Q buffers: one per slot
+  static constexpr int NOBUF = 1;                    // O staging buffer, shared by the slots
+  static constexpr int NST_FIT = (TILE_BUDGET - (NQBUF + NOBUF) * TILE) / TILE;
   static constexpr int NST = NST_FIT > 12 ? 12 : NST_FIT;
-  // barrier indices (per slot a and Q buffer b: index a * 2 + b)
-  static constexpr int B_QFULL = 0, B_QEMPTY = 4, B_FULL = 8, B_EMPTY = 8 + NST;
-  static constexpr int B_SFULL = 8 + 2 * NST, B_PFULL = B_SFULL + 2, B_OFINAL = B_PFULL + 2;
-  // EPI is per (slot, Q buffer): an epilogue can only finish into a buffer after the store
-  // of that buffer's previous tile freed it, so its phases cannot run ahead of the issuer.
-  static constexpr int B_OFREE = B_OFINAL + 2, B_EPI = B_OFREE + 2, B_DRAIN = B_EPI + 4;
+  // barrier indices (per slot a: index + a).  GRANT[a] hands the staging buffer to slot
+  // a's epilogue, EPI[a] hands the filled buffer back; each completes once per item of the
+  // slot, in order, so a parity wait on either can never be two phases behind.
+  static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_FULL = 4, B_EMPTY = 4 + NST;
+  static constexpr int B_SFULL = 4 + 2 * NST, B_PFULL = B_SFULL + 2, B_OFINAL = B_PFULL + 2;
+  static constexpr int B_OFREE = B_OFINAL + 2, B_GRANT = B_OFREE + 2, B_EPI = B_GRANT + 2;
+  static constexpr int B_DRAIN = B_EPI + 2;
   static constexpr int NBAR = B_DRAIN + 2;
-  static constexpr int TILE_BYTES = NST * TILE + NQBUF * TILE;
+  static constexpr int TILE_BYTES = NST * TILE + (NQBUF + NOBUF) * TILE;
   static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + 8 * NBAR + 16;
   static constexpr int O_COL = 256;
   static constexpr int TMEM_COLS = 512;
@@ -83,8 +92,8 @@ __device__ __forceinline__ PPItem pp_decode(int r, const FwdParams &p) {
 }
 
 template <int D>
-__device__ __forceinline__ uint32_t pp_q_tile(uint32_t q_s, int slot, int il) {
-  return q_s + static_cast<uint32_t>(slot * 2 + (il & 1)) * PPCfg<D>::TILE;
+__device__ __forceinline__ uint32_t pp_q_tile(uint32_t q_s, int slot) {
+  return q_s + static_cast<uint32_t>(slot) * PPCfg<D>::TILE;
 }
 
 // MMA issuer of one slot.  Ring positions follow the producer's load order: item by item,
@@ -104,14 +113,15 @@ struct PPIssuer {
     tc_fence_after();
     return true;
   }
-  // S_slot = Q_slot K_j^T, then release K_j's stage and signal the softmax.
-  __device__ bool qk(int j, int il, uint32_t item_base) {
+  // S_slot = Q_slot K_j^T, then release K_j's stage and signal the softmax; after the
+  // slot's last key tile of the item (`last`) the Q buffer is released too.
+  __device__ bool qk(int j, int il, uint32_t item_base, bool last) {
     const uint32_t pos = item_base + 2u * static_cast<uint32_t>(j);
     WaitSet ws;
-    if (j == 0) ws.add(bar(C::B_QFULL + slot * 2 + (il & 1)), (il >> 1) & 1);
+    if (j == 0) ws.add(bar(C::B_QFULL + slot), il & 1);
     ws.add(bar(C::B_FULL + pos % C::NST), (pos / C::NST) & 1u);
     if (!wait_all(ws)) return false;
-    const SDesc a = sdesc_split(sdesc_sw128(pp_q_tile<D>(q_s, slot, il), 16, 1024));
+    const SDesc a = sdesc_split(sdesc_sw128(pp_q_tile<D>(q_s, slot), 16, 1024));
     const SDesc b = sdesc_split(sdesc_sw128(ring_s + (pos % C::NST) * C::TILE, 16, 1024));
     const uint32_t d_tmem = tmem + slot * 128u;
 #pragma unroll
@@ -122,6 +132,7 @@ struct PPIssuer {
                     (c | kk) != 0 ? 1u : 0u);
     umma_commit(bar(C::B_SFULL + slot));
     umma_commit(bar(C::B_EMPTY + pos % C::NST));
+    if (last) umma_commit(bar(C::B_QEMPTY + slot));
     return true;
   }
   // O_slot (+)= P_slot V_j, then release V_j's stage (and signal the epilogue after the
@@ -149,20 +160,21 @@ struct PPIssuer {
     int r;
     if (!sc.next(r)) return;
     PPItem cur = pp_decode<CAUSAL>(r, *p);
-    if (!qk(0, 0, 0)) return;
+    if (!qk(0, 0, 0, (slot == 0 ? cur.n0 : cur.n1) == 1)) return;
     for (int il = 0;; ++il) {
       Sched peek = sc;
       int rn;
       const bool has_next = peek.next(rn);
       const PPItem nxt = has_next ? pp_decode<CAUSAL>(rn, *p) : cur;
       const int n = slot == 0 ? cur.n0 : cur.n1;
+      const int n_next = slot == 0 ? nxt.n0 : nxt.n1;
       const uint32_t next_base = base + 2u * static_cast<uint32_t>(cur.n1);
       for (int j = 0; j < n; ++j) {
         if (!pv(j, il, n)) return;
         if (j + 1 < n) {
-          if (!qk(j + 1, il, base)) return;
+          if (!qk(j + 1, il, base, j + 2 == n)) return;
         } else if (has_next) {
-          if (!qk(0, il + 1, next_base)) return;
+          if (!qk(0, il + 1, next_base, n_next == 1)) return;
         }
       }
       if (!has_next) return;
@@ -184,8 +196,9 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *const base_ptr = smem_raw + (base - raw);
   const uint32_t ring_s = base;                     // NST x TILE (first: see attn_fwd_kernel.cuh)
-  const uint32_t q_s = ring_s + C::NST * C::TILE;   // Q[slot][item parity], also O staging
-  const uint32_t bar_s = q_s + C::NQBUF * C::TILE;  // NBAR x 8
+  const uint32_t q_s = ring_s + C::NST * C::TILE;   // Q[slot]
+  const uint32_t o_s = q_s + C::NQBUF * C::TILE;    // O staging
+  const uint32_t bar_s = o_s + C::NOBUF * C::TILE;  // NBAR x 8
   uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + (bar_s - base) + 8 * C::NBAR);
   volatile uint32_t *const abort_flag = tmem_slot + 1;
   auto BAR = [&](int i) -> uint32_t { return bar_s + 8u * static_cast<uint32_t>(i); };
@@ -193,12 +206,11 @@ __global__ void __launch_bounds__(384, 1)
   const long long LIM = p.wait_limit;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(BAR(C::B_QFULL + i), 1);
       mbar_init(BAR(C::B_QEMPTY + i), 1);
+      mbar_init(BAR(C::B_GRANT + i), 1);
       mbar_init(BAR(C::B_EPI + i), 128);
-    }
-    for (int i = 0; i < 2; ++i) {
       mbar_init(BAR(C::B_SFULL + i), 1);
       mbar_init(BAR(C::B_PFULL + i), 128);
       mbar_init(BAR(C::B_OFINAL + i), 1);
@@ -280,44 +292,46 @@ __global__ void __launch_bounds__(384, 1)
       // ---------------------------------------------------------- Q loads and O stores
       const uint64_t pol_q = policy_evict_first();
       Sched sc(blockIdx.x, gridDim.x, p.n_items, &tbl);
-      int r, il = 0, q_loads = 0;
+      int r, il = 0;
+      int nq[2] = {0, 0};  // Q loads issued per buffer
       bool ok = true;
-      auto load_q = [&](int ql, const PPItem &item) -> bool {
-        for (int a = 0; a < 2; ++a) {
-          const int b = a * 2 + (ql & 1);
-          if (!wait_bounded(BAR(C::B_QEMPTY + b), ((ql >> 1) & 1) ^ 1u, abort_flag, p.status, kDevTimeoutLoad, LIM))
-            return false;
-          mbar_arrive_expect_tx(BAR(C::B_QFULL + b), C::TILE);
-          const uint32_t dst = pp_q_tile<D>(q_s, a, ql);
-          for (int c = 0; c < C::NCH; ++c)
-            tma_load_3d_hint(dst + c * C::CHUNK, &tm_q, c * 64, item.qb * 256 + a * 128, item.bh,
-                             BAR(C::B_QFULL + b), pol_q);
-        }
-        q_loads = ql + 1;
+      // Slot a's Q tile of the ql-th item, once the slot's last QK of item ql-1 released
+      // the buffer.
+      auto load_q = [&](int a, int ql, const PPItem &item) -> bool {
+        if (!wait_bounded(BAR(C::B_QEMPTY + a), (ql & 1) ^ 1u, abort_flag, p.status, kDevTimeoutLoad, LIM))
+          return false;
+        mbar_arrive_expect_tx(BAR(C::B_QFULL + a), C::TILE);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d_hint(pp_q_tile<D>(q_s, a) + c * C::CHUNK, &tm_q, c * 64, item.qb * 256 + a * 128, item.bh,
+                           BAR(C::B_QFULL + a), pol_q);
+        ++nq[a];
         return true;
       };
+      // Slot a's O tile of the ol-th item, once its epilogue staged it; then the staging
+      // buffer goes to the other slot.
+      auto store_o = [&](int a, int ol, const PPItem &item) -> bool {
+        if (!wait_bounded(BAR(C::B_EPI + a), ol & 1, abort_flag, p.status, kDevTimeoutEpilogue, LIM)) return false;
+        const int qrow0 = item.qb * 256 + a * 128;
+        if (qrow0 < p.L) {
+          for (int c = 0; c < C::NCH; ++c) tma_store_3d(&tm_o, o_s + c * C::CHUNK, c * 64, qrow0, item.bh);
+          bulk_commit();
+          bulk_wait_read0();
+        }
+        mbar_arrive(BAR(C::B_GRANT + (a ^ 1)));
+        return true;
+      };
+      mbar_arrive(BAR(C::B_GRANT + 0));  // slot 0's first epilogue has the buffer
       if (sc.next(r)) {
         PPItem cur = pp_decode<CAUSAL>(r, p);
-        ok = load_q(0, cur);
+        ok = load_q(0, 0, cur) && load_q(1, 0, cur);
         while (ok) {
           Sched peek = sc;
           int rn;
           const bool has_next = peek.next(rn);
           const PPItem nxt = has_next ? pp_decode<CAUSAL>(rn, p) : cur;
-          if (has_next && !(ok = load_q(il + 1, nxt))) break;  // next item's Q while this one runs
-          for (int a = 0; a < 2 && ok; ++a) {
-            if (!(ok = wait_bounded(BAR(C::B_EPI + a * 2 + (il & 1)), (il >> 1) & 1, abort_flag, p.status,
-                                    kDevTimeoutEpilogue, LIM)))
-              break;
-            const int qrow0 = cur.qb * 256 + a * 128;
-            if (qrow0 < p.L) {
-              const uint32_t src = pp_q_tile<D>(q_s, a, il);
-              for (int c = 0; c < C::NCH; ++c) tma_store_3d(&tm_o, src + c * C::CHUNK, c * 64, qrow0, cur.bh);
-              bulk_commit();
-              bulk_wait_read0();
-            }
-            mbar_arrive(BAR(C::B_QEMPTY + a * 2 + (il & 1)));  // the staging buffer may be refilled
-          }
+          // The next item's Q tiles first (they gate its first QKs), then this item's O.
+          if (has_next && !(ok = load_q(0, il + 1, nxt) && load_q(1, il + 1, nxt))) break;
+          if (!(ok = store_o(0, il, cur) && store_o(1, il, cur))) break;
           if (!has_next) break;
           sc = peek;
           cur = nxt;
@@ -325,9 +339,9 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       bulk_wait0();
-      // Drain the Q loads of the last two items.
-      for (int i = (q_loads > 2 ? q_loads - 2 : 0); i < q_loads; ++i)
-        for (int a = 0; a < 2; ++a) wait_drain(BAR(C::B_QFULL + a * 2 + (i & 1)), (i >> 1) & 1, LIM);
+      // Drain: the last Q load into each buffer must have landed (earlier ones were read).
+      for (int a = 0; a < 2; ++a)
+        if (nq[a] > 0) wait_drain(BAR(C::B_QFULL + a), (nq[a] - 1) & 1, LIM);
     }
     __syncwarp();
   } else {
@@ -366,11 +380,12 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok) break;
       // --------------------------------------------------------------- epilogue
-      // O / l as fp16 into this tile's Q buffer (swizzled like a TMA box), then the store
-      // issuer writes it out; LSE goes straight to global memory.
+      // O / l as fp16 into the staging buffer once it is granted to this slot (swizzled like
+      // a TMA box), then the store issuer writes it out; LSE goes straight to global memory.
       if (!(ok = wait_warp(BAR(C::B_OFINAL + slot), il & 1))) break;
+      if (!(ok = wait_warp(BAR(C::B_GRANT + slot), il & 1))) break;  // the staging buffer is ours
       tc_fence_after();
-      const uint32_t stage = pp_q_tile<D>(q_s, slot, il);
+      const uint32_t stage = o_s;
       const float inv_l = 1.0f / l;
 #pragma unroll 1
       for (int c32 = 0; c32 < D / 32; ++c32) {
@@ -396,7 +411,7 @@ __global__ void __launch_bounds__(384, 1)
       if (grow < p.L)
         p.lse[static_cast<long long>(item.bh) * p.L + grow] = (m_used + __log2f(l)) * 0.69314718055994531f;
       fence_proxy_async_smem();
-      mbar_arrive(BAR(C::B_EPI + slot * 2 + (il & 1)));
+      mbar_arrive(BAR(C::B_EPI + slot));
       ++il;
     }
   }
