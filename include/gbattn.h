@@ -73,8 +73,9 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
  *   two-tile kernel (d <= 128 only): each work item is a 256-row query block whose two
  *     128-row halves share every K/V tile and have their own softmax warpgroup;
  *   single-tile kernel (every d): each work item is one 128-row query tile.
- * With flags = 0, attn_fwd picks the two-tile kernel for d <= 128 when it has at least
- * two items per SM, else the single-tile kernel.  Options:
+ * With flags = 0: d > 128 uses the single-tile kernel; d <= 128 the two-tile kernel when
+ * it has at least two items per SM, else whichever of the two kernels has the shorter
+ * estimated schedule.  Options:
  *   flags bit 0 (GBATTN_FLAG_P_SMEM): single-tile kernel, with P staged through shared
  *     memory instead of tensor memory before the PV product (the SMEM-P path of the
  *     STAGE_D.md notes, section 4); only for d <= 128, otherwise GBATTN_ERR_HEAD_DIM.
@@ -128,6 +129,17 @@ int attn_debug_wait_probe(long long limit_cycles, void *stream);
  */
 int attn_debug_schedule(int B, int H, int L, int d, int causal, int grid, int flags, int *start, int *items,
                         int max_items);
+
+/*
+ * attn_debug_plan -- test hook: the kernel attn_fwd_ex would launch for this shape,
+ * `flags` and `grid_limit` on a GPU with `sm_count` SMs (host-only; needs no GPU).
+ * Fills out[0] = kernel (0 single-tile, 1 two-tile), out[1] = work items, out[2] = CTAs,
+ * out[3] = estimated makespan x 100 (in units of one tile step of a query tile in the
+ * two-tile kernel; -100 when the kernels use their fixed order).
+ * Returns 0 or a negative GBATTN_ERR_* code.
+ */
+int attn_debug_plan(int B, int H, int L, int d, int causal, int sm_count, int flags, int grid_limit,
+                    int *out);
 
 /* Human-readable text for a GBATTN_ERR_* or GBATTN_DEV_* code (static storage). */
 const char *attn_strerror(int code);

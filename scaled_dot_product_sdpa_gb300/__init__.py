@@ -5,8 +5,10 @@ and FP32 row log-sum-exp, computed by one fused persistent CUDA kernel (TMA, tcg
 tensor cores, tensor memory) behind the C ABI of include/gbattn.h.  This package is the
 thin Python binding of that library; every step of the computation runs on the GPU.
 """
-from ._binding import (FLAG_P_SMEM, FLAG_SINGLE_TILE, FLAG_TWO_TILE, GbattnError, attn_debug_schedule, attn_debug_scores, attn_debug_wait_probe, attn_fwd,
-                       attn_last_device_error, attn_strerror, attn_version, load_library, LIB_PATH)
+from ._binding import (FLAG_P_SMEM, FLAG_SINGLE_TILE, FLAG_TWO_TILE, LIB_PATH, GbattnError,
+                       attn_debug_plan, attn_debug_schedule, attn_debug_scores, attn_debug_wait_probe, attn_fwd,
+                       attn_last_device_error, attn_strerror, attn_version, load_library)
 
-__all__ = ["attn_fwd", "attn_debug_scores", "attn_debug_schedule", "attn_debug_wait_probe", "attn_last_device_error",
-           "attn_strerror", "attn_version", "load_library", "GbattnError", "FLAG_P_SMEM", "FLAG_SINGLE_TILE", "FLAG_TWO_TILE", "LIB_PATH"]
+__all__ = ["attn_fwd", "attn_debug_plan", "attn_debug_scores", "attn_debug_schedule", "attn_debug_wait_probe",
+           "attn_last_device_error", "attn_strerror", "attn_version", "load_library", "GbattnError", "FLAG_P_SMEM",
+           "FLAG_SINGLE_TILE", "FLAG_TWO_TILE", "LIB_PATH"]

@@ -54,6 +54,8 @@ def load_library(path: str | None = None):
     ip = ctypes.POINTER(ctypes.c_int)
     lib.attn_debug_schedule.argtypes = [i, i, i, i, i, i, i, ip, ip, i]
     lib.attn_debug_schedule.restype = i
+    lib.attn_debug_plan.argtypes = [i, i, i, i, i, i, i, i, ip]
+    lib.attn_debug_plan.restype = i
     lib.attn_version.argtypes = []
     lib.attn_version.restype = i
     _lib = lib
@@ -152,3 +154,14 @@ def attn_debug_schedule(B: int, H: int, L: int, d: int, causal: bool, grid: int,
     if n == 0:
         return None
     return [list(items[start[c]:start[c + 1]]) for c in range(grid)]
+
+
+def attn_debug_plan(B: int, H: int, L: int, d: int, causal: bool, sm_count: int, flags: int = 0,
+                    grid_limit: int = 0) -> dict:
+    """The kernel attn_fwd would launch on a GPU with `sm_count` SMs (host-only):
+    kind 0 single-tile, 1 two-tile."""
+    out = (ctypes.c_int * 4)()
+    rc = load_library().attn_debug_plan(B, H, L, d, int(bool(causal)), sm_count, flags, grid_limit, out)
+    if rc != 0:
+        raise GbattnError(rc, "attn_debug_plan")
+    return {"kind": out[0], "items": out[1], "grid": out[2], "makespan": out[3] / 100.0}

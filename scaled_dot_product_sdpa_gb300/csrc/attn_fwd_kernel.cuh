@@ -64,7 +64,13 @@ struct FwdCfg {
   static constexpr int KST = NCH / SC;               // ring stages per K tile
   static constexpr int VST = NCHV / SC;              // ring stages per V tile
   static constexpr int NQB = D <= 128 ? 2 : 1;       // Q buffers (also the O staging tiles)
-  static constexpr bool LOOKAHEAD = NQB >= 2;        // next item's first QK before last PV
+  static constexpr bool LOOKAHEAD = NQB >= 2;        // next item's QKs before its last PVs
+  // S buffers in tensor memory; the issuer runs QK NSB - 1 key tiles ahead of PV.  Three
+  // would fit for O tiles of at most 128 columns, but measured slower on GB300: the QK two
+  // tiles ahead needs its K tile one ring stage earlier, and with five stages of 32 KB that
+  // costs more load latency than the earlier S saves.  (The P-in-shared-memory variant
+  // would also need a third P buffer.)
+  static constexpr int NSB = 2;
   static constexpr int CHUNK = 128 * 128;            // bytes of a 128-row x 64-col fp16 box
   static constexpr int STAGE = SC * CHUNK;
   static constexpr int QBYTES = NCH * CHUNK;
@@ -75,13 +81,13 @@ struct FwdCfg {
   static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
   // barrier indices
   static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_FULL = 4, B_EMPTY = 4 + NST;
-  static constexpr int B_SFULL = 4 + 2 * NST, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2;
+  static constexpr int B_SFULL = 4 + 2 * NST, B_PFULL = B_SFULL + NSB, B_ODONE = B_PFULL + NSB;
   static constexpr int B_OFREE = B_ODONE + 1, B_EPI = B_OFREE + 1, B_DRAIN = B_EPI + 1;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int TILE_BYTES = NQB * QBYTES + NPB * PBYTES + NST * STAGE;
   static constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + TILE_BYTES + 8 * NBAR + 16;
-  // tensor memory columns: S buffers at [0,128) and [128,256), O at [256, 256 + DV)
-  static constexpr int O_COL = 256;
+  // tensor memory columns: S buffer b at [128 b, 128 b + 128), O after the S buffers
+  static constexpr int O_COL = 128 * NSB;
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_QK = idesc_f16_f32(128, 128, 0, 0);
   static constexpr uint32_t IDESC_PV = idesc_f16_f32(128, SC * 64, 0, 1);
@@ -205,6 +211,40 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, long l
   return true;
 }
 
+// The order in which the single-tile kernel's MMA issuer consumes ring stages, walked
+// identically by the producer (which loads in that order) and the issuer: per key tile g
+// (counted across items) the QK, then -- once NSB - 1 PVs wait in the queue -- the oldest
+// PV (its S buffer is the next QK's), then PV(g) joins the queue: QK runs NSB - 1 tiles
+// ahead of PV.  Before the first QK of an item every PV of an item two back (one back
+// without LOOKAHEAD) leaves the queue: that item's epilogue must be able to finish, since
+// its Q buffer is its O staging tile and receives the Q of the item after next.
+struct PendingPv {
+  uint32_t g;
+  int il, t, n, bh, half;
+};
+template <int NSB>
+struct PvQueue {
+  static constexpr int CAP = NSB > 1 ? NSB - 1 : 1;  // at most 2
+  static_assert(CAP <= 2, "selects below index at most two entries");
+  PendingPv e[CAP];
+  int head = 0, size = 0;
+  // Entries are picked by selects on constant indices, so the queue stays in registers.
+  __device__ void push(const PendingPv &v) {
+    int tail = head + size;
+    if (tail >= CAP) tail -= CAP;
+    if (tail == 0) e[0] = v;
+    else e[CAP - 1] = v;
+    ++size;
+  }
+  __device__ PendingPv pop() {
+    const PendingPv v = head == 0 ? e[0] : e[CAP - 1];
+    head = head + 1 == CAP ? 0 : head + 1;
+    --size;
+    return v;
+  }
+  __device__ const PendingPv &front() const { return head == 0 ? e[0] : e[CAP - 1]; }
+};
+
 template <int D, bool CAUSAL, bool P_TMEM>
 __global__ void __launch_bounds__(256, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -236,7 +276,7 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(BAR(C::B_FULL + i), 1);
       mbar_init(BAR(C::B_EMPTY + i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::NSB; ++i) {
       mbar_init(BAR(C::B_SFULL + i), 1);
       mbar_init(BAR(C::B_PFULL + i), 128);
     }
@@ -271,8 +311,7 @@ __global__ void __launch_bounds__(256, 1)
       Sched sc(blockIdx.x, gridDim.x, p.n_items, &tbl);
       uint32_t it = 0;
       int il = 0, item;
-      bool ok = true, have_v = false;
-      int v_bh = 0, v_kt = 0, v_half = 0;
+      bool ok = true;
       const uint64_t pol_kv = policy_evict_last();
       auto load_stage = [&](const CUtensorMap *tm, int chunk0, int y, int z) -> bool {
         const uint32_t s = it % C::NST, ph = (it / C::NST) & 1u;
@@ -286,18 +325,18 @@ __global__ void __launch_bounds__(256, 1)
         ++it;
         return true;
       };
-      auto load_v = [&]() -> bool {
+      auto load_v = [&](const PendingPv &v) -> bool {
         for (int vs = 0; vs < C::VST; ++vs)
-          if (!load_stage(&tm_v, v_half * C::NCHV + vs * C::SC, v_kt * C::BN, v_bh)) return false;
+          if (!load_stage(&tm_v, v.half * C::NCHV + vs * C::SC, v.t * C::BN, v.bh)) return false;
         return true;
       };
+      PvQueue<C::NSB> pq;
+      uint32_t g = 0;
       while (ok && sc.next(item)) {
         int bh, qt, half, n;
         decode_item<C::DVS, CAUSAL>(item, p, bh, qt, half, n);
-        if (!C::LOOKAHEAD && have_v) {
-          have_v = false;
-          if (!(ok = load_v())) break;
-        }
+        while (ok && pq.size > 0 && pq.front().il < il - (C::LOOKAHEAD ? 1 : 0)) ok = load_v(pq.pop());
+        if (!ok) break;
         const int qb = il % C::NQB;
         const uint32_t qph = (il / C::NQB) & 1;
         if (!(ok = wait_bounded(BAR(C::B_QEMPTY + qb), qph ^ 1u, abort_flag, p.status, kDevTimeoutLoad, LIM)))
@@ -305,17 +344,14 @@ __global__ void __launch_bounds__(256, 1)
         mbar_arrive_expect_tx(BAR(C::B_QFULL + qb), C::QBYTES);
         for (int c = 0; c < C::NCH; ++c)
           tma_load_3d(q_s + qb * C::QBYTES + c * C::CHUNK, &tm_q, c * 64, qt * C::BM, bh, BAR(C::B_QFULL + qb));
-        for (int t = 0; t < n && ok; ++t) {
+        for (int t = 0; t < n && ok; ++t, ++g) {
           for (int ks = 0; ks < C::KST && ok; ++ks) ok = load_stage(&tm_k, ks * C::SC, t * C::BN, bh);
-          if (ok && have_v) ok = load_v();
-          have_v = true;
-          v_bh = bh;
-          v_kt = t;
-          v_half = half;
+          if (ok && pq.size == C::NSB - 1) ok = load_v(pq.pop());
+          pq.push(PendingPv{g, il, t, n, bh, half});
         }
         ++il;
       }
-      if (ok && have_v) ok = load_v();
+      while (ok && pq.size > 0) ok = load_v(pq.pop());
       // Drain: every load issued must have landed before the CTA may exit.
       const uint32_t first = it > static_cast<uint32_t>(C::NST) ? it - C::NST : 0u;
       for (uint32_t i = first; i < it; ++i)
@@ -330,15 +366,13 @@ __global__ void __launch_bounds__(256, 1)
       Sched sc(blockIdx.x, gridDim.x, p.n_items, &tbl);
       uint32_t it = 0, g = 0;
       int il = 0, item;
-      bool ok = true, have_pv = false;
-      uint32_t pv_g = 0;
-      bool pv_first = false;
-      int pv_il = 0;
+      bool ok = true;
       auto wait = [&](uint32_t bar, uint32_t ph) -> bool {
         return wait_bounded(bar, ph, abort_flag, p.status, kDevTimeoutMma, LIM);
       };
       auto issue_qk = [&](uint32_t gg, int qb) -> bool {
-        const uint32_t d_tmem = tmem + (gg & 1u) * 128u;
+        const uint32_t sb = gg % C::NSB;
+        const uint32_t d_tmem = tmem + sb * 128u;
         for (int ks = 0; ks < C::KST; ++ks) {
           const uint32_t s = it % C::NST;
           if (!wait(BAR(C::B_FULL + s), (it / C::NST) & 1u)) return false;
@@ -356,13 +390,14 @@ __global__ void __launch_bounds__(256, 1)
           umma_commit(BAR(C::B_EMPTY + s));
           ++it;
         }
-        umma_commit(BAR(C::B_SFULL + (gg & 1u)));
+        umma_commit(BAR(C::B_SFULL + sb));
         return true;
       };
-      auto issue_pv = [&]() -> bool {
-        const uint32_t sb = pv_g & 1u;
-        if (!wait(BAR(C::B_PFULL + sb), (pv_g >> 1) & 1u)) return false;
-        if (pv_first && pv_il > 0 && !wait(BAR(C::B_OFREE), (pv_il - 1) & 1)) return false;
+      auto issue_pv = [&](const PendingPv &v) -> bool {
+        const uint32_t sb = v.g % C::NSB;
+        const bool first = v.t == 0;
+        if (!wait(BAR(C::B_PFULL + sb), (v.g / C::NSB) & 1u)) return false;
+        if (first && v.il > 0 && !wait(BAR(C::B_OFREE), (v.il - 1) & 1)) return false;
         tc_fence_after();
         for (int vs = 0; vs < C::VST; ++vs) {
           const uint32_t s = it % C::NST;
@@ -370,10 +405,10 @@ __global__ void __launch_bounds__(256, 1)
           tc_fence_after();
           const uint32_t o_tmem = tmem + C::O_COL + vs * C::SC * 64;
           const SDesc b = sdesc_split(sdesc_sw128(ring_s + s * C::STAGE, C::CHUNK, 1024));
-          const SDesc a = sdesc_split(sdesc_sw128(p_s + sb * C::PBYTES, 16, 1024));
+          const SDesc a = sdesc_split(sdesc_sw128(p_s + (v.g & 1u) * C::PBYTES, 16, 1024));
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t acc = (pv_first && kk == 0) ? 0u : 1u;
+            const uint32_t acc = (first && kk == 0) ? 0u : 1u;
             if constexpr (P_TMEM) {
               umma_ts_off(o_tmem, tmem + sb * 128u + kk * 8u, b, kk * 2048, C::IDESC_PV, acc);
             } else {
@@ -386,28 +421,23 @@ __global__ void __launch_bounds__(256, 1)
         umma_commit(BAR(C::B_ODONE));
         return true;
       };
+      PvQueue<C::NSB> pq;
       while (ok && sc.next(item)) {
         int bh, qt, half, n;
         decode_item<C::DVS, CAUSAL>(item, p, bh, qt, half, n);
-        if (!C::LOOKAHEAD && have_pv) {
-          have_pv = false;
-          if (!(ok = issue_pv())) break;
-        }
+        while (ok && pq.size > 0 && pq.front().il < il - (C::LOOKAHEAD ? 1 : 0)) ok = issue_pv(pq.pop());
+        if (!ok) break;
         const int qb = il % C::NQB;
         if (!(ok = wait(BAR(C::B_QFULL + qb), (il / C::NQB) & 1))) break;
         tc_fence_after();
-        for (int t = 0; t < n && ok; ++t) {
+        for (int t = 0; t < n && ok; ++t, ++g) {
           ok = issue_qk(g, qb);
-          if (ok && have_pv) ok = issue_pv();
-          have_pv = true;
-          pv_g = g;
-          pv_first = (t == 0);
-          pv_il = il;
-          ++g;
+          if (ok && pq.size == C::NSB - 1) ok = issue_pv(pq.pop());
+          pq.push(PendingPv{g, il, t, n, bh, half});
         }
         ++il;
       }
-      if (ok && have_pv) ok = issue_pv();
+      while (ok && pq.size > 0) ok = issue_pv(pq.pop());
       // Drain: all MMAs issued by this thread complete before tensor memory is freed.
       umma_commit(BAR(C::B_DRAIN));
       wait_drain(BAR(C::B_DRAIN), 0, LIM);
@@ -432,31 +462,35 @@ __global__ void __launch_bounds__(256, 1)
       decode_item<C::DVS, CAUSAL>(item, p, bh, qt, half, n);
       float m_used = 0.f, l = 0.f;
       for (int t = 0; t < n; ++t, ++g) {
-        const uint32_t sb = g & 1u;
-        if (!(ok = wait_warp(BAR(C::B_SFULL + sb), (g >> 1) & 1u))) break;
+        const uint32_t sb = g % C::NSB;
+        if (!(ok = wait_warp(BAR(C::B_SFULL + sb), (g / C::NSB) & 1u))) break;
         tc_fence_after();
         const int lim = CAUSAL ? (t == qt ? row + 1 : 128) : min(128, p.L - t * C::BN);
-        // PV of the previous key tile must be complete before O may be rescaled: wait for
-        // it once the tile maximum is known (every tile but the first, to keep the
-        // barrier's phases in step).
+        // ODONE completes once per PV, and every phase is waited for exactly once, in
+        // order: on tile t > 0, the phase of PV(t-1) -- just before a rescale of O (which
+        // must not race with it), else at the end of the tile, when that PV has long been
+        // done.  Either way PV(t-2) is complete (it was issued before this tile's QK) and
+        // PV(t) cannot be (it needs this tile's P), so the wait's parity is unambiguous.
+        // The softmax of tile t+1 therefore never waits for PV(t) on the common path.
         auto wait_prev_pv = [&]() -> bool {
           if (!wait_warp(BAR(C::B_ODONE), (g - 1) & 1u)) return false;
           tc_fence_after();
           return true;
         };
+        bool rescaled = false;
         if constexpr (P_TMEM) {
           if (!(ok = softmax_tile<C::DV>(tmem + lane_base + sb * 128u, tmem + lane_base + C::O_COL, lim, c2, t == 0,
-                                         m_used, l, wait_prev_pv)))
+                                         m_used, l, wait_prev_pv, &rescaled)))
             break;
         } else {
           // P through shared memory: run the step into tensor memory, then move the fp16
           // P from the S columns into the swizzled shared-memory operand tile.
           if (!(ok = softmax_tile<C::DV>(tmem + lane_base + sb * 128u, tmem + lane_base + C::O_COL, lim, c2, t == 0,
-                                         m_used, l, wait_prev_pv)))
+                                         m_used, l, wait_prev_pv, &rescaled)))
             break;
           uint32_t pk[64];
           tmem_ld32x64(tmem + lane_base + sb * 128u, pk);
-          const uint32_t pb = p_s + sb * C::PBYTES + row * 128;
+          const uint32_t pb = p_s + (g & 1u) * C::PBYTES + row * 128;
 #pragma unroll
           for (int ch = 0; ch < 16; ++ch) {
             const uint32_t addr = pb + (ch >> 3) * C::CHUNK + ((((ch & 7) ^ (row & 7))) << 4);
@@ -464,6 +498,7 @@ __global__ void __launch_bounds__(256, 1)
           }
           fence_proxy_async_smem();
         }
+        if (t > 0 && !rescaled && !(ok = wait_prev_pv())) break;
         tc_fence_before();
         mbar_arrive(BAR(C::B_PFULL + sb));
       }

@@ -96,50 +96,64 @@ int encode_bhld(CUtensorMap *tm, const void *ptr, int BH, int L, int D) {
 }
 
 // ------------------------------------------------------------------ work schedule
-// Cost of a work item in 128 x 128 tile units plus a per-item overhead (fill, drain and
-// epilogue of the item's pipeline), the latter measured on GB300 for each kernel.
-constexpr double kItemOverheadTwoTile = 1.7;
-constexpr double kItemOverheadSingle = 1.0;
+// The kernels a launch can use.
+enum Kind { kSingle = 0, kPair = 1 };
+
+// Cost of a work item in units of one 128 x 128 tile step of one query tile in the
+// two-tile kernel (it runs two such steps at once, one per query tile of its item), plus
+// a per-item overhead (fill, drain and epilogue of the item's pipeline).  A tile step of
+// the single-tile kernel costs about 1.2 such units.  Measured on GB300.
+constexpr double kItemOverheadTwoSlot = 1.7;
+constexpr double kSingleStepCost = 1.2;
+constexpr double kItemOverheadSingle = 1.0;  // in single-tile steps
 
 struct SchedKey {
-  int two_tile, BH, nQ, nQB, dvs, causal, grid;
+  int kind, BH, nQ, nQB, dvs, causal, grid;
   bool operator==(const SchedKey &o) const {
-    return two_tile == o.two_tile && BH == o.BH && nQ == o.nQ && nQB == o.nQB && dvs == o.dvs &&
-           causal == o.causal && grid == o.grid;
+    return kind == o.kind && BH == o.BH && nQ == o.nQ && nQB == o.nQB && dvs == o.dvs && causal == o.causal &&
+           grid == o.grid;
   }
 };
 
-// Work units of item r, mirroring the kernels' item decoding (pp_decode / decode_item).
-int item_units(const SchedKey &k, int r) {
-  if (k.two_tile) {
-    if (!k.causal) return 2 * k.nQ;
+long long count_items(const SchedKey &k) {
+  return k.kind == kPair ? static_cast<long long>(k.BH) * k.nQB : static_cast<long long>(k.BH) * k.nQ * k.dvs;
+}
+
+// Cost of item r, mirroring the kernels' item decoding (decode_item / pp_decode).
+double item_cost(const SchedKey &k, int r) {
+  if (k.kind == kPair) {
+    if (!k.causal) return 2.0 * k.nQ + kItemOverheadTwoSlot;
     const int qb = k.nQB - 1 - r / k.BH;
-    return (2 * qb + 1) + std::min(2 * qb + 2, k.nQ);
+    return (2 * qb + 1) + std::min(2 * qb + 2, k.nQ) + kItemOverheadTwoSlot;
   }
-  if (!k.causal) return k.nQ;
-  const int qt = k.nQ - 1 - r / (k.BH * k.dvs);
-  return qt + 1;
+  const int n = k.causal ? k.nQ - r / (k.BH * k.dvs) : k.nQ;
+  return kSingleStepCost * (n + kItemOverheadSingle);
 }
 
 // Longest-processing-time-first: take items by decreasing cost, give each to the CTA with
 // the least accumulated cost (ties: lowest CTA).  Each CTA's list keeps assignment order.
-void build_lpt(const SchedKey &k, int n_items, SchedTable &t) {
+// Returns the largest accumulated cost (the estimated makespan), or -1 with t.n = 0
+// (the kernels' fixed snake order) when the items or CTAs do not fit the table.
+double build_lpt(const SchedKey &k, SchedTable &t) {
   std::memset(&t, 0, sizeof(t));
-  if (n_items > kSchedMaxItems || k.grid > kSchedMaxCtas || k.grid <= 0) return;  // snake order
-  const double over = k.two_tile ? kItemOverheadTwoTile : kItemOverheadSingle;
-  std::vector<int> order(n_items);
-  std::iota(order.begin(), order.end(), 0);
+  const long long n_items = count_items(k);
+  if (n_items > kSchedMaxItems || k.grid > kSchedMaxCtas || k.grid <= 0) return -1.0;
+  std::vector<std::pair<double, int>> order;
+  order.reserve(static_cast<size_t>(n_items));
+  for (int r = 0; r < n_items; ++r) order.push_back({item_cost(k, r), r});
   std::stable_sort(order.begin(), order.end(),
-                   [&](int a, int b) { return item_units(k, a) > item_units(k, b); });
+                   [](const std::pair<double, int> &a, const std::pair<double, int> &b) { return a.first > b.first; });
   using Slot = std::pair<double, int>;
   std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
   for (int c = 0; c < k.grid; ++c) heap.push({0.0, c});
   std::vector<std::vector<uint16_t>> lists(k.grid);
-  for (int r : order) {
+  double makespan = 0.0;
+  for (const auto &w : order) {
     const Slot s = heap.top();
     heap.pop();
-    lists[s.second].push_back(static_cast<uint16_t>(r));
-    heap.push({s.first + item_units(k, r) + over, s.second});
+    lists[s.second].push_back(static_cast<uint16_t>(w.second));
+    makespan = std::max(makespan, s.first + w.first);
+    heap.push({s.first + w.first, s.second});
   }
   int pos = 0;
   for (int c = 0; c < k.grid; ++c) {
@@ -147,36 +161,87 @@ void build_lpt(const SchedKey &k, int n_items, SchedTable &t) {
     for (uint16_t r : lists[c]) t.items[pos++] = r;
   }
   t.start[k.grid] = static_cast<uint16_t>(pos);
-  t.n = n_items;
+  t.n = static_cast<int>(n_items);
+  return makespan;
 }
 
 struct SchedEntry {
   bool valid = false;
   unsigned long long stamp = 0;
   SchedKey key{};
+  double makespan = 0.0;
   SchedTable tbl;
 };
-SchedEntry g_sched_cache[8];
+SchedEntry g_sched_cache[16];
 unsigned long long g_sched_clock = 0;
 std::mutex g_sched_mu;
 
-// Copy the schedule for `k` into `out`, building and caching it on a miss.
-void get_schedule(const SchedKey &k, int n_items, SchedTable &out) {
+// The schedule for `k`, built and cached on a miss; copies the table into `out` when
+// given.  Returns the estimated makespan (< 0: no table, snake order).
+double get_schedule(const SchedKey &k, SchedTable *out) {
   std::lock_guard<std::mutex> lock(g_sched_mu);
   SchedEntry *victim = &g_sched_cache[0];
   for (SchedEntry &e : g_sched_cache) {
     if (e.valid && e.key == k) {
       e.stamp = ++g_sched_clock;
-      out = e.tbl;
-      return;
+      if (out) *out = e.tbl;
+      return e.makespan;
     }
     if (!e.valid || e.stamp < victim->stamp) victim = &e;
   }
-  build_lpt(k, n_items, victim->tbl);
+  victim->makespan = build_lpt(k, victim->tbl);
   victim->key = k;
   victim->valid = true;
   victim->stamp = ++g_sched_clock;
-  out = victim->tbl;
+  if (out) *out = victim->tbl;
+  return victim->makespan;
+}
+
+// ------------------------------------------------------------------ launch plan
+// The kernel and grid of a launch.  Options force a kernel; otherwise head_dim > 128
+// takes the single-tile kernel, and head_dim <= 128 the two-tile kernel, unless that has
+// fewer than two items per SM: then whichever of the two has the smaller estimated
+// makespan (measured on GB300 at 1x16x512x64 causal 7.6 vs 11.2 us, 1x32x1024x128
+// causal 15.9 vs 23.7 us, both for the single-tile kernel).
+SchedKey make_key(int kind, int BH, int L, int d, int causal, int grid) {
+  const int nQ = (L + 127) / 128, nQB = (L + 255) / 256, dvs = d > 256 ? d / 256 : 1;
+  SchedKey k{kind, BH, nQ, nQB, kind == kSingle ? dvs : 1, causal != 0 ? 1 : 0, grid};
+  const long long n = count_items(k);
+  if (n < grid) k.grid = static_cast<int>(n);
+  return k;
+}
+
+int choose_plan(int BH, int L, int d, int causal, int sm_count, int flags, int grid_limit, SchedKey &out,
+                double &makespan) {
+  int grid = sm_count;
+  if (grid_limit > 0 && grid_limit < grid) grid = grid_limit;
+  int kind;
+  if (flags & (GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE) || d > 128) {
+    kind = kSingle;
+  } else if (flags & GBATTN_FLAG_TWO_TILE) {
+    kind = kPair;
+  } else {
+    const SchedKey pair = make_key(kPair, BH, L, d, causal, grid);
+    if (count_items(pair) > INT_MAX) return GBATTN_ERR_DIMS;
+    if (count_items(pair) >= 2LL * grid) {
+      kind = kPair;
+    } else {
+      double best = 0.0;
+      kind = -1;
+      for (int cand : {kSingle, kPair}) {
+        const double m = get_schedule(make_key(cand, BH, L, d, causal, grid), nullptr);
+        if (m >= 0.0 && (kind < 0 || m < best)) {
+          best = m;
+          kind = cand;
+        }
+      }
+      if (kind < 0) kind = kPair;
+    }
+  }
+  out = make_key(kind, BH, L, d, causal, grid);
+  if (count_items(out) > INT_MAX) return GBATTN_ERR_DIMS;
+  makespan = get_schedule(out, nullptr);
+  return GBATTN_OK;
 }
 
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
@@ -185,6 +250,16 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The option bits of attn_fwd_ex: known bits only, the two-tile kernel not together with
+// a single-tile option, and the two-tile kernel and shared-memory P only for d <= 128.
+int check_flags(int flags, int d) {
+  if (flags & ~(GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE | GBATTN_FLAG_TWO_TILE)) return GBATTN_ERR_FLAGS;
+  if ((flags & GBATTN_FLAG_TWO_TILE) && (flags & (GBATTN_FLAG_SINGLE_TILE | GBATTN_FLAG_P_SMEM)))
+    return GBATTN_ERR_FLAGS;
+  if ((flags & (GBATTN_FLAG_P_SMEM | GBATTN_FLAG_TWO_TILE)) && d > 128) return GBATTN_ERR_HEAD_DIM;
+  return GBATTN_OK;
+}
 
 int check_shape(int B, int H, int L, int d) {
   if (B <= 0 || H <= 0 || L <= 0) return GBATTN_ERR_DIMS;
@@ -207,17 +282,7 @@ extern "C" int attn_fwd_ex(const void *q, const void *k, const void *v, void *o,
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return GBATTN_ERR_ALIGN;
   if (!std::isfinite(scale) || !(scale > 0.f)) return GBATTN_ERR_SCALE;
   const bool p_smem = (flags & GBATTN_FLAG_P_SMEM) != 0;
-  if (p_smem && d > 128) return GBATTN_ERR_HEAD_DIM;
-  if (flags & ~(GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE | GBATTN_FLAG_TWO_TILE)) return GBATTN_ERR_FLAGS;
-  if ((flags & GBATTN_FLAG_TWO_TILE) && (flags & (GBATTN_FLAG_SINGLE_TILE | GBATTN_FLAG_P_SMEM)))
-    return GBATTN_ERR_FLAGS;
-  if ((flags & GBATTN_FLAG_TWO_TILE) && d > 128) return GBATTN_ERR_HEAD_DIM;
-  // d <= 128: the two-tile kernel (two 128-row query tiles per item) unless an option asks
-  // for the single-tile kernel, or unless it would get fewer than two items per SM: then
-  // the single-tile kernel's twice-as-many, half-as-long items balance the SMs better
-  // (measured on GB300: 1x16x512x64 causal 7.7 vs 10.5 us, 1x32x1024x128 causal 15.0 vs
-  // 19.2 us), while the two-tile kernel is faster once every SM has several items.
-  bool two_tile = d <= 128 && !(flags & (GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE));
+  if ((rc = check_flags(flags, d)) != GBATTN_OK) return rc;
   if (grid_limit < 0) return GBATTN_ERR_DIMS;
   const long long rows = static_cast<long long>(B) * H * L;
   const size_t tbytes = static_cast<size_t>(rows) * static_cast<size_t>(d) * 2u;
@@ -231,13 +296,10 @@ extern "C" int attn_fwd_ex(const void *q, const void *k, const void *v, void *o,
   if ((rc = device_info(&di)) != GBATTN_OK) return rc;
 
   const int BH = B * H;
-  const int nQ = (L + 127) / 128;
-  const int nQB = (L + 255) / 256;
-  const int dvs = d > 256 ? d / 256 : 1;
-  if (two_tile && !(flags & GBATTN_FLAG_TWO_TILE) && static_cast<long long>(BH) * nQB < 2LL * di->sm_count)
-    two_tile = false;
-  const long long n_items = two_tile ? static_cast<long long>(BH) * nQB : static_cast<long long>(BH) * nQ * dvs;
-  if (n_items > INT_MAX) return GBATTN_ERR_DIMS;
+  SchedKey key;
+  double makespan = 0.0;
+  if ((rc = choose_plan(BH, L, d, causal, di->sm_count, flags, grid_limit, key, makespan)) != GBATTN_OK) return rc;
+  const bool two_tile = key.kind != kSingle;
 
   FwdLaunch a;
   SchedTable tbl;
@@ -245,12 +307,8 @@ extern "C" int attn_fwd_ex(const void *q, const void *k, const void *v, void *o,
   if (encode_bhld(&a.tm_q, q, BH, L, d) || encode_bhld(&a.tm_k, k, BH, L, d) || encode_bhld(&a.tm_v, v, BH, L, d) ||
       encode_bhld(&a.tm_o, o, BH, L, d))
     return GBATTN_ERR_TENSORMAP;
-  int grid = di->sm_count;
-  if (grid_limit > 0 && grid_limit < grid) grid = grid_limit;
-  if (n_items < grid) grid = static_cast<int>(n_items);
-  a.grid = grid;
-  get_schedule(SchedKey{two_tile ? 1 : 0, BH, nQ, nQB, two_tile ? 1 : dvs, causal != 0 ? 1 : 0, grid},
-               static_cast<int>(n_items), tbl);
+  a.grid = key.grid;
+  get_schedule(key, &tbl);
   a.causal = causal != 0;
   a.p_smem = p_smem;
   a.stream = static_cast<cudaStream_t>(stream);
@@ -260,9 +318,9 @@ extern "C" int attn_fwd_ex(const void *q, const void *k, const void *v, void *o,
   a.p.wait_limit = kWaitLimitCycles;
   a.p.BH = BH;
   a.p.L = L;
-  a.p.nQ = nQ;
-  a.p.nQB = nQB;
-  a.p.n_items = static_cast<int>(n_items);
+  a.p.nQ = key.nQ;
+  a.p.nQB = key.nQB;
+  a.p.n_items = static_cast<int>(count_items(key));
   a.p.c2 = scale * 1.4426950408889634f;
 
   cudaError_t e;
@@ -356,15 +414,14 @@ extern "C" int attn_debug_schedule(int B, int H, int L, int d, int causal, int g
   if (rc != GBATTN_OK) return rc;
   if (grid <= 0 || grid > kSchedMaxCtas) return GBATTN_ERR_DIMS;
   if (!start || !items) return GBATTN_ERR_NULL;
-  // The schedule of the kernel the flags name: the two-tile kernel when d <= 128 and no
-  // single-tile option is set (the automatic choice of attn_fwd is not applied here).
-  const bool two_tile = d <= 128 && !(flags & (GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE));
-  const int BH = B * H, nQ = (L + 127) / 128, nQB = (L + 255) / 256, dvs = d > 256 ? d / 256 : 1;
-  const long long n_items = two_tile ? static_cast<long long>(BH) * nQB : static_cast<long long>(BH) * nQ * dvs;
-  if (n_items > INT_MAX) return GBATTN_ERR_DIMS;
+  // The schedule of the kernel the flags name (no flag, d <= 128: the two-tile kernel;
+  // the automatic choice of attn_fwd is not applied here).
+  const int kind = ((flags & (GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE)) || d > 128) ? kSingle : kPair;
+  SchedKey key{kind, B * H, (L + 127) / 128, (L + 255) / 256, kind == kSingle && d > 256 ? d / 256 : 1,
+               causal != 0 ? 1 : 0, grid};
+  if (count_items(key) > INT_MAX) return GBATTN_ERR_DIMS;
   static SchedTable t;  // large; this is a test hook, not thread-safe
-  get_schedule(SchedKey{two_tile ? 1 : 0, BH, nQ, nQB, two_tile ? 1 : dvs, causal != 0 ? 1 : 0, grid},
-               static_cast<int>(n_items), t);
+  get_schedule(key, &t);
   if (t.n == 0) return 0;
   if (t.n > max_items) return GBATTN_ERR_DIMS;
   for (int c = 0; c <= grid; ++c) start[c] = t.start[c];
@@ -372,4 +429,21 @@ extern "C" int attn_debug_schedule(int B, int H, int L, int d, int causal, int g
   return t.n;
 }
 
-extern "C" int attn_version(void) { return 100; }
+extern "C" int attn_debug_plan(int B, int H, int L, int d, int causal, int sm_count, int flags, int grid_limit,
+                               int *out) {
+  if (!out) return GBATTN_ERR_NULL;
+  int rc = check_shape(B, H, L, d);
+  if (rc != GBATTN_OK) return rc;
+  if (sm_count <= 0 || sm_count > kSchedMaxCtas || grid_limit < 0) return GBATTN_ERR_DIMS;
+  if ((rc = check_flags(flags, d)) != GBATTN_OK) return rc;
+  SchedKey key;
+  double makespan = 0.0;
+  if ((rc = choose_plan(B * H, L, d, causal, sm_count, flags, grid_limit, key, makespan)) != GBATTN_OK) return rc;
+  out[0] = key.kind;
+  out[1] = static_cast<int>(count_items(key));
+  out[2] = key.grid;
+  out[3] = static_cast<int>(makespan * 100.0);
+  return GBATTN_OK;
+}
+
+extern "C" int attn_version(void) { return 10100; }

@@ -24,15 +24,17 @@ namespace gbattn {
 // masked to -inf (lim = row + 1 on a causal diagonal tile, L - first key on a ragged last
 // tile, 128 otherwise).  P (fp16) is written over the first 64 columns of the S tile.
 // Warp-collective (tcgen05.ld/st): all 32 lanes must call it together.
-// `before_rescale()` runs on every tile but the first, after the tile maximum is known
-// and before O may be touched (the single-tile kernel waits there for the previous PV);
-// if it returns false the step stops and returns false.
+// `before_rescale()` runs only when this warp rescales O (a tile but the first whose
+// maximum exceeds the running one by more than 8), before O is touched: a caller whose
+// PV into O may still be in flight waits for it there.  If it returns false the step
+// stops and returns false.  It returns whether it ran through `rescaled`.
 struct NoWait {
   __device__ bool operator()() const { return true; }
 };
 template <int DV, class Hook = NoWait>
 __device__ __forceinline__ bool softmax_tile(uint32_t s_tmem, uint32_t o_tmem, int lim, float c2, bool first,
-                                             float &m_used, float &l, const Hook &before_rescale = Hook()) {
+                                             float &m_used, float &l, const Hook &before_rescale = Hook(),
+                                             bool *rescaled = nullptr) {
   uint32_t ra[64], rb[64];
   // Both halves of S in flight at once, then one wait.
   tmem_ld32x64_async(s_tmem, ra);
@@ -68,13 +70,13 @@ __device__ __forceinline__ bool softmax_tile(uint32_t s_tmem, uint32_t o_tmem, i
   }
   const float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
   const float m_tile = mx * c2;
+  if (rescaled) *rescaled = false;
   if (first) {
     m_used = (m_tile == -INFINITY) ? 0.f : m_tile;
     l = 0.f;
-  } else if (!before_rescale()) {
-    return false;
   } else if (__any_sync(0xffffffffu, m_tile > m_used + 8.0f)) {
-    // The caller guarantees that no PV into O is in flight here.
+    if (rescaled) *rescaled = true;
+    if (!before_rescale()) return false;  // no PV into O may be in flight from here on
     const float m_new = fmaxf(m_used, m_tile);
     const float alpha = ex2_approx(m_used - m_new);
     m_used = m_new;

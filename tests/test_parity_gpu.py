@@ -202,12 +202,37 @@ def test_outputs_stay_inside_their_buffers(L, d, causal):
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
 
 
-def test_repeated_calls_are_bitwise_identical():
+@pytest.mark.parametrize("flags", [0, 4, 2], ids=["auto", "two_tile", "single_tile"])
+def test_repeated_calls_are_bitwise_identical(flags):
     w = WORKLOADS["caseC"]
     q, k, v = _dev(*inputs.qkv(w.B, w.H, w.L, w.d, w.seed, w.sigma))
-    o1, l1 = _run(q, k, v, w.causal, w.scale)
-    o2, l2 = _run(q, k, v, w.causal, w.scale)
+    o1, l1 = _run(q, k, v, w.causal, w.scale, flags=flags)
+    o2, l2 = _run(q, k, v, w.causal, w.scale, flags=flags)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("flags", [4, 2], ids=["two_tile", "single_tile"])
+def test_replays_from_a_cuda_graph(flags):
+    """A launch captured in a CUDA graph (as bench.py times it) replays with the same
+    results as the eager call."""
+    w = WORKLOADS["caseC"]
+    q, k, v = _dev(*inputs.qkv(w.B, w.H, w.L, w.d, w.seed, w.sigma))
+    o_ref, l_ref = _run(q, k, v, w.causal, w.scale, flags=flags)
+    s = torch.cuda.Stream()
+    o, lse = torch.empty_like(q), torch.empty_like(l_ref)
+    with torch.cuda.stream(s):
+        gb.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse, stream=s, flags=flags)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        gb.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse, stream=s, flags=flags)
+    for _ in range(3):
+        o.fill_(0)
+        lse.fill_(0)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
 
 
 def test_runs_on_a_side_stream():

@@ -1,0 +1,72 @@
+"""Host-side checks of the launch planner (attn_debug_plan; no GPU needed): which kernel
+variant a launch uses, with how many work items and CTAs.
+
+Kernels (include/gbattn.h, attn_fwd_ex): 0 single-tile (items: one 128-row query tile
+per value-column half), 1 two-tile (items: 256-row query blocks).  The item counts below
+follow from those definitions alone."""
+import math
+
+import pytest
+
+import scaled_dot_product_sdpa_gb300 as gb
+
+SM = 152
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from scaled_dot_product_sdpa_gb300 import build
+    gb.load_library(build.build())
+
+
+def _items(kind, B, H, L, d):
+    nQ, nQB = math.ceil(L / 128), math.ceil(L / 256)
+    if kind == 1:
+        return B * H * nQB
+    return B * H * nQ * (d // 256 if d > 256 else 1)
+
+
+SHAPES = [(1, 8, 128, 64, False), (1, 16, 512, 64, True), (1, 32, 1024, 128, True), (8, 32, 512, 128, True),
+          (1, 8, 2048, 512, True), (2, 3, 1000, 64, False), (1, 4, 4096, 128, True), (4, 64, 2048, 64, False)]
+
+
+@pytest.mark.parametrize("B,H,L,d,causal", SHAPES)
+@pytest.mark.parametrize("flags,kind", [(2, 0), (1, 0), (4, 1)])
+def test_flags_force_the_variant(B, H, L, d, causal, flags, kind):
+    if d > 128 and flags in (1, 4):
+        with pytest.raises(gb.GbattnError):
+            gb.attn_debug_plan(B, H, L, d, causal, SM, flags=flags)
+        return
+    p = gb.attn_debug_plan(B, H, L, d, causal, SM, flags=flags)
+    n = _items(kind, B, H, L, d)
+    assert (p["kind"], p["items"], p["grid"]) == (kind, n, min(SM, n))
+
+
+@pytest.mark.parametrize("B,H,L,d,causal", SHAPES)
+def test_auto_plan(B, H, L, d, causal):
+    p = gb.attn_debug_plan(B, H, L, d, causal, SM)
+    if d > 128:
+        assert p["kind"] == 0
+        return
+    pair = gb.attn_debug_plan(B, H, L, d, causal, SM, flags=4)
+    if pair["items"] >= 2 * SM:
+        assert p["kind"] == 1  # enough blocks: the two-tile kernel, whose K/V reuse is highest
+        return
+    # Few blocks: the kernel with the shorter estimated schedule.
+    alternatives = [gb.attn_debug_plan(B, H, L, d, causal, SM, flags=f)["makespan"] for f in (4, 2)]
+    assert p["makespan"] == min(m for m in alternatives if m >= 0)
+
+
+def test_grid_limit_caps_the_ctas():
+    p = gb.attn_debug_plan(1, 32, 1024, 128, True, SM, flags=2, grid_limit=7)
+    assert p["grid"] == 7 and p["items"] == 256
+
+
+def test_rejects_bad_arguments():
+    for kw in ({"sm_count": 0}, {"sm_count": 100000}, {"grid_limit": -1}):
+        args = dict(B=1, H=2, L=256, d=64, causal=True, sm_count=SM)
+        args.update(kw)
+        with pytest.raises(gb.GbattnError):
+            gb.attn_debug_plan(**args)
+    with pytest.raises(gb.GbattnError):
+        gb.attn_debug_plan(1, 2, 256, 96, True, SM)

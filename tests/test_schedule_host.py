@@ -8,11 +8,15 @@ import pytest
 import scaled_dot_product_sdpa_gb300 as gb
 
 
+def _kind(d, flags):
+    return "single" if d > 128 or flags & 3 else "pair"
+
+
 def _units(B, H, L, d, causal, flags, r):
     """Work units of item r, from the item numbering documented with the kernels."""
     BH, nQ, nQB = B * H, math.ceil(L / 128), math.ceil(L / 256)
-    two_tile = d <= 128 and not (flags & 3)
-    if two_tile:
+    kind = _kind(d, flags)
+    if kind == "pair":
         if not causal:
             return 2 * nQ
         qb = nQB - 1 - r // BH
@@ -25,7 +29,8 @@ def _units(B, H, L, d, causal, flags, r):
 
 def _n_items(B, H, L, d, flags):
     BH, nQ, nQB = B * H, math.ceil(L / 128), math.ceil(L / 256)
-    if d <= 128 and not (flags & 3):
+    kind = _kind(d, flags)
+    if kind == "pair":
         return BH * nQB
     return BH * nQ * (d // 256 if d > 256 else 1)
 
