@@ -68,15 +68,18 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def kernel_name(d: int) -> str:
-    """The kernel attn_fwd runs for head_dim d (two-tile kernel for d <= 128)."""
-    return "attn_fwd_pp_kernel" if d <= 128 else "attn_fwd_kernel"
+def kernel_name(w, sm_count: int) -> str:
+    """The kernel attn_fwd runs for workload w on a GPU with sm_count SMs (the library's
+    own launch plan)."""
+    import scaled_dot_product_sdpa_gb300 as gb
+    kind = gb.attn_debug_plan(w.B, w.H, w.L, w.d, w.causal, sm_count)["kind"]
+    return "attn_fwd_pp_kernel" if kind == 1 else "attn_fwd_kernel"
 
 
-def stored_traffic(workload: str, d: int):
+def stored_traffic(workload: str, kernel: str):
     """dram read+write bytes per launch from the committed ncu summary of this workload,
     if it was taken on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"{kernel_name(d)}_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -264,6 +267,45 @@ def bench_e2e(w, steps, warmup, device, torch, gb, host):
     return t, h2d, d2h
 
 
+def interleaved_per_call(workloads, reps, device, torch, gb, inputs):
+    """Device time of single calls, `reps` rounds interleaved across the workloads (each
+    round calls every workload once, on its next rotating input set, so inputs come
+    from HBM).  A GPU-side sleep before each timed call keeps the stream busy while the
+    host enqueues the call, so the events bracket the kernel and not the host's launch
+    work.  Returns {name: (median, p10, p90) seconds}."""
+    prepared = {}
+    for name, w in workloads.items():
+        R = n_rotating_sets(w)
+        _, sets = make_sets(w, R, device, torch, inputs)
+        prepared[name] = (w, sets)
+    stream = torch.cuda.current_stream()
+    for name, (w, sets) in prepared.items():  # first calls (descriptors, plans) untimed
+        s = sets[0]
+        gb.attn_fwd(s[0], s[1], s[2], causal=w.causal, scale=w.scale, o=s[3], lse=s[4], stream=stream)
+    torch.cuda.synchronize()
+    events = {name: [] for name in prepared}
+    for r in range(reps):
+        for name, (w, sets) in prepared.items():
+            s = sets[r % len(sets)]
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(200000)
+            a.record(stream)
+            gb.attn_fwd(s[0], s[1], s[2], causal=w.causal, scale=w.scale, o=s[3], lse=s[4], stream=stream)
+            b.record(stream)
+            events[name].append((a, b))
+        if r % 50 == 49:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    out = {}
+    for name, ev in events.items():
+        ts = sorted(a.elapsed_time(b) * 1e-3 for a, b in ev)
+        n = len(ts)
+        out[name] = (ts[n // 2], ts[max(0, n // 10)], ts[min(n - 1, (9 * n) // 10)])
+    del prepared
+    return out
+
+
 def cpu_oracle_baseline(w, min_seconds=10.0, max_reps=20):
     """Float64 oracle, as it stands, on the host cores: whole workload, repeated until
     about `min_seconds` of CPU work (bounded by max_reps)."""
@@ -281,6 +323,19 @@ def cpu_oracle_baseline(w, min_seconds=10.0, max_reps=20):
     nthreads = int(os.environ.get("OMP_NUM_THREADS", "0")) or len(os.sched_getaffinity(0))
     t = total / reps
     return t, reps, nthreads
+
+
+def oracle_one_thread(w, reps=5):
+    """Seconds per call of the float64 oracle on one host thread for workload w."""
+    import oracle
+    from scaled_dot_product_sdpa_gb300 import inputs
+    q, k, v = inputs.qkv(w.B, w.H, w.L, w.d, w.seed, w.sigma)
+    qf, kf, vf = (oracle._f64(t) for t in (q, k, v))
+    scale = float(__import__("numpy").float32(w.scale))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.sdpa_fwd(qf, kf, vf, w.causal, scale, nthreads=1)
+    return (time.perf_counter() - t0) / reps
 
 
 def bench_ours(args):
@@ -332,7 +387,9 @@ def bench_ours(args):
     hbm_peak = peaks["hbm_gbs"]
     achieved_gbs = w.bytes() / t_max / 1e9
     bound = "hbm" if w.flops() / w.bytes() < fp16_peak * 1e12 / (hbm_peak * 1e9) else "tensor"
-    traffic = stored_traffic(w.name, w.d)
+    sm_count = torch.cuda.get_device_properties(device).multi_processor_count
+    kname = kernel_name(w, sm_count)
+    traffic = stored_traffic(w.name, kname)
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved_gbs / hbm_peak, 4)}
@@ -340,7 +397,7 @@ def bench_ours(args):
         roof = {"bound": "tensor", "achieved": round(w.flops() / t_max / 1e12, 1), "peak": fp16_peak,
                 "unit": "TFLOP/s", "frac": round(w.flops() / t_max / 1e12 / fp16_peak, 4)}
     roof["traffic"] = traffic
-    roof["kernel"] = kernel_name(w.d)
+    roof["kernel"] = kname
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
     roof["algorithmic_bytes_per_launch"] = w.bytes()
     roof["algorithmic_flops_per_launch"] = w.flops()
@@ -368,11 +425,22 @@ def bench_ours(args):
         for name, wk in WORKLOADS.items():
             tk = bench_workload(wk, 200, 10, device, torch, gb, inputs, world)[0]
             fl = wk.flops() / tk / 1e12
-            per[name] = {"shape": wk.describe(), "us": round(tk * 1e6, 3), "tflops": round(fl, 1),
-                         "pct_fp16_peak": round(100 * fl / fp16_peak, 2),
+            # Attainable: the lower of the tensor roof and (FLOP/byte) x the HBM roof.
+            attain = min(fp16_peak, wk.flops() / wk.bytes() * hbm_peak * 1e9 / 1e12)
+            per[name] = {"shape": wk.describe(), "kernel": kernel_name(wk, sm_count), "us": round(tk * 1e6, 3),
+                         "tflops": round(fl, 1), "pct_fp16_peak": round(100 * fl / fp16_peak, 2),
                          "hbm_gbs": round(wk.bytes() / tk / 1e9, 1),
-                         "pct_hbm_peak": round(100 * wk.bytes() / tk / 1e9 / hbm_peak, 2)}
+                         "pct_hbm_peak": round(100 * wk.bytes() / tk / 1e9 / hbm_peak, 2),
+                         "attainable_tflops": round(attain, 1), "pct_attainable": round(100 * fl / attain, 2)}
+        # Per-call distribution, interleaved across the configs (300 rounds).
+        dist_t = interleaved_per_call(WORKLOADS, 300, device, torch, gb, inputs)
+        for name, (med, p10, p90) in dist_t.items():
+            per[name].update({"per_call_us_median": round(med * 1e6, 3), "per_call_us_p10": round(p10 * 1e6, 3),
+                              "per_call_us_p90": round(p90 * 1e6, 3)})
         line["per_config"] = per
+        line["per_config_timing"] = ("us: mean of 200 graph-replayed calls over rotating input sets; "
+                                     "per_call_*: 300 single calls interleaved across the configs, CUDA events "
+                                     "around each call behind a GPU-side sleep")
         status = gb.attn_last_device_error()
         if status != 0:
             raise RuntimeError(f"device status {status}: {gb.attn_strerror(status)}")
@@ -381,6 +449,9 @@ def bench_ours(args):
             line["cpu_baseline"] = {"value": round(w.flops() / tc / 1e12, 6), "unit": "TFLOPS", "cores": cores,
                                     "kind": "oracle", "seconds_per_call": round(tc, 3),
                                     "sample": f"the whole {w.name} workload, {reps} call(s), float64 C oracle"}
+            # The smallest config on one thread as well (the same oracle, nthreads = 1).
+            t1 = oracle_one_thread(WORKLOADS["caseA"])
+            line["cpu_baseline"]["caseA_one_thread_seconds"] = round(t1, 4)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
