@@ -29,6 +29,8 @@
 #ifndef GBATTN_H
 #define GBATTN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -44,6 +46,7 @@ extern "C" {
 #define GBATTN_ERR_ALIAS (-8)       /* an output overlaps an input or the other output       */
 #define GBATTN_ERR_TENSORMAP (-9)   /* the driver rejected a TMA descriptor                  */
 #define GBATTN_ERR_FLAGS (-10)      /* attn_fwd_ex: unknown bits in flags                    */
+#define GBATTN_ERR_WORKSPACE (-11)  /* attn_fwd_host: device workspace too small             */
 
 /* Device-side status codes reported by attn_last_device_error() (positive). */
 #define GBATTN_DEV_TIMEOUT_LOAD 1    /* the TMA producer's wait for a free buffer timed out  */
@@ -91,6 +94,32 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
 int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                 int H, int L, int d, int causal, float scale, void *stream, int flags,
                 int grid_limit);
+
+/*
+ * attn_fwd_host -- attn_fwd on inputs and outputs in HOST memory, for callers whose
+ * tensors are not on the GPU.  Same operation, arguments and errors as attn_fwd, except:
+ *   q, k, v, o, lse : HOST pointers (page-locked memory -- e.g. cudaHostAlloc or
+ *                     PyTorch pin_memory -- for the copies to overlap; other host
+ *                     memory works, the driver then stages the copies), any alignment.
+ *   workspace       : DEVICE memory of at least attn_fwd_host_workspace_size(B, H, L, d)
+ *                     bytes, 256-byte aligned (else GBATTN_ERR_ALIGN), owned by the caller;
+ *                     too small: GBATTN_ERR_WORKSPACE.  Launches that share a workspace
+ *                     must not overlap on the GPU (give them one stream).
+ * The heads are cut into chunks of about 12 MB of Q+K+V; chunk by chunk, the library's
+ * own streams copy Q, K, V in, run the forward pass, and copy O and LSE out, through two
+ * alternating halves of the workspace, so that the copies in, the kernels and the copies
+ * out of different chunks overlap (the host link is the bound: ~0.2 TB/s each way on
+ * GB300).  The work starts after what is already queued on `stream`, and `stream` waits
+ * for its end: synchronise `stream` before reading o and lse.  The streams and events are
+ * created on the first call per device and kept; calls from several host threads are
+ * serialised.
+ */
+int attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                  int L, int d, int causal, float scale, void *workspace, size_t workspace_bytes,
+                  void *stream);
+
+/* Device workspace bytes attn_fwd_host needs for this shape (0 for invalid arguments). */
+size_t attn_fwd_host_workspace_size(int B, int H, int L, int d);
 
 /*
  * attn_debug_scores -- test hook: the raw scaled logits s[b,h,i,j] = scale * q_i . k_j

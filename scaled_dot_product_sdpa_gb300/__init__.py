@@ -6,9 +6,9 @@ tensor cores, tensor memory) behind the C ABI of include/gbattn.h.  This package
 thin Python binding of that library; every step of the computation runs on the GPU.
 """
 from ._binding import (FLAG_P_SMEM, FLAG_SINGLE_TILE, FLAG_TWO_TILE, LIB_PATH, GbattnError,
-                       attn_debug_plan, attn_debug_schedule, attn_debug_scores, attn_debug_wait_probe, attn_fwd,
+                       attn_debug_plan, attn_debug_schedule, attn_debug_scores, attn_debug_wait_probe, attn_fwd, attn_fwd_host,
                        attn_last_device_error, attn_strerror, attn_version, load_library)
 
-__all__ = ["attn_fwd", "attn_debug_plan", "attn_debug_scores", "attn_debug_schedule", "attn_debug_wait_probe",
+__all__ = ["attn_fwd", "attn_fwd_host", "attn_debug_plan", "attn_debug_scores", "attn_debug_schedule", "attn_debug_wait_probe",
            "attn_last_device_error", "attn_strerror", "attn_version", "load_library", "GbattnError", "FLAG_P_SMEM",
            "FLAG_SINGLE_TILE", "FLAG_TWO_TILE", "LIB_PATH"]

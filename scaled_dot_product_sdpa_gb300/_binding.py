@@ -54,6 +54,11 @@ def load_library(path: str | None = None):
     ip = ctypes.POINTER(ctypes.c_int)
     lib.attn_debug_schedule.argtypes = [i, i, i, i, i, i, i, ip, ip, i]
     lib.attn_debug_schedule.restype = i
+    sz = ctypes.c_size_t
+    lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    lib.attn_fwd_host.restype = i
+    lib.attn_fwd_host_workspace_size.argtypes = [i, i, i, i]
+    lib.attn_fwd_host_workspace_size.restype = sz
     lib.attn_debug_plan.argtypes = [i, i, i, i, i, i, i, i, ip]
     lib.attn_debug_plan.restype = i
     lib.attn_version.argtypes = []
@@ -165,3 +170,48 @@ def attn_debug_plan(B: int, H: int, L: int, d: int, causal: bool, sm_count: int,
     if rc != 0:
         raise GbattnError(rc, "attn_debug_plan")
     return {"kind": out[0], "items": out[1], "grid": out[2], "makespan": out[3] / 100.0}
+
+
+# Device workspaces of attn_fwd_host, one per (device, stream): calls on one stream never
+# overlap on the GPU, calls on different streams may.
+_host_workspaces: dict = {}
+
+
+def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None,
+                  device=None, stream=None):
+    """O, LSE = SDPA forward of fp16 [B, H, L, d] CPU tensors q, k, v (pin them for the
+    copies to overlap), computed on `device` (default: the current CUDA device) in
+    chunks whose host<->device copies overlap the kernels.  Outputs are CPU tensors
+    (pinned, allocated here unless given).  Enqueued on `stream` (default: the device's
+    current stream); synchronise it before reading the outputs."""
+    for t in (q, k, v):
+        if t.is_cuda:
+            raise ValueError("gbattn: attn_fwd_host takes CPU tensors (use attn_fwd for CUDA tensors)")
+        if t.dtype != torch.float16 or t.dim() != 4 or not t.is_contiguous() or t.shape != q.shape:
+            raise ValueError("gbattn: q, k, v must be contiguous float16 [B, H, L, d] of one shape")
+    B, H, L, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, H, L), dtype=torch.float32).pin_memory()
+    if o.is_cuda or o.shape != q.shape or o.dtype != torch.float16 or not o.is_contiguous():
+        raise ValueError("gbattn: o must be a contiguous float16 CPU tensor like q")
+    if lse.is_cuda or lse.shape != (B, H, L) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("gbattn: lse must be a contiguous float32 CPU tensor [B, H, L]")
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    lib = load_library()
+    with torch.cuda.device(device):
+        sh = _stream_handle(stream)
+        need = int(lib.attn_fwd_host_workspace_size(B, H, L, d))
+        key = (device.index, sh)
+        ws = _host_workspaces.get(key)
+        if ws is None or ws.numel() < need:
+            ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+            _host_workspaces[key] = ws
+        rc = lib.attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               B, H, L, d, int(bool(causal)), float(scale), ws.data_ptr(), ws.numel(), sh)
+    if rc != 0:
+        raise GbattnError(rc, "attn_fwd_host")
+    return o, lse

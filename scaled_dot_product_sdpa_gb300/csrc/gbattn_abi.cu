@@ -342,6 +342,131 @@ extern "C" int attn_fwd(const void *q, const void *k, const void *v, void *o, fl
   return attn_fwd_ex(q, k, v, o, lse, B, H, L, d, causal, scale, stream, 0, 0);
 }
 
+// ------------------------------------------------------------------ host buffers
+namespace gbattn {
+namespace {
+
+// Heads per chunk of attn_fwd_host: chunks of about 12 MB of Q+K+V (the copy engines
+// reach ~205 GB/s from 16 MB chunks, ~190 from 4 MB ones on GB300), at least 4 chunks
+// when there are enough heads, so the copies of one chunk overlap the others' work.
+long long host_chunk_heads(long long BH, int L, int d) {
+  const long long head_qkv = 3LL * L * d * 2;
+  long long ch = std::max(1LL, (12LL << 20) / head_qkv);
+  ch = std::min(ch, std::max(1LL, (BH + 3) / 4));
+  return std::min(ch, BH);
+}
+size_t host_chunk_bytes(long long ch, int L, int d) {
+  auto up = [](size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); };
+  const size_t t = static_cast<size_t>(ch) * L * d * 2u;
+  return 4u * up(t) + up(static_cast<size_t>(ch) * L * 4u);  // q, k, v, o, lse
+}
+
+// Streams and events of the host-buffer pipeline, created once per device.
+struct HostPipe {
+  bool init = false;
+  cudaStream_t s_in = nullptr, s_comp = nullptr, s_out = nullptr;
+  cudaEvent_t start = nullptr, in_done[2] = {}, comp_done[2] = {}, out_done[2] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mu;
+
+int host_pipe(HostPipe **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GBATTN_ERR_LAUNCH;
+  if (dev < 0 || dev >= kMaxDevices) return GBATTN_ERR_DEVICE;
+  HostPipe &hp = g_pipe[dev];
+  if (!hp.init) {
+    const unsigned f = cudaEventDisableTiming;
+    if (cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&hp.s_comp, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp.start, f) != cudaSuccess)
+      return GBATTN_ERR_LAUNCH;
+    for (int i = 0; i < 2; ++i)
+      if (cudaEventCreateWithFlags(&hp.in_done[i], f) != cudaSuccess ||
+          cudaEventCreateWithFlags(&hp.comp_done[i], f) != cudaSuccess ||
+          cudaEventCreateWithFlags(&hp.out_done[i], f) != cudaSuccess)
+        return GBATTN_ERR_LAUNCH;
+    hp.init = true;
+  }
+  *out = &hp;
+  return GBATTN_OK;
+}
+
+}  // namespace
+}  // namespace gbattn
+
+extern "C" size_t attn_fwd_host_workspace_size(int B, int H, int L, int d) {
+  if (check_shape(B, H, L, d) != GBATTN_OK) return 0;
+  const long long BH = static_cast<long long>(B) * H;
+  return 2u * host_chunk_bytes(host_chunk_heads(BH, L, d), L, d);
+}
+
+extern "C" int attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int L,
+                             int d, int causal, float scale, void *workspace, size_t workspace_bytes, void *stream) {
+  if (!q || !k || !v || !o || !lse || !workspace) return GBATTN_ERR_NULL;
+  int rc = check_shape(B, H, L, d);
+  if (rc != GBATTN_OK) return rc;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return GBATTN_ERR_SCALE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GBATTN_ERR_ALIGN;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long ch = host_chunk_heads(BH, L, d);
+  const size_t slot_bytes = host_chunk_bytes(ch, L, d);
+  if (workspace_bytes < 2u * slot_bytes) return GBATTN_ERR_WORKSPACE;
+  const size_t rows = static_cast<size_t>(BH) * L;
+  const size_t tbytes = rows * d * 2u, lbytes = rows * 4u;
+  if (overlaps(o, tbytes, q, tbytes) || overlaps(o, tbytes, k, tbytes) || overlaps(o, tbytes, v, tbytes) ||
+      overlaps(lse, lbytes, q, tbytes) || overlaps(lse, lbytes, k, tbytes) || overlaps(lse, lbytes, v, tbytes) ||
+      overlaps(lse, lbytes, o, tbytes))
+    return GBATTN_ERR_ALIAS;
+  DevInfo *di = nullptr;
+  if ((rc = device_info(&di)) != GBATTN_OK) return rc;
+  HostPipe *hp = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    if ((rc = host_pipe(&hp)) != GBATTN_OK) return rc;
+    const cudaStream_t user = static_cast<cudaStream_t>(stream);
+    auto up = [](size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); };
+    const size_t t_ch = up(static_cast<size_t>(ch) * L * d * 2u);
+    // Everything starts after the work already queued on the caller's stream.
+    if (cudaEventRecord(hp->start, user) != cudaSuccess || cudaStreamWaitEvent(hp->s_in, hp->start, 0) != cudaSuccess)
+      return GBATTN_ERR_LAUNCH;
+    const size_t head_t = static_cast<size_t>(L) * d * 2u, head_l = static_cast<size_t>(L) * 4u;
+    int c = 0;
+    for (long long h0 = 0; h0 < BH; h0 += ch, ++c) {
+      const long long nh = std::min(ch, BH - h0);
+      const int slot = c & 1;
+      char *base = static_cast<char *>(workspace) + slot * slot_bytes;
+      char *dq = base, *dk = base + t_ch, *dv = base + 2 * t_ch, *dO = base + 3 * t_ch;
+      float *dl = reinterpret_cast<float *>(base + 4 * t_ch);
+      const size_t nb = static_cast<size_t>(nh) * head_t, nl = static_cast<size_t>(nh) * head_l;
+      const size_t off = static_cast<size_t>(h0) * head_t, offl = static_cast<size_t>(h0) * head_l;
+      // The slot is free once the chunk two back has been copied out (its kernel read
+      // the inputs before that).
+      if (c >= 2 && cudaStreamWaitEvent(hp->s_in, hp->out_done[slot], 0) != cudaSuccess) return GBATTN_ERR_LAUNCH;
+      if (cudaMemcpyAsync(dq, static_cast<const char *>(q) + off, nb, cudaMemcpyHostToDevice, hp->s_in) != cudaSuccess ||
+          cudaMemcpyAsync(dk, static_cast<const char *>(k) + off, nb, cudaMemcpyHostToDevice, hp->s_in) != cudaSuccess ||
+          cudaMemcpyAsync(dv, static_cast<const char *>(v) + off, nb, cudaMemcpyHostToDevice, hp->s_in) != cudaSuccess ||
+          cudaEventRecord(hp->in_done[slot], hp->s_in) != cudaSuccess ||
+          cudaStreamWaitEvent(hp->s_comp, hp->in_done[slot], 0) != cudaSuccess)
+        return GBATTN_ERR_LAUNCH;
+      if ((rc = attn_fwd(dq, dk, dv, dO, dl, 1, static_cast<int>(nh), L, d, causal, scale, hp->s_comp)) != GBATTN_OK)
+        return rc;
+      if (cudaEventRecord(hp->comp_done[slot], hp->s_comp) != cudaSuccess ||
+          cudaStreamWaitEvent(hp->s_out, hp->comp_done[slot], 0) != cudaSuccess ||
+          cudaMemcpyAsync(static_cast<char *>(o) + off, dO, nb, cudaMemcpyDeviceToHost, hp->s_out) != cudaSuccess ||
+          cudaMemcpyAsync(reinterpret_cast<char *>(lse) + offl, dl, nl, cudaMemcpyDeviceToHost, hp->s_out) !=
+              cudaSuccess ||
+          cudaEventRecord(hp->out_done[slot], hp->s_out) != cudaSuccess)
+        return GBATTN_ERR_LAUNCH;
+    }
+    // The caller's stream continues once the last copy out is done (the copies out run
+    // in order on one stream).
+    if (cudaStreamWaitEvent(user, hp->out_done[(c - 1) & 1], 0) != cudaSuccess) return GBATTN_ERR_LAUNCH;
+  }
+  return GBATTN_OK;
+}
+
 extern "C" int attn_debug_scores(const void *q, const void *k, float *s, int B, int H, int L, int d, float scale,
                                  void *stream) {
   if (!q || !k || !s) return GBATTN_ERR_NULL;
@@ -399,6 +524,7 @@ extern "C" const char *attn_strerror(int code) {
     case GBATTN_ERR_ALIAS: return "an output overlaps an input or the other output";
     case GBATTN_ERR_TENSORMAP: return "the driver rejected a TMA tensor-map descriptor";
     case GBATTN_ERR_FLAGS: return "flags holds bits that name no option";
+    case GBATTN_ERR_WORKSPACE: return "the device workspace is smaller than attn_fwd_host_workspace_size()";
     case GBATTN_DEV_TIMEOUT_LOAD: return "device: the TMA producer's wait timed out";
     case GBATTN_DEV_TIMEOUT_MMA: return "device: the MMA issuer's wait timed out";
     case GBATTN_DEV_TIMEOUT_SOFTMAX: return "device: a softmax warp's wait timed out";

@@ -127,3 +127,30 @@ def test_debug_scores_validation(lib):
     assert lib.attn_debug_scores(Q, K, O, 1, 1, 128, 48, 0.1, None) == c["GBATTN_ERR_HEAD_DIM"]
     assert lib.attn_debug_scores(Q, K, O + 4, 1, 1, 128, 64, 0.1, None) == c["GBATTN_ERR_ALIGN"]
     assert lib.attn_debug_scores(Q, K, Q, 1, 1, 128, 64, 0.1, None) == c["GBATTN_ERR_ALIAS"]
+
+
+WS = 0x60000000  # fake, 256-byte-aligned device workspace
+
+
+def _host(lib, q=Q, k=K, v=V, o=O, lse=LSE, B=1, H=2, L=128, d=64, scale=0.125, ws=WS, ws_bytes=1 << 30):
+    return lib.attn_fwd_host(q, k, v, o, lse, B, H, L, d, 1, scale, ws, ws_bytes, None)
+
+
+def test_host_entry_validation(lib):
+    c = _codes()
+    for kw in ("q", "k", "v", "o", "lse", "ws"):
+        assert _host(lib, **{kw: 0}) == c["GBATTN_ERR_NULL"]
+    assert _host(lib, d=96) == c["GBATTN_ERR_HEAD_DIM"]
+    assert _host(lib, L=0) == c["GBATTN_ERR_DIMS"]
+    assert _host(lib, scale=float("nan")) == c["GBATTN_ERR_SCALE"]
+    assert _host(lib, ws=WS + 16) == c["GBATTN_ERR_ALIGN"]
+    assert _host(lib, ws_bytes=1024) == c["GBATTN_ERR_WORKSPACE"]
+    assert _host(lib, o=Q) == c["GBATTN_ERR_ALIAS"]
+
+
+def test_host_workspace_size(lib):
+    lib.attn_fwd_host_workspace_size.restype = ctypes.c_size_t
+    # caseD: 256 heads of 512 x 128 -> chunks of 32 heads (12 MB of Q+K+V), two slots of
+    # q, k, v, o (4 x 4 MiB) and lse (64 KiB).
+    assert lib.attn_fwd_host_workspace_size(8, 32, 512, 128) == 2 * (4 * 32 * 512 * 128 * 2 + 32 * 512 * 4)
+    assert lib.attn_fwd_host_workspace_size(1, 1, 0, 64) == 0

@@ -246,6 +246,42 @@ def test_runs_on_a_side_stream():
     _check(o, lse, o_ref, lse_ref, "side stream")
 
 
+@pytest.mark.parametrize("B,H,L,d,causal", [(2, 10, 300, 64, True), (1, 9, 200, 128, False), (1, 3, 300, 512, True),
+                                             (1, 1, 129, 64, True)])
+def test_host_buffer_entry_matches_oracle(B, H, L, d, causal):
+    """attn_fwd_host: chunked copies in, kernels, copies out on the library's streams."""
+    q, k, v = inputs.qkv(B, H, L, d, seed=17 * L + d, sigma=0.5 if d == 512 else 1.0)
+    scale = 1.0 / math.sqrt(d)
+    qp, kp, vp = (t.pin_memory() for t in (q, k, v))
+    s = torch.cuda.Stream()
+    o, lse = gb.attn_fwd_host(qp, kp, vp, causal=causal, scale=scale, stream=s)
+    s.synchronize()
+    o_ref, lse_ref = oracle.sdpa_fwd(q, k, v, causal, float(np.float32(scale)))
+    _check(o, lse, o_ref, lse_ref, f"host entry {B}x{H}x{L}x{d}")
+    # pageable (not pinned) host memory works too, and repeated calls agree bitwise
+    o2, l2 = gb.attn_fwd_host(q, k, v, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, o) and torch.equal(l2, lse)
+
+
+def test_host_buffer_entry_orders_with_the_callers_stream():
+    """The pipeline starts after work queued on the caller's stream: inputs filled by a
+    copy on that stream just before the call are the ones used."""
+    w = WORKLOADS["caseB"]
+    q, k, v = inputs.qkv(w.B, w.H, w.L, w.d, w.seed, w.sigma)
+    qp, kp, vp = (torch.zeros_like(t).pin_memory() for t in (q, k, v))
+    src = [t.cuda() for t in (q, k, v)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(2_000_000)  # the copies below land late unless the call waits for them
+        for dst, x in zip((qp, kp, vp), src):
+            dst.copy_(x, non_blocking=True)
+        o, lse = gb.attn_fwd_host(qp, kp, vp, causal=w.causal, scale=w.scale, stream=s)
+    s.synchronize()
+    o_ref, lse_ref = oracle.sdpa_fwd(q, k, v, w.causal, float(np.float32(w.scale)))
+    _check(o, lse, o_ref, lse_ref, "host entry after queued copies")
+
+
 def test_cpu_tensors_are_rejected_loudly():
     q, k, v = inputs.qkv(1, 1, 128, 64, seed=1)
     with pytest.raises(ValueError):
