@@ -346,14 +346,26 @@ extern "C" int attn_fwd(const void *q, const void *k, const void *v, void *o, fl
 namespace gbattn {
 namespace {
 
-// Heads per chunk of attn_fwd_host: chunks of about 12 MB of Q+K+V (the copy engines
-// reach ~205 GB/s from 16 MB chunks, ~190 from 4 MB ones on GB300), at least 4 chunks
-// when there are enough heads, so the copies of one chunk overlap the others' work.
+// Heads per chunk of attn_fwd_host: chunks of about 24 MB of Q+K+V, at least 4 chunks
+// when there are enough heads.  On GB300 every host-link copy costs ~2 us of ramp on top
+// of its bytes (4 MB copies reach ~177 GB/s, 32 MB ones ~206), and only the copy out of
+// the last chunk is not hidden behind the copies in, so a few large chunks with a short
+// final one beat many small chunks.
 long long host_chunk_heads(long long BH, int L, int d) {
   const long long head_qkv = 3LL * L * d * 2;
-  long long ch = std::max(1LL, (12LL << 20) / head_qkv);
+  long long ch = std::max(1LL, (24LL << 20) / head_qkv);
   ch = std::min(ch, std::max(1LL, (BH + 3) / 4));
   return std::min(ch, BH);
+}
+// Size of the chunk of attn_fwd_host that starts at head h0: `ch` heads, except that the
+// last `ch` or fewer heads are cut 3:1 (when there are at least 4) so that the final
+// kernel and copy out, which nothing overlaps, are short.
+long long host_chunk_at(long long BH, long long ch, long long h0) {
+  const long long r = BH - (BH - 1) / ch * ch;  // heads of the last full-size slot, 1..ch
+  const long long tail = BH - r;
+  if (h0 < tail) return ch;
+  if (h0 == tail && r >= 4) return r - r / 4;
+  return BH - h0;
 }
 size_t host_chunk_bytes(long long ch, int L, int d) {
   auto up = [](size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); };
@@ -433,8 +445,8 @@ extern "C" int attn_fwd_host(const void *q, const void *k, const void *v, void *
       return GBATTN_ERR_LAUNCH;
     const size_t head_t = static_cast<size_t>(L) * d * 2u, head_l = static_cast<size_t>(L) * 4u;
     int c = 0;
-    for (long long h0 = 0; h0 < BH; h0 += ch, ++c) {
-      const long long nh = std::min(ch, BH - h0);
+    for (long long h0 = 0, nh = 0; h0 < BH; h0 += nh, ++c) {
+      nh = host_chunk_at(BH, ch, h0);
       const int slot = c & 1;
       char *base = static_cast<char *>(workspace) + slot * slot_bytes;
       char *dq = base, *dk = base + t_ch, *dv = base + 2 * t_ch, *dO = base + 3 * t_ch;

@@ -150,7 +150,7 @@ def test_host_entry_validation(lib):
 
 def test_host_workspace_size(lib):
     lib.attn_fwd_host_workspace_size.restype = ctypes.c_size_t
-    # caseD: 256 heads of 512 x 128 -> chunks of 32 heads (12 MB of Q+K+V), two slots of
-    # q, k, v, o (4 x 4 MiB) and lse (64 KiB).
-    assert lib.attn_fwd_host_workspace_size(8, 32, 512, 128) == 2 * (4 * 32 * 512 * 128 * 2 + 32 * 512 * 4)
+    # caseD: 256 heads of 512 x 128 -> chunks of 64 heads (24 MB of Q+K+V), two slots of
+    # q, k, v, o (4 x 8 MiB) and lse (128 KiB).
+    assert lib.attn_fwd_host_workspace_size(8, 32, 512, 128) == 2 * (4 * 64 * 512 * 128 * 2 + 64 * 512 * 4)
     assert lib.attn_fwd_host_workspace_size(1, 1, 0, 64) == 0
