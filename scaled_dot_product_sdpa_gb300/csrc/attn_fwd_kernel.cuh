@@ -183,6 +183,25 @@ struct WaitSet {
     }
     ++n;
   }
+  // Non-blocking: the first phase not yet complete (false when all are).
+  __device__ bool first_pending(uint32_t &b, uint32_t &ph) const {
+    if (!mbar_test(b0, p0)) {
+      b = b0;
+      ph = p0;
+      return true;
+    }
+    if (n > 1 && !mbar_test(b1, p1)) {
+      b = b1;
+      ph = p1;
+      return true;
+    }
+    if (n > 2 && !mbar_test(b2, p2)) {
+      b = b2;
+      ph = p2;
+      return true;
+    }
+    return false;
+  }
   // Non-blocking: are all phases complete?
   __device__ bool test() const {
     bool all = mbar_test(b0, p0);

@@ -5,24 +5,23 @@
 // row LSE, fused into one persistent kernel.  The work item is a 256-row query block
 // split into two 128-row tiles Q0 and Q1 ("slots") that share every K/V tile the
 // producer loads (half the K/V traffic per query row of the single-tile kernel).  Each
-// slot has its own S buffer and O accumulator in tensor memory, its own softmax
-// warpgroup and its own MMA-issuing thread:
+// slot has its own S buffer and O accumulator in tensor memory and its own softmax
+// warpgroup:
 //   TMEM columns  S0 [0,128)  S1 [128,256)  O0 [256, 256+D)  O1 [256+D, 256+2D).
 //
-// Slot a's issuer runs the chain  QK_0, then for each key tile j:  PV_j, QK_{j+1}
-// (QK_{j+1} after the last tile is the first QK of the next item).  PV_j comes right
-// before QK_{j+1} from the same thread, so when softmax warpgroup a sees S of tile j+1
-// complete, PV of tile j is complete too (tcgen05 operations of one thread complete in
-// order): the lazy O rescale never waits for a PV.  The two issuers' MMAs interleave in
-// the tensor core's queue, so while slot a waits for its softmax the tensor core runs
-// slot b's work and neither slot's wait holds the other back.  Under the causal mask Q0
-// needs key tiles 0..2qb and Q1 needs 0..2qb+1; the last one belongs to Q1 alone.
+// One thread issues every MMA, both slots' in one stream (see PPIssuer): PV_a of tile j
+// comes right before QK_a of tile j+1 from that thread, so when softmax warpgroup a sees
+// S of tile j+1 complete, PV of tile j is complete too (tcgen05 operations of one thread
+// complete in order) and the lazy O rescale never waits for a PV; and the two slots
+// alternate on the tensor core, so each softmax warpgroup works while the tensor core
+// runs the other slot's PV and QK.  Under the causal mask Q0 needs key tiles 0..2qb and
+// Q1 needs 0..2qb+1; the last one belongs to Q1 alone.
 //
 // Warp roles (384 threads):
 //   warp 0      K/V producer: per item, K_0, V_0, K_1, V_1, ... into an mbarrier ring; a
 //               stage is free again once both slots released it (the producer itself
 //               gives the release for tiles only Q1 uses).
-//   warp 1      TMEM owner + MMA issuer of slot 0;  warp 2  MMA issuer of slot 1.
+//   warp 1      TMEM owner + MMA issuer;  warp 2 idle.
 //   warp 3      Q loader and O store issuer.  Each slot has one Q buffer, released by the
 //               commit of the slot's last QK of an item, so the next item's Q tile lands
 //               while the last softmax and PV of the current one run.  Finished O tiles
@@ -40,7 +39,6 @@
 #include "softmax_tile.cuh"
 
 namespace gbattn {
-
 template <int D>
 struct PPCfg {
   static constexpr int NCH = D / 64;
@@ -58,7 +56,7 @@ struct PPCfg {
   static constexpr int B_SFULL = 4 + 2 * NST, B_PFULL = B_SFULL + 2, B_OFINAL = B_PFULL + 2;
   static constexpr int B_OFREE = B_OFINAL + 2, B_GRANT = B_OFREE + 2, B_EPI = B_GRANT + 2;
   static constexpr int B_DRAIN = B_EPI + 2;
-  static constexpr int NBAR = B_DRAIN + 2;
+  static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int TILE_BYTES = NST * TILE + (NQBUF + NOBUF) * TILE;
   static constexpr int SMEM_BYTES = 1024 + TILE_BYTES + 8 * NBAR + 16;
   static constexpr int O_COL = 256;
@@ -96,34 +94,43 @@ __device__ __forceinline__ uint32_t pp_q_tile(uint32_t q_s, int slot) {
   return q_s + static_cast<uint32_t>(slot) * PPCfg<D>::TILE;
 }
 
-// MMA issuer of one slot.  Ring positions follow the producer's load order: item by item,
-// K_0, V_0, K_1, V_1, ... for the n1 key tiles of the item.
+// The MMA issuer: one thread issues the tensor-core work of both slots, so the operations
+// reach the tensor core in program order (MMAs issued by two threads are interleaved by
+// the hardware, which makes both slots' S tiles complete together and both softmax
+// warpgroups run at once while the tensor core idles).  Within an item the order is
+//     QK0_0, QK1_0, then for each key tile j:  PV0_j, QK0_{j+1}, PV1_j, QK1_{j+1}
+// so softmax warpgroup 0 works on S0 while the tensor core runs PV1 and QK1, and the
+// other way round.  The next item's QK0_0 cannot be issued right after the slot's last PV
+// (its Q tile is loaded only once the slot's last QK released the buffer): it is issued
+// from inside the issuer's later waits as soon as its Q and K tiles have landed, and at
+// the latest before the next item's QK1_0, so it never holds back slot 1's work.
+// Ring positions follow the producer's load order: item by item, K_0, V_0, K_1, V_1, ...
+// for the n1 key tiles of the item.
 template <int D, bool CAUSAL>
 struct PPIssuer {
   using C = PPCfg<D>;
   const FwdParams *p;
   uint32_t ring_s, q_s, bar_s, tmem;
   volatile uint32_t *abort_flag;
-  int slot;
-  uint32_t base = 0;  // ring position of K_0 of the current item
-  uint32_t n_pv = 0;  // PVs of this slot so far (phase of its P barrier)
+  uint32_t base = 0;                // ring position of K_0 of the current item
+  uint32_t n_pv0 = 0, n_pv1 = 0;    // PVs per slot so far (phases of the P barriers)
+  // The next item's slot-0 QK, while it waits for its Q and K tiles.
+  bool side_pending = false, side_last = false;
+  int side_il = 0;
+  uint32_t side_base = 0;
+
   __device__ uint32_t bar(int i) const { return bar_s + 8u * static_cast<uint32_t>(i); }
-  __device__ bool wait_all(const WaitSet &ws) {
-    if (!ws.wait(abort_flag, p->status, kDevTimeoutMma, p->wait_limit)) return false;
-    tc_fence_after();
-    return true;
+  __device__ bool side_ready() const {
+    return mbar_test(bar(C::B_QFULL + 0), side_il & 1) &&
+           mbar_test(bar(C::B_FULL + side_base % C::NST), (side_base / C::NST) & 1u);
   }
-  // S_slot = Q_slot K_j^T, then release K_j's stage and signal the softmax; after the
-  // slot's last key tile of the item (`last`) the Q buffer is released too.
-  __device__ bool qk(int j, int il, uint32_t item_base, bool last) {
-    const uint32_t pos = item_base + 2u * static_cast<uint32_t>(j);
-    WaitSet ws;
-    if (j == 0) ws.add(bar(C::B_QFULL + slot), il & 1);
-    ws.add(bar(C::B_FULL + pos % C::NST), (pos / C::NST) & 1u);
-    if (!wait_all(ws)) return false;
+  // S_slot = Q_slot K_j^T for the K tile at ring position pos, then release the stage and
+  // signal the softmax; after the slot's last key tile of the item (`last`) the Q buffer
+  // is released too.  Its inputs must have landed.
+  __device__ void qk_issue(int slot, uint32_t pos, bool last) {
     const SDesc a = sdesc_split(sdesc_sw128(pp_q_tile<D>(q_s, slot), 16, 1024));
     const SDesc b = sdesc_split(sdesc_sw128(ring_s + (pos % C::NST) * C::TILE, 16, 1024));
-    const uint32_t d_tmem = tmem + slot * 128u;
+    const uint32_t d_tmem = tmem + static_cast<uint32_t>(slot) * 128u;
 #pragma unroll
     for (int c = 0; c < C::NCH; ++c)
 #pragma unroll
@@ -133,26 +140,67 @@ struct PPIssuer {
     umma_commit(bar(C::B_SFULL + slot));
     umma_commit(bar(C::B_EMPTY + pos % C::NST));
     if (last) umma_commit(bar(C::B_QEMPTY + slot));
+  }
+  // Wait for every phase of ws.  While the next item's slot-0 QK is pending, the wait
+  // polls (suspending ~0.1 us at a time) and issues that QK as soon as its inputs are in.
+  __device__ bool wait_all(const WaitSet &ws) {
+    if (side_pending) {
+      const long long t0 = clock64();
+      uint32_t b, ph;
+      while (ws.first_pending(b, ph)) {
+        if (side_ready()) {
+          tc_fence_after();
+          qk_issue(0, side_base, side_last);
+          side_pending = false;
+          if (!ws.wait(abort_flag, p->status, kDevTimeoutMma, p->wait_limit)) return false;
+          break;
+        }
+        if (mbar_try_for(b, ph, 100u)) continue;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > p->wait_limit) {
+          atomicCAS(p->status, 0u, kDevTimeoutMma);
+          *abort_flag = 1u;
+          return false;
+        }
+      }
+    } else if (!ws.wait(abort_flag, p->status, kDevTimeoutMma, p->wait_limit)) {
+      return false;
+    }
+    tc_fence_after();
+    return true;
+  }
+  // QK of key tile j of item il (ring position of its K_0: item_base) for `slot`.
+  __device__ bool qk(int slot, int j, int il, uint32_t item_base, bool last) {
+    const uint32_t pos = item_base + 2u * static_cast<uint32_t>(j);
+    WaitSet ws;
+    if (j == 0) ws.add(bar(C::B_QFULL + slot), il & 1);
+    ws.add(bar(C::B_FULL + pos % C::NST), (pos / C::NST) & 1u);
+    if (!wait_all(ws)) return false;
+    qk_issue(slot, pos, last);
     return true;
   }
   // O_slot (+)= P_slot V_j, then release V_j's stage (and signal the epilogue after the
   // slot's last tile of the item).
-  __device__ bool pv(int j, int il, int n_slot) {
+  __device__ bool pv(int slot, int j, int il, int n_slot) {
     const uint32_t pos = base + 2u * static_cast<uint32_t>(j) + 1u;
+    const uint32_t np = slot == 0 ? n_pv0 : n_pv1;
     WaitSet ws;
-    ws.add(bar(C::B_PFULL + slot), n_pv & 1u);
+    ws.add(bar(C::B_PFULL + slot), np & 1u);
     if (j == 0 && il > 0) ws.add(bar(C::B_OFREE + slot), (il - 1) & 1);
     ws.add(bar(C::B_FULL + pos % C::NST), (pos / C::NST) & 1u);
     if (!wait_all(ws)) return false;
     const SDesc b = sdesc_split(sdesc_sw128(ring_s + (pos % C::NST) * C::TILE, C::CHUNK, 1024));
-    const uint32_t o_tmem = tmem + C::O_COL + slot * D;
-    const uint32_t p_tmem = tmem + slot * 128u;
+    const uint32_t o_tmem = tmem + C::O_COL + static_cast<uint32_t>(slot) * D;
+    const uint32_t p_tmem = tmem + static_cast<uint32_t>(slot) * 128u;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       umma_ts_off(o_tmem, p_tmem + kk * 8u, b, kk * 2048, C::IDESC_PV, (j == 0 && kk == 0) ? 0u : 1u);
     umma_commit(bar(C::B_EMPTY + pos % C::NST));
     if (j == n_slot - 1) umma_commit(bar(C::B_OFINAL + slot));
-    ++n_pv;
+    if (slot == 0)
+      ++n_pv0;
+    else
+      ++n_pv1;
     return true;
   }
   __device__ void run(const SchedTable *tbl) {
@@ -160,24 +208,34 @@ struct PPIssuer {
     int r;
     if (!sc.next(r)) return;
     PPItem cur = pp_decode<CAUSAL>(r, *p);
-    if (!qk(0, 0, 0, (slot == 0 ? cur.n0 : cur.n1) == 1)) return;
+    if (!qk(0, 0, 0, 0, cur.n0 == 1) || !qk(1, 0, 0, 0, cur.n1 == 1)) return;
     for (int il = 0;; ++il) {
       Sched peek = sc;
       int rn;
       const bool has_next = peek.next(rn);
       const PPItem nxt = has_next ? pp_decode<CAUSAL>(rn, *p) : cur;
-      const int n = slot == 0 ? cur.n0 : cur.n1;
-      const int n_next = slot == 0 ? nxt.n0 : nxt.n1;
       const uint32_t next_base = base + 2u * static_cast<uint32_t>(cur.n1);
-      for (int j = 0; j < n; ++j) {
-        if (!pv(j, il, n)) return;
-        if (j + 1 < n) {
-          if (!qk(j + 1, il, base, j + 2 == n)) return;
-        } else if (has_next) {
-          if (!qk(0, il + 1, next_base, n_next == 1)) return;
+      for (int j = 0; j < cur.n1; ++j) {
+        if (j < cur.n0) {
+          if (!pv(0, j, il, cur.n0)) return;
+          if (j + 1 < cur.n0) {
+            if (!qk(0, j + 1, il, base, j + 2 == cur.n0)) return;
+          } else if (has_next) {
+            side_pending = true;
+            side_il = il + 1;
+            side_base = next_base;
+            side_last = nxt.n0 == 1;
+          }
         }
+        if (!pv(1, j, il, cur.n1)) return;
+        if (j + 1 < cur.n1 && !qk(1, j + 1, il, base, j + 2 == cur.n1)) return;
       }
       if (!has_next) return;
+      if (side_pending) {
+        side_pending = false;
+        if (!qk(0, 0, il + 1, next_base, nxt.n0 == 1)) return;
+      }
+      if (!qk(1, 0, il + 1, next_base, nxt.n1 == 1)) return;
       sc = peek;
       cur = nxt;
       base = next_base;
@@ -215,8 +273,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(BAR(C::B_PFULL + i), 128);
       mbar_init(BAR(C::B_OFINAL + i), 1);
       mbar_init(BAR(C::B_OFREE + i), 128);
-      mbar_init(BAR(C::B_DRAIN + i), 1);
     }
+    mbar_init(BAR(C::B_DRAIN), 1);
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(BAR(C::B_FULL + i), 1);
       mbar_init(BAR(C::B_EMPTY + i), 2);  // one release per slot
@@ -274,8 +332,8 @@ __global__ void __launch_bounds__(384, 1)
       // Drain: every load issued must have landed before the CTA may exit.
       const uint32_t first = it > static_cast<uint32_t>(C::NST) ? it - C::NST : 0u;
       for (uint32_t i = first; i < it; ++i) wait_drain(BAR(C::B_FULL + (i % C::NST)), (i / C::NST) & 1u, LIM);
-    } else if ((warp == 1 || warp == 2) && lane == 0) {
-      // ---------------------------------------------------------- MMA issuers
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       PPIssuer<D, CAUSAL> is;
       is.p = &p;
       is.ring_s = ring_s;
@@ -283,11 +341,10 @@ __global__ void __launch_bounds__(384, 1)
       is.bar_s = bar_s;
       is.tmem = tmem;
       is.abort_flag = abort_flag;
-      is.slot = warp - 1;
       is.run(&tbl);
       // Drain: all MMAs issued by this thread complete before tensor memory is freed.
-      umma_commit(BAR(C::B_DRAIN + is.slot));
-      wait_drain(BAR(C::B_DRAIN + is.slot), 0, LIM);
+      umma_commit(BAR(C::B_DRAIN));
+      wait_drain(BAR(C::B_DRAIN), 0, LIM);
     } else if (warp == 3 && lane == 0) {
       // ---------------------------------------------------------- Q loads and O stores
       const uint64_t pol_q = policy_evict_first();
