@@ -44,7 +44,6 @@ constexpr unsigned kDevTimeoutEpilogue = 4;
 constexpr unsigned kDevTimeoutProbe = 5;
 
 struct FwdParams {
-  void *o;                 // [BH, L, D] fp16 (written directly by the two-tile kernel)
   float *lse;              // [BH, L] fp32
   unsigned *status;        // device status word (first error code wins)
   long long wait_limit;    // SM clock cycles a single wait may take before it gives up

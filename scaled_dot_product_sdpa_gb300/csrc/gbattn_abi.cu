@@ -312,7 +312,6 @@ extern "C" int attn_fwd_ex(const void *q, const void *k, const void *v, void *o,
   a.causal = causal != 0;
   a.p_smem = p_smem;
   a.stream = static_cast<cudaStream_t>(stream);
-  a.p.o = o;
   a.p.lse = lse;
   a.p.status = di->status;
   a.p.wait_limit = kWaitLimitCycles;
