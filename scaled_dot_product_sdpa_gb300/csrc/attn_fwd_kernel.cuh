@@ -471,6 +471,18 @@ __global__ void __launch_bounds__(256, 1)
     uint32_t g = 0;
     int il = 0, item;
     bool ok = true;
+    // Store issuer (warp 4, lane 0) with two Q buffers: the Q buffer whose O store has not
+    // yet been waited for (-1: none).  Its release waits until the next item's first
+    // softmax tile is done, by when the store has read it, so the softmax never waits for
+    // the store; the producer needs that buffer only for the item after next.
+    int qempty_pending = -1;
+    auto release_pending = [&]() {
+      if (qempty_pending >= 0) {
+        bulk_wait_read0();
+        mbar_arrive(BAR(C::B_QEMPTY + qempty_pending));
+        qempty_pending = -1;
+      }
+    };
     auto wait_warp = [&](uint32_t bar, uint32_t ph) -> bool {
       const bool r = wait_bounded(bar, ph, abort_flag, p.status, kDevTimeoutSoftmax, LIM);
       return __all_sync(0xffffffffu, r);
@@ -519,6 +531,7 @@ __global__ void __launch_bounds__(256, 1)
         if (t > 0 && !rescaled && !(ok = wait_prev_pv())) break;
         tc_fence_before();
         mbar_arrive(BAR(C::B_PFULL + sb));
+        if (t == 0 && warp == 4 && lane == 0) release_pending();
       }
       if (!ok) break;
       // ------------------------------------------------------------- epilogue
@@ -555,14 +568,18 @@ __global__ void __launch_bounds__(256, 1)
           for (int j = 0; j < C::NCHV; ++j)
             tma_store_3d(&tm_o, stage + j * C::CHUNK, half * C::DV + j * 64, qt * C::BM, bh);
           bulk_commit();
-          bulk_wait_read0();
-          mbar_arrive(BAR(C::B_QEMPTY + qb));
+          qempty_pending = qb;
+          // With one Q buffer the next item's Q load needs it back now.
+          if (C::NQB < 2) release_pending();
         }
       }
       __syncwarp();
       ++il;
     }
-    if (warp == 4 && lane == 0) bulk_wait0();
+    if (warp == 4 && lane == 0) {
+      release_pending();
+      bulk_wait0();
+    }
     __syncwarp();
   }
 
