@@ -14,6 +14,10 @@ Definitions followed (cited by page title and section):
 * STAGE_D.md (nvfp4-megamoe-kernel), section 4: the row log-sum-exp (LSE) output;
   section 2: head_dim sub-tiles are additive in logit space (S = S_0 + S_1) and an
   "external merge" of softmax outputs over partial dot products is not the attention.
+* "Validating Memory-Optimal Transformer Kernels on Real Hardware", section 5 ("Paper
+  III: Inference (Decode)"): decoding, one new query row per sequence against the whole
+  cached key/value sequence; ``decode`` computes it by the same definition with every key
+  visible.
 
 Every function takes arrays of shape [B, H, L, d] (anything numpy can view, including
 CPU torch tensors), converts them to float64 (exact for fp16 values) and returns numpy
@@ -59,6 +63,12 @@ def _load():
         lib.oracle_softmax.restype = None
         lib.oracle_pv.argtypes = [dp, dp, dp, i, i, i, i]
         lib.oracle_pv.restype = None
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        lib.oracle_f16_to_f64.argtypes = [u16p, dp, ctypes.c_long]
+        lib.oracle_f16_to_f64.restype = None
+        lib.oracle_decode_f16.argtypes = [u16p, u16p, u16p, dp, dp, ctypes.c_long, ctypes.c_long, i,
+                                          ctypes.c_double, ctypes.POINTER(ctypes.c_int64), ctypes.c_long, i]
+        lib.oracle_decode_f16.restype = i
         _lib = lib
     return _lib
 
@@ -146,3 +156,49 @@ def pv(p, v):
     o = np.empty((B, H, L, d), np.float64)
     _load().oracle_pv(_ptr(p), _ptr(v), _ptr(o), B, H, L, d)
     return o
+
+
+def _u16(x) -> np.ndarray:
+    """Raw fp16 bits of x (a float16 numpy array or a CPU fp16 torch tensor), contiguous."""
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().contiguous().numpy()
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.float16:
+        raise TypeError("decode takes fp16 inputs")
+    return x.view(np.uint16)
+
+
+def f16_to_f64(h) -> np.ndarray:
+    """The oracle's own binary16 -> float64 conversion of raw bits h (uint16 array)."""
+    h = np.ascontiguousarray(np.asarray(h, dtype=np.uint16))
+    out = np.empty(h.shape, np.float64)
+    _load().oracle_f16_to_f64(h.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)), _ptr(out), h.size)
+    return out
+
+
+def decode(q, k, v, scale: float, heads=None, nthreads: int = 0):
+    """Decode by the plain definition: q [B, H, d] (or [B, H, 1, d]), k, v [B, H, L, d], all
+    fp16; every key visible.  Returns (O [n, d], LSE [n]) in float64 for the flat heads
+    (b*H + h) listed in `heads` (default: all B*H heads, in order)."""
+    qu, ku, vu = _u16(q), _u16(k), _u16(v)
+    if ku.ndim != 4 or vu.shape != ku.shape:
+        raise ValueError("k and v must share one [B, H, L, d] shape")
+    B, H, L, d = ku.shape
+    if qu.size != B * H * d:
+        raise ValueError("q must hold one d-vector per (b, h)")
+    BH = B * H
+    if heads is None:
+        hp, n = None, BH
+    else:
+        hs = np.ascontiguousarray(np.asarray(heads, dtype=np.int64))
+        hp, n = hs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), hs.size
+    o = np.empty((n, d), np.float64)
+    lse = np.empty((n,), np.float64)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    rc = _load().oracle_decode_f16(qu.ctypes.data_as(u16p), ku.ctypes.data_as(u16p), vu.ctypes.data_as(u16p),
+                                   _ptr(o), _ptr(lse), BH, L, d, float(scale), hp, n, int(nthreads))
+    if rc == -2:
+        raise IndexError("head index out of range")
+    if rc < 0:
+        raise MemoryError("oracle scratch allocation failed")
+    return o, lse

@@ -30,6 +30,11 @@
  *
  * Layout of every tensor: [B, H, L, d] (or [B, H, L, L] for scores), contiguous, the
  * layout of PyTorch's scaled_dot_product_attention, which the first page gates against.
+ *
+ * Decode ("Validating Memory-Optimal Transformer Kernels on Real Hardware", section 5,
+ * "Paper III: Inference (Decode)": one new token per sequence attends to the whole cached
+ * sequence, at O(n) cost in the sequence length n) is the same definition with a single
+ * query row per (b, h) and every one of the L keys visible; see oracle_decode_f16.
  */
 #include <math.h>
 #include <stdint.h>
@@ -211,4 +216,99 @@ void oracle_pv(const double *p, const double *v, double *o, int B, int H, int L,
                 o[(bh * L + i) * d + c] = acc;
             }
         }
+}
+
+/* IEEE 754 binary16 -> double, from the format's definition: 1 sign bit, 5 exponent bits
+ * (bias 15), 10 fraction bits.  Exponent 0: zero or subnormal, fraction * 2^-24;
+ * exponent 31: infinity (fraction 0) or NaN; otherwise (1024 + fraction) * 2^(e - 25).
+ * Exact: every binary16 value is a double. */
+static double f16_to_f64(uint16_t h)
+{
+    int e = (h >> 10) & 31, f = h & 1023;
+    double mag;
+    if (e == 0)
+        mag = ldexp((double)f, -24);
+    else if (e == 31)
+        mag = f ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(f + 1024), e - 25);
+    return (h >> 15) ? -mag : mag;
+}
+
+/* The conversion above over an array (exported so that it can be checked on its own). */
+void oracle_f16_to_f64(const uint16_t *h, double *out, long n)
+{
+    for (long i = 0; i < n; ++i)
+        out[i] = f16_to_f64(h[i]);
+}
+
+/* Decode: one query row per head bh against all L keys of that head, no mask.
+ * Inputs are raw fp16 bits, q [BH, d] and k, v [BH, L, d], converted element by element
+ * (the full key and value sets of a long sequence are never copied to float64).  For
+ * every head listed in `heads` (n_heads of them; NULL: all BH heads, in order):
+ *     s_j = scale * sum_{t=0}^{d-1} q[bh,t] * k[bh,j,t]        j < L
+ *     m = max_j s_j,   e_j = exp(s_j - m),   l = sum_j e_j
+ *     o[n, c] = (sum_j e_j * v[bh,j,c]) / l,   lse[n] = m + log(l)
+ * with n the position of bh in the list; float64 throughout, sums in ascending order.
+ * Returns the thread count used, -1 if scratch allocation failed, -2 for a head index out
+ * of range. */
+int oracle_decode_f16(const uint16_t *q, const uint16_t *k, const uint16_t *v, double *o,
+                      double *lse, long BH, long L, int d, double scale, const int64_t *heads,
+                      long n_heads, int nthreads)
+{
+    int nt = resolve_threads(nthreads);
+    long n = heads ? n_heads : BH;
+    size_t per = (size_t)(L > 0 ? L : 1) + (size_t)d + (size_t)d;
+    double *scratch = (double *)malloc(sizeof(double) * (size_t)nt * per);
+    if (!scratch)
+        return -1;
+    int bad = 0;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 1) reduction(| : bad)
+    for (long i = 0; i < n; ++i) {
+        int tid = 0;
+#ifdef _OPENMP
+        tid = omp_get_thread_num();
+#endif
+        long bh = heads ? (long)heads[i] : i;
+        if (bh < 0 || bh >= BH) {
+            bad = 1;
+            continue;
+        }
+        double *srow = scratch + (size_t)tid * per;
+        double *qf = srow + (L > 0 ? L : 1);
+        double *acc = qf + d;
+        for (int t = 0; t < d; ++t)
+            qf[t] = f16_to_f64(q[bh * d + t]);
+        /* scores */
+        for (long j = 0; j < L; ++j) {
+            const uint16_t *kj = k + ((size_t)bh * L + j) * d;
+            double dot = 0.0;
+            for (int t = 0; t < d; ++t)
+                dot += qf[t] * f16_to_f64(kj[t]);
+            srow[j] = scale * dot;
+        }
+        /* softmax: max, exp, sum */
+        double m = -INFINITY;
+        for (long j = 0; j < L; ++j)
+            if (srow[j] > m)
+                m = srow[j];
+        double l = 0.0;
+        for (long j = 0; j < L; ++j) {
+            srow[j] = exp(srow[j] - m);
+            l += srow[j];
+        }
+        /* weights times values (key order ascending for every column), then divide */
+        for (int c = 0; c < d; ++c)
+            acc[c] = 0.0;
+        for (long j = 0; j < L; ++j) {
+            const uint16_t *vj = v + ((size_t)bh * L + j) * d;
+            for (int c = 0; c < d; ++c)
+                acc[c] += srow[j] * f16_to_f64(vj[c]);
+        }
+        for (int c = 0; c < d; ++c)
+            o[i * d + c] = acc[c] / l;
+        lse[i] = m + log(l);
+    }
+    free(scratch);
+    return bad ? -2 : nt;
 }

@@ -229,7 +229,8 @@ MUTANTS = {
     "causal_mask_ignored": ("long jmax = causal ? i + 1 : L; /* keys j <= i",
                             "long jmax = L; /* keys j <= i"),
     "lse_without_max": ("*lse_out = m + log(l);", "*lse_out = log(l);"),
-    "exp_sign_flipped": ("srow[j] = exp(srow[j] - m);", "srow[j] = exp(m - srow[j]);"),
+    "exp_sign_flipped": ("srow[j] = exp(srow[j] - m);\n        l += srow[j];",
+                         "srow[j] = exp(m - srow[j]);\n        l += srow[j];"),
     "no_max_subtraction": ("srow[j] = exp(srow[j] - m);\n        l += srow[j];",
                            "srow[j] = exp(srow[j]);\n        l += srow[j];"),
     "missing_divide": ("o_row[c] = acc / l;", "o_row[c] = acc;"),
