@@ -21,6 +21,10 @@ step, the copy of Q, K, V from pinned host memory to the GPU, the forward pass, 
 copy of O and LSE back into pinned host memory, all inside the timed region (the library
 overlaps the copies of one chunk of heads with the kernels of the others).
 
+`per_config` times every forward workload; `decode` times the decode workloads (one
+query row per head against 8192 and 1,048,576 cached keys) and reports them against the
+HBM roofline (K and V are read once).
+
 `cpu_baseline` (rank 0, N=1 only) times the float64 CPU oracle (test infrastructure) on
 the same workload on the host cores; `--impl reference` times that oracle as the
 reference arm.
@@ -302,6 +306,70 @@ def interleaved_per_call(workloads, reps, device, torch, gb, inputs):
     return out
 
 
+def bench_decode(device, torch, gb, inputs, hbm_peak, only=None):
+    """Decode workloads (one query row per head against a long key/value sequence): mean
+    time per call over 30 graph-replayed calls, CUDA events on the replay stream; K and V
+    (1.1 and 4.3 GB) are far larger than L2, so every call reads them from HBM."""
+    from scaled_dot_product_sdpa_gb300.configs import DECODE_WORKLOADS
+    sm_count = torch.cuda.get_device_properties(device).multi_processor_count
+    out = {}
+    for name, w in DECODE_WORKLOADS.items():
+        if only is not None and name != only:
+            continue
+        q, k, v = inputs.decode_qkv(w.B, w.H, w.L, w.d, w.seed, w.sigma, device=device, draw_on_device=True)
+        o = torch.empty(w.B, w.H, w.d, dtype=torch.float16, device=device)
+        lse = torch.empty(w.B, w.H, dtype=torch.float32, device=device)
+        stream = torch.cuda.Stream(device)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                gb.attn_decode(q, k, v, scale=w.scale, o=o, lse=lse, stream=stream)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(10):
+                    gb.attn_decode(q, k, v, scale=w.scale, o=o, lse=lse, stream=stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):  # replay() launches on the current stream
+            g.replay()
+            stream.synchronize()
+            a.record(stream)
+            for _ in range(3):
+                g.replay()
+            b.record(stream)
+        b.synchronize()
+        t = a.elapsed_time(b) * 1e-3 / 30
+        plan = gb.attn_debug_decode_plan(w.B, w.H, w.L, w.d, sm_count)
+        gbs = w.bytes() / t / 1e9
+        out[name] = {"shape": w.describe(), "kernel": "attn_decode_kernel", "us": round(t * 1e6, 2),
+                     "hbm_gbs": round(gbs, 1), "pct_hbm_peak": round(100 * gbs / hbm_peak, 2),
+                     "tflops": round(w.flops() / t / 1e12, 2), "ctas_per_head": plan["ranks"],
+                     "keys_per_cta": plan["keys_per_rank"]}
+        del q, k, v, g
+        torch.cuda.empty_cache()
+    return out
+
+
+def decode_only(name):
+    """`--decode NAME`: the decode timing of one workload alone, as a JSON line."""
+    import torch
+    import scaled_dot_product_sdpa_gb300 as gb
+    from scaled_dot_product_sdpa_gb300 import build as gbuild
+    from scaled_dot_product_sdpa_gb300 import inputs
+    from scaled_dot_product_sdpa_gb300.configs import DECODE_WORKLOADS
+    if name not in DECODE_WORKLOADS:
+        raise SystemExit(f"unknown decode workload {name!r}; known: {sorted(DECODE_WORKLOADS)}")
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    gb.load_library(gbuild.build())
+    peaks, _ = load_peaks()
+    res = bench_decode(device, torch, gb, inputs, peaks["hbm_gbs"], only=name)
+    status = gb.attn_last_device_error()
+    if status != 0:
+        raise RuntimeError(f"device status {status}: {gb.attn_strerror(status)}")
+    print(json.dumps({"decode": res}), flush=True)
+
+
 def cpu_oracle_baseline(w, min_seconds=10.0, max_reps=20):
     """Float64 oracle, as it stands, on the host cores: whole workload, repeated until
     about `min_seconds` of CPU work (bounded by max_reps)."""
@@ -437,6 +505,7 @@ def bench_ours(args):
         line["per_config_timing"] = ("us: mean of 200 graph-replayed calls over rotating input sets; "
                                      "per_call_*: 300 single calls interleaved across the configs, CUDA events "
                                      "around each call behind a GPU-side sleep")
+        line["decode"] = bench_decode(device, torch, gb, inputs, hbm_peak)
         status = gb.attn_last_device_error()
         if status != 0:
             raise RuntimeError(f"device status {status}: {gb.attn_strerror(status)}")
@@ -510,10 +579,13 @@ def main(argv=None):
     ap.add_argument("--workload", default="caseD")
     ap.add_argument("--quick", action="store_true", help="timed region only (for profiler runs)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--decode", metavar="NAME", help="time only this decode workload (diagnostic; for profiler runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.decode:
+        decode_only(args.decode)
+    elif args.impl == "reference":
         bench_reference(args)
     else:
         bench_ours(args)

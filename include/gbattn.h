@@ -54,6 +54,7 @@ extern "C" {
 #define GBATTN_DEV_TIMEOUT_SOFTMAX 3 /* the softmax warps' wait for S or O timed out         */
 #define GBATTN_DEV_TIMEOUT_EPILOGUE 4 /* the epilogue's wait for its staging tile timed out   */
 #define GBATTN_DEV_TIMEOUT_PROBE 5   /* the self-test wait of attn_debug_wait_probe ran out */
+#define GBATTN_DEV_TIMEOUT_MERGE 6   /* attn_decode: waiting for the other CTAs' partials ran out */
 
 /*
  * attn_fwd -- the fused forward pass.
@@ -120,6 +121,34 @@ int attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *l
 
 /* Device workspace bytes attn_fwd_host needs for this shape (0 for invalid arguments). */
 size_t attn_fwd_host_workspace_size(int B, int H, int L, int d);
+
+/*
+ * attn_decode -- decoding: one query row per (b, h) against all L cached keys, every key
+ * visible ("Validating Memory-Optimal Transformer Kernels on Real Hardware", section 5,
+ * "Paper III: Inference (Decode)"):
+ *     o[b,h,:] = sum_j softmax_j(scale * q[b,h] . k[b,h,j]) v[b,h,j,:]
+ *     lse[b,h] = log sum_j exp(scale * q[b,h] . k[b,h,j])                (natural log)
+ *   q       : const fp16 [B, H, d] (the [B, H, 1, d] query), device, 16-byte aligned.
+ *   k, v    : const fp16 [B, H, L, d], device, 16-byte aligned.
+ *   o       : fp16 [B, H, d] output;  lse : fp32 [B, H] output.
+ *   B, H, L : > 0.  d : 64, 128, 256 or 512.  scale : finite and > 0.
+ * Ownership, stream, return values and errors as for attn_fwd.  Each head's keys are
+ * split over the CTAs of one thread-block cluster (up to 16), which merge their partial
+ * results in distributed shared memory: no global scratch memory is used.  The work is
+ * bound by the HBM reads of K and V (when B * H is below about ten, the clusters cannot
+ * occupy every SM).
+ */
+int attn_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int L, int d,
+                float scale, void *stream);
+
+/*
+ * attn_debug_decode_plan -- test hook (host-only): the split attn_decode uses for this
+ * shape on a GPU with `sm_count` SMs whose clusters hold at most `max_ranks` CTAs (1..16):
+ * out[0] = CTAs per head (a power of two; at most 16, 8, 4 for d <= 128, 256, 512),
+ * out[1] = keys per CTA (whole key tiles of 8192 / d keys).  Returns 0 or a negative
+ * GBATTN_ERR_* code.
+ */
+int attn_debug_decode_plan(int B, int H, int L, int d, int sm_count, int max_ranks, int *out);
 
 /*
  * attn_debug_scores -- test hook: the raw scaled logits s[b,h,i,j] = scale * q_i . k_j

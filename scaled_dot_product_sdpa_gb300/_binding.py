@@ -61,6 +61,10 @@ def load_library(path: str | None = None):
     lib.attn_fwd_host_workspace_size.restype = sz
     lib.attn_debug_plan.argtypes = [i, i, i, i, i, i, i, i, ip]
     lib.attn_debug_plan.restype = i
+    lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, vp]
+    lib.attn_decode.restype = i
+    lib.attn_debug_decode_plan.argtypes = [i, i, i, i, i, i, ip]
+    lib.attn_debug_decode_plan.restype = i
     lib.attn_version.argtypes = []
     lib.attn_version.restype = i
     _lib = lib
@@ -118,6 +122,48 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, 
     if rc != 0:
         raise GbattnError(rc, "attn_fwd")
     return o, lse
+
+
+def attn_decode(q, k, v, scale: float | None = None, o=None, lse=None, stream=None):
+    """Decode: O [B, H, d] and LSE [B, H] for one fp16 query row q ([B, H, d] or
+    [B, H, 1, d]) per head against fp16 k, v [B, H, L, d], every key visible.  Outputs are
+    allocated by torch on q's device unless given.  Enqueued on `stream`."""
+    for t in (q, k, v):
+        if not t.is_cuda:
+            raise ValueError("gbattn: tensors must be on a CUDA device (no CPU path exists)")
+        if t.dtype != torch.float16 or not t.is_contiguous():
+            raise ValueError("gbattn: q, k, v must be contiguous float16")
+    if k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("gbattn: k and v must share one [B, H, L, d] shape")
+    B, H, L, d = k.shape
+    if tuple(q.shape) not in ((B, H, d), (B, H, 1, d)):
+        raise ValueError("gbattn: q must be [B, H, d] or [B, H, 1, d]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty((B, H, d), dtype=torch.float16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if o.numel() != B * H * d or o.dtype != torch.float16 or not o.is_contiguous():
+        raise ValueError("gbattn: o must be contiguous float16 with B*H*d elements")
+    if lse.numel() != B * H or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("gbattn: lse must be contiguous float32 [B, H]")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, L, d,
+                             float(scale), _stream_handle(stream))
+    if rc != 0:
+        raise GbattnError(rc, "attn_decode")
+    return o, lse
+
+
+def attn_debug_decode_plan(B: int, H: int, L: int, d: int, sm_count: int, max_ranks: int = 16) -> dict:
+    """The split attn_decode uses (host-only): CTAs per head and keys per CTA."""
+    out = (ctypes.c_int * 2)()
+    rc = load_library().attn_debug_decode_plan(B, H, L, d, sm_count, max_ranks, out)
+    if rc != 0:
+        raise GbattnError(rc, "attn_debug_decode_plan")
+    return {"ranks": out[0], "keys_per_rank": out[1]}
 
 
 def attn_debug_scores(q, k, scale: float | None = None, s=None, stream=None):

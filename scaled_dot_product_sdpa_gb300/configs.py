@@ -50,3 +50,42 @@ WORKLOADS = {
     "caseD": Workload("caseD", 8, 32, 512, 128, True, 4),
     "hd512": Workload("hd512", 1, 8, 2048, 512, True, 5, 0.5),
 }
+
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """Decoding: one query row per (b, h) against L cached keys, every key visible
+    ("Validating Memory-Optimal Transformer Kernels on Real Hardware", section 5, "Paper
+    III: Inference (Decode)"; the pages scale the sequence length from 1,024 to 1,048,576
+    and give no batch, head or head_dim sizes)."""
+    name: str
+    B: int
+    H: int
+    L: int
+    d: int
+    seed: int
+    sigma: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def flops(self) -> float:
+        """Algorithmic FLOPs: 4*B*H*L*d (q.K^T and p.V, 2*L*d each per head)."""
+        return 4.0 * self.B * self.H * self.L * self.d
+
+    def bytes(self) -> int:
+        """Algorithmic HBM bytes: read K, V (and q) once, write o (2 B each) and LSE (4 B)."""
+        bh = self.B * self.H
+        return 2 * bh * self.d * (2 * self.L + 2) + 4 * bh
+
+    def describe(self) -> str:
+        return f"decode B={self.B} H={self.H} L={self.L} d={self.d} seed={self.seed} sigma={self.sigma}"
+
+
+# A batched decode step (B x H = 256 sequences of 8192 cached tokens, 1.07 GB of K and V)
+# and the pages' longest sequence, 1,048,576 tokens, for 8 heads (4.3 GB of K and V).
+DECODE_WORKLOADS = {
+    "decB": DecodeWorkload("decB", 8, 32, 8192, 128, 6),
+    "dec1M": DecodeWorkload("dec1M", 1, 8, 1048576, 128, 7),
+}

@@ -15,6 +15,7 @@
 #include <queue>
 #include <vector>
 
+#include "attn_decode.cuh"
 #include "attn_fwd_kernel.cuh"
 #include "attn_fwd_pp.cuh"
 #include "gbattn.h"
@@ -38,6 +39,7 @@ struct DevInfo {
   bool init = false;
   int cc_major = 0, cc_minor = 0, sm_count = 0;
   unsigned *status = nullptr;
+  int dec_max_ranks[4] = {0, 0, 0, 0};  // decode cluster size limit per head_dim (0: not yet asked)
 };
 DevInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -81,13 +83,13 @@ int device_info(DevInfo **out) {
 }
 
 // [BH, L, D] fp16 viewed as a 3-D tensor (D innermost); box = 64 columns (128 B, the
-// swizzle span) x 128 rows x 1 head.  Rows past L read as zero and are never written.
-int encode_bhld(CUtensorMap *tm, const void *ptr, int BH, int L, int D) {
+// swizzle span) x box_rows rows x 1 head.  Rows past L read as zero and are never written.
+int encode_bhld(CUtensorMap *tm, const void *ptr, int BH, int L, int D, int box_rows = 128) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2u,
                                  static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(D) * 2u};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estride[3] = {1, 1, 1};
   const CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
                               estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -268,6 +270,22 @@ int check_shape(int B, int H, int L, int d) {
   if (d != 64 && d != 128 && d != 256 && d != 512) return GBATTN_ERR_HEAD_DIM;
   return GBATTN_OK;
 }
+
+// Decode launch plan: the CTAs per head (one cluster, a power of two) and the keys each
+// one streams (whole key tiles).  Enough CTAs for two waves of two CTAs per SM, at most
+// max_ranks (and the head_dim's own bound), and at least one key tile per CTA.
+void decode_plan(long long BH, int L, int d, int sm_count, int max_ranks, int &ranks, int &keys_per_rank) {
+  max_ranks = std::min(max_ranks, dec_max_ranks_for(d));
+  const int kt = dec_key_tile(d);
+  const long long tiles = (static_cast<long long>(L) + kt - 1) / kt;
+  const long long want = (4LL * sm_count + BH - 1) / BH;
+  int r = 1;
+  while (r < want && 2 * r <= max_ranks && 2 * r <= tiles) r *= 2;
+  ranks = r;
+  keys_per_rank = static_cast<int>((tiles + r - 1) / r) * kt;
+}
+
+int dec_dim_index(int d) { return d == 64 ? 0 : d == 128 ? 1 : d == 256 ? 2 : 3; }
 
 }  // namespace
 }  // namespace gbattn
@@ -478,6 +496,61 @@ extern "C" int attn_fwd_host(const void *q, const void *k, const void *v, void *
   return GBATTN_OK;
 }
 
+extern "C" int attn_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int L,
+                           int d, float scale, void *stream) {
+  if (!q || !k || !v || !o || !lse) return GBATTN_ERR_NULL;
+  int rc = check_shape(B, H, L, d);
+  if (rc != GBATTN_OK) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return GBATTN_ERR_ALIGN;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return GBATTN_ERR_SCALE;
+  const long long BH = static_cast<long long>(B) * H;
+  const size_t qbytes = static_cast<size_t>(BH) * d * 2u, kvbytes = qbytes * static_cast<size_t>(L),
+               lbytes = static_cast<size_t>(BH) * 4u;
+  if (overlaps(o, qbytes, q, qbytes) || overlaps(o, qbytes, k, kvbytes) || overlaps(o, qbytes, v, kvbytes) ||
+      overlaps(lse, lbytes, q, qbytes) || overlaps(lse, lbytes, k, kvbytes) || overlaps(lse, lbytes, v, kvbytes) ||
+      overlaps(lse, lbytes, o, qbytes))
+    return GBATTN_ERR_ALIAS;
+  DevInfo *di = nullptr;
+  if ((rc = device_info(&di)) != GBATTN_OK) return rc;
+  int &max_ranks = di->dec_max_ranks[dec_dim_index(d)];
+  if (max_ranks == 0) {
+    const int mr = decode_max_ranks(d);
+    if (mr <= 0) return GBATTN_ERR_LAUNCH;
+    max_ranks = mr;
+  }
+  DecLaunch a;
+  const int kt = dec_key_tile(d);
+  if (encode_bhld(&a.tm_k, k, static_cast<int>(BH), L, d, kt) || encode_bhld(&a.tm_v, v, static_cast<int>(BH), L, d, kt))
+    return GBATTN_ERR_TENSORMAP;
+  decode_plan(BH, L, d, di->sm_count, max_ranks, a.p.ranks, a.p.keys_per_rank);
+  a.p.q = q;
+  a.p.o = o;
+  a.p.lse = lse;
+  a.p.status = di->status;
+  a.p.wait_limit = kWaitLimitCycles;
+  a.p.BH = static_cast<int>(BH);
+  a.p.L = L;
+  a.p.c2 = scale * 1.4426950408889634f;
+  a.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (d) {
+    case 64: e = launch_decode_64(a); break;
+    case 128: e = launch_decode_128(a); break;
+    case 256: e = launch_decode_256(a); break;
+    default: e = launch_decode_512(a); break;
+  }
+  return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_LAUNCH;
+}
+
+extern "C" int attn_debug_decode_plan(int B, int H, int L, int d, int sm_count, int max_ranks, int *out) {
+  if (!out) return GBATTN_ERR_NULL;
+  const int rc = check_shape(B, H, L, d);
+  if (rc != GBATTN_OK) return rc;
+  if (sm_count <= 0 || max_ranks < 1 || max_ranks > kDecMaxRanks) return GBATTN_ERR_DIMS;
+  decode_plan(static_cast<long long>(B) * H, L, d, sm_count, max_ranks, out[0], out[1]);
+  return GBATTN_OK;
+}
+
 extern "C" int attn_debug_scores(const void *q, const void *k, float *s, int B, int H, int L, int d, float scale,
                                  void *stream) {
   if (!q || !k || !s) return GBATTN_ERR_NULL;
@@ -541,6 +614,7 @@ extern "C" const char *attn_strerror(int code) {
     case GBATTN_DEV_TIMEOUT_SOFTMAX: return "device: a softmax warp's wait timed out";
     case GBATTN_DEV_TIMEOUT_EPILOGUE: return "device: the epilogue's wait timed out";
     case GBATTN_DEV_TIMEOUT_PROBE: return "device: the wait-probe barrier timed out (expected)";
+    case GBATTN_DEV_TIMEOUT_MERGE: return "device: decode's wait for the other CTAs' partial results timed out";
     default: return "unknown gbattn status code";
   }
 }

@@ -154,3 +154,33 @@ def test_host_workspace_size(lib):
     # q, k, v, o (4 x 8 MiB) and lse (128 KiB).
     assert lib.attn_fwd_host_workspace_size(8, 32, 512, 128) == 2 * (4 * 64 * 512 * 128 * 2 + 64 * 512 * 4)
     assert lib.attn_fwd_host_workspace_size(1, 1, 0, 64) == 0
+
+
+def _dec(lib, q=Q, k=K, v=V, o=O, lse=LSE, B=1, H=2, L=128, d=64, scale=0.125):
+    return lib.attn_decode(q, k, v, o, lse, B, H, L, d, scale, None)
+
+
+def test_decode_validation(lib):
+    c = _codes()
+    for kw in ("q", "k", "v", "o", "lse"):
+        assert _dec(lib, **{kw: 0}) == c["GBATTN_ERR_NULL"]
+    for B, H, L in [(0, 1, 1), (1, 0, 1), (1, 1, 0), (1 << 16, 1 << 16, 1)]:
+        assert _dec(lib, B=B, H=H, L=L) == c["GBATTN_ERR_DIMS"]
+    for d in (0, 32, 96, 1024):
+        assert _dec(lib, d=d) == c["GBATTN_ERR_HEAD_DIM"]
+    for kw in ("q", "k", "v", "o", "lse"):
+        base = {"q": Q, "k": K, "v": V, "o": O, "lse": LSE}[kw]
+        assert _dec(lib, **{kw: base + 8}) == c["GBATTN_ERR_ALIGN"]
+    for scale in (0.0, -1.0, float("inf"), float("nan")):
+        assert _dec(lib, scale=scale) == c["GBATTN_ERR_SCALE"]
+    assert _dec(lib, o=Q) == c["GBATTN_ERR_ALIAS"]
+    assert _dec(lib, o=K + 1024) == c["GBATTN_ERR_ALIAS"]      # inside k
+    assert _dec(lib, lse=O + 64) == c["GBATTN_ERR_ALIAS"]      # inside o (2*64*2 bytes)
+    assert _dec(lib, lse=V) == c["GBATTN_ERR_ALIAS"]
+
+
+def test_decode_without_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; the fake addresses must never reach a launch")
+    assert _dec(lib) in (_codes()["GBATTN_ERR_LAUNCH"], _codes()["GBATTN_ERR_DEVICE"])
