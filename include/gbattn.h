@@ -86,12 +86,21 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
  *   flags bit 1 (GBATTN_FLAG_SINGLE_TILE): single-tile kernel, P in tensor memory.
  *   flags bit 2 (GBATTN_FLAG_TWO_TILE): two-tile kernel whatever the item count; only for
  *     d <= 128 (else GBATTN_ERR_HEAD_DIM) and not with bits 0 or 1 (GBATTN_ERR_FLAGS).
+ *   flags bit 3 (GBATTN_FLAG_DSPLIT): the single-tile kernel with head_dim split over the
+ *     two CTAs of a thread-block cluster: each CTA computes the logits over half of
+ *     head_dim, the two exchange their partial S tiles through distributed shared memory,
+ *     and each produces half of O, so no QK product is computed twice (without it each of
+ *     the two value halves of a d = 512 tile recomputes the full QK product).  Only for
+ *     d = 512 (else GBATTN_ERR_HEAD_DIM) and alone (else GBATTN_ERR_FLAGS).  Slower on
+ *     GB300: moving a 64 KB partial S tile between SMs takes longer than the QK work it
+ *     saves.
  *   grid_limit: 0 = one persistent CTA per SM; n > 0 = at most n CTAs (scheduler tests).
  * Every option gives the same results up to rounding.
  */
 #define GBATTN_FLAG_P_SMEM 1
 #define GBATTN_FLAG_SINGLE_TILE 2
 #define GBATTN_FLAG_TWO_TILE 4
+#define GBATTN_FLAG_DSPLIT 8
 int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                 int H, int L, int d, int causal, float scale, void *stream, int flags,
                 int grid_limit);
@@ -179,7 +188,8 @@ int attn_debug_wait_probe(long long limit_cycles, void *stream);
 
 /*
  * attn_debug_schedule -- test hook: the static work schedule attn_fwd_ex would use for
- * this shape, `grid` CTAs and `flags`.  Returns the number of work items n and fills
+ * this shape, `grid` CTAs (clusters of two CTAs with GBATTN_FLAG_DSPLIT) and `flags`.
+ * Returns the number of work items n and fills
  * start[0..grid] (CTA c runs items[start[c] .. start[c+1]) in order) and items[0..n), or
  * returns 0 when the problem is too large for a table (the kernels then use a fixed
  * snake order), or a negative GBATTN_ERR_* code (GBATTN_ERR_DIMS if n > max_items).
@@ -191,7 +201,8 @@ int attn_debug_schedule(int B, int H, int L, int d, int causal, int grid, int fl
 /*
  * attn_debug_plan -- test hook: the kernel attn_fwd_ex would launch for this shape,
  * `flags` and `grid_limit` on a GPU with `sm_count` SMs (host-only; needs no GPU).
- * Fills out[0] = kernel (0 single-tile, 1 two-tile), out[1] = work items, out[2] = CTAs,
+ * Fills out[0] = kernel (0 single-tile, 1 two-tile, 2 single-tile with the head_dim split),
+ * out[1] = work items, out[2] = CTAs (clusters of two CTAs for kernel 2),
  * out[3] = estimated makespan x 100 (in units of one tile step of a query tile in the
  * two-tile kernel; -100 when the kernels use their fixed order).
  * Returns 0 or a negative GBATTN_ERR_* code.

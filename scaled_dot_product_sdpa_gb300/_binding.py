@@ -20,6 +20,7 @@ _lib = None
 FLAG_P_SMEM = 1
 FLAG_SINGLE_TILE = 2
 FLAG_TWO_TILE = 4
+FLAG_DSPLIT = 8
 
 
 class GbattnError(RuntimeError):

@@ -52,15 +52,17 @@ struct FwdParams {
   float c2;                // scale * log2(e)
 };
 
-template <int D, bool P_TMEM>
+template <int D, bool P_TMEM, bool DSPLIT = false>
 struct FwdCfg {
   static constexpr int BM = 128, BN = 128;
   static constexpr int DVS = D > 256 ? D / 256 : 1;  // value-column splits per (bh, qt)
   static constexpr int DV = D / DVS;                 // O columns owned by one item
   static constexpr int NCH = D / 64;                 // 64-column chunks of a Q / K tile
+  // head_dim split over a CTA pair: each CTA holds half of Q and of every K tile
+  static constexpr int QCH = DSPLIT ? NCH / 2 : NCH;  // chunks of Q (and of each K tile) held
   static constexpr int NCHV = DV / 64;               // 64-column chunks of an item's V tile
   static constexpr int SC = D == 64 ? 1 : 2;         // chunks per ring stage
-  static constexpr int KST = NCH / SC;               // ring stages per K tile
+  static constexpr int KST = QCH / SC;               // ring stages per K tile (this CTA's chunks)
   static constexpr int VST = NCHV / SC;              // ring stages per V tile
   static constexpr int NQB = D <= 128 ? 2 : 1;       // Q buffers (also the O staging tiles)
   static constexpr bool LOOKAHEAD = NQB >= 2;        // next item's QKs before its last PVs
@@ -72,18 +74,24 @@ struct FwdCfg {
   static constexpr int NSB = 2;
   static constexpr int CHUNK = 128 * 128;            // bytes of a 128-row x 64-col fp16 box
   static constexpr int STAGE = SC * CHUNK;
-  static constexpr int QBYTES = NCH * CHUNK;
+  static constexpr int QBYTES = QCH * CHUNK;
+  // head_dim split: the peer's partial S tile (128 x 128 fp32), 16-byte chunks of each
+  // 512-byte row XOR-swizzled by row & 7
+  static constexpr int RBYTES = DSPLIT ? 128 * 128 * 4 : 0;
   static constexpr int NPB = P_TMEM ? 0 : 2;         // shared-memory P buffers
   static constexpr int PBYTES = 2 * CHUNK;           // 128 x 128 fp16
   static constexpr int TILE_BUDGET = 224 * 1024;
-  static constexpr int NST_FIT = (TILE_BUDGET - NQB * QBYTES - NPB * PBYTES) / STAGE;
+  static constexpr int NST_FIT = (TILE_BUDGET - NQB * QBYTES - NPB * PBYTES - RBYTES) / STAGE;
   static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
   // barrier indices
   static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_FULL = 4, B_EMPTY = 4 + NST;
   static constexpr int B_SFULL = 4 + 2 * NST, B_PFULL = B_SFULL + NSB, B_ODONE = B_PFULL + NSB;
   static constexpr int B_OFREE = B_ODONE + 1, B_EPI = B_OFREE + 1, B_DRAIN = B_EPI + 1;
-  static constexpr int NBAR = B_DRAIN + 1;
-  static constexpr int TILE_BYTES = NQB * QBYTES + NPB * PBYTES + NST * STAGE;
+  // head_dim split: RECV completes when the peer's partial S is in this CTA's buffer,
+  // RFREE when the peer has read this CTA's partial out of its own buffer
+  static constexpr int B_RECV = B_DRAIN + 1, B_RFREE = B_RECV + 1;
+  static constexpr int NBAR = B_RFREE + 1;
+  static constexpr int TILE_BYTES = NQB * QBYTES + NPB * PBYTES + RBYTES + NST * STAGE;
   static constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + TILE_BYTES + 8 * NBAR + 16;
   // tensor memory columns: S buffer b at [128 b, 128 b + 128), O after the S buffers
   static constexpr int O_COL = 128 * NSB;
@@ -93,7 +101,8 @@ struct FwdCfg {
   static_assert(NST >= 2, "ring too shallow");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(O_COL + DV <= TMEM_COLS, "tensor memory budget");
-  static_assert(NCH % SC == 0 && NCHV % SC == 0, "stage split");
+  static_assert(QCH % SC == 0 && NCHV % SC == 0, "stage split");
+  static_assert(!DSPLIT || (D == 512 && P_TMEM), "head_dim split: D = 512, P in tensor memory");
 };
 
 // Static schedule.  With a table (n > 0), CTA c processes items[start[c] .. start[c+1]):
@@ -156,6 +165,22 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
   const long long t0 = clock64();
   while (true) {
     if (mbar_try(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      atomicCAS(status, 0u, code);
+      *abort_flag = 1u;
+      return false;
+    }
+  }
+}
+// Same, for a barrier that another CTA of the cluster arrives on (acquire at cluster
+// scope, so that what it wrote into this CTA's shared memory before arriving is visible).
+__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                                     unsigned *status, unsigned code, long long limit) {
+  if (mbar_try_acquire_cluster(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_acquire_cluster(bar, parity)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > limit) {
       atomicCAS(status, 0u, code);
@@ -263,12 +288,12 @@ struct PvQueue {
   __device__ const PendingPv &front() const { return head == 0 ? e[0] : e[CAP - 1]; }
 };
 
-template <int D, bool CAUSAL, bool P_TMEM>
+template <int D, bool CAUSAL, bool P_TMEM, bool DSPLIT>
 __global__ void __launch_bounds__(256, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     const FwdParams p, const __grid_constant__ SchedTable tbl) {
-  using C = FwdCfg<D, P_TMEM>;
+  using C = FwdCfg<D, P_TMEM, DSPLIT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -278,14 +303,25 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t ring_s = base;                             // NST x STAGE
   const uint32_t q_s = ring_s + C::NST * C::STAGE;          // NQB x QBYTES
   const uint32_t p_s = q_s + C::NQB * C::QBYTES;            // NPB x PBYTES
-  const uint32_t bar_s = p_s + C::NPB * C::PBYTES;          // NBAR x 8
+  const uint32_t recv_s = p_s + C::NPB * C::PBYTES;         // RBYTES (head_dim split)
+  const uint32_t bar_s = recv_s + C::RBYTES;                // NBAR x 8
   uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + (bar_s - base) + 8 * C::NBAR);
   volatile uint32_t *const abort_flag = tmem_slot + 1;
   auto BAR = [&](int i) -> uint32_t { return bar_s + 8u * static_cast<uint32_t>(i); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // head_dim split: the two CTAs of a cluster share every work item; rank r holds Q / K
+  // columns [r * D/2, (r + 1) * D/2) and computes the value columns of half r.
+  const uint32_t rank = DSPLIT ? cluster_ctarank() : 0u;
+  const int qc0 = static_cast<int>(rank) * C::QCH;  // first 64-column chunk of Q / K held
+  const int sched_id = DSPLIT ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int sched_n = DSPLIT ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
+    if (DSPLIT) {
+      mbar_init(BAR(C::B_RECV), 128);   // the peer's 128 softmax threads
+      mbar_init(BAR(C::B_RFREE), 128);
+    }
     for (int i = 0; i < C::NQB; ++i) {
       mbar_init(BAR(C::B_QFULL + i), 1);
       mbar_init(BAR(C::B_QEMPTY + i), 1);
@@ -317,6 +353,9 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Both CTAs of a pair have initialised their barriers before either arrives on the
+  // other's (every thread reaches this, unconditionally).
+  if constexpr (DSPLIT) cluster_sync_all();
   // The prologue above touches no global memory: the next kernel may launch now, and this
   // one waits here for the previous kernel's writes (inputs may be its outputs).
   grid_launch_dependents();
@@ -326,7 +365,7 @@ __global__ void __launch_bounds__(256, 1)
   if (warp == 0) {
     // =============================================================== TMA producer
     if (lane == 0) {
-      Sched sc(blockIdx.x, gridDim.x, p.n_items, &tbl);
+      Sched sc(sched_id, sched_n, p.n_items, &tbl);
       uint32_t it = 0;
       int il = 0, item;
       bool ok = true;
@@ -352,7 +391,8 @@ __global__ void __launch_bounds__(256, 1)
       uint32_t g = 0;
       while (ok && sc.next(item)) {
         int bh, qt, half, n;
-        decode_item<C::DVS, CAUSAL>(item, p, bh, qt, half, n);
+        decode_item<DSPLIT ? 1 : C::DVS, CAUSAL>(item, p, bh, qt, half, n);
+        if (DSPLIT) half = static_cast<int>(rank);
         while (ok && pq.size > 0 && pq.front().il < il - (C::LOOKAHEAD ? 1 : 0)) ok = load_v(pq.pop());
         if (!ok) break;
         const int qb = il % C::NQB;
@@ -360,10 +400,11 @@ __global__ void __launch_bounds__(256, 1)
         if (!(ok = wait_bounded(BAR(C::B_QEMPTY + qb), qph ^ 1u, abort_flag, p.status, kDevTimeoutLoad, LIM)))
           break;
         mbar_arrive_expect_tx(BAR(C::B_QFULL + qb), C::QBYTES);
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_3d(q_s + qb * C::QBYTES + c * C::CHUNK, &tm_q, c * 64, qt * C::BM, bh, BAR(C::B_QFULL + qb));
+        for (int c = 0; c < C::QCH; ++c)
+          tma_load_3d(q_s + qb * C::QBYTES + c * C::CHUNK, &tm_q, (qc0 + c) * 64, qt * C::BM, bh,
+                      BAR(C::B_QFULL + qb));
         for (int t = 0; t < n && ok; ++t, ++g) {
-          for (int ks = 0; ks < C::KST && ok; ++ks) ok = load_stage(&tm_k, ks * C::SC, t * C::BN, bh);
+          for (int ks = 0; ks < C::KST && ok; ++ks) ok = load_stage(&tm_k, qc0 + ks * C::SC, t * C::BN, bh);
           if (ok && pq.size == C::NSB - 1) ok = load_v(pq.pop());
           pq.push(PendingPv{g, il, t, n, bh, half});
         }
@@ -381,7 +422,7 @@ __global__ void __launch_bounds__(256, 1)
   } else if (warp == 1) {
     // =============================================================== MMA issuer
     if (lane == 0) {
-      Sched sc(blockIdx.x, gridDim.x, p.n_items, &tbl);
+      Sched sc(sched_id, sched_n, p.n_items, &tbl);
       uint32_t it = 0, g = 0;
       int il = 0, item;
       bool ok = true;
@@ -442,7 +483,8 @@ __global__ void __launch_bounds__(256, 1)
       PvQueue<C::NSB> pq;
       while (ok && sc.next(item)) {
         int bh, qt, half, n;
-        decode_item<C::DVS, CAUSAL>(item, p, bh, qt, half, n);
+        decode_item<DSPLIT ? 1 : C::DVS, CAUSAL>(item, p, bh, qt, half, n);
+        if (DSPLIT) half = static_cast<int>(rank);
         while (ok && pq.size > 0 && pq.front().il < il - (C::LOOKAHEAD ? 1 : 0)) ok = issue_pv(pq.pop());
         if (!ok) break;
         const int qb = il % C::NQB;
@@ -467,7 +509,7 @@ __global__ void __launch_bounds__(256, 1)
     const int row = quarter * 32 + lane;  // query row within the tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const float c2 = p.c2;
-    Sched sc(blockIdx.x, gridDim.x, p.n_items, &tbl);
+    Sched sc(sched_id, sched_n, p.n_items, &tbl);
     uint32_t g = 0;
     int il = 0, item;
     bool ok = true;
@@ -487,9 +529,14 @@ __global__ void __launch_bounds__(256, 1)
       const bool r = wait_bounded(bar, ph, abort_flag, p.status, kDevTimeoutSoftmax, LIM);
       return __all_sync(0xffffffffu, r);
     };
+    auto wait_warp_cluster = [&](uint32_t bar, uint32_t ph) -> bool {
+      const bool r = wait_bounded_cluster(bar, ph, abort_flag, p.status, kDevTimeoutSoftmax, LIM);
+      return __all_sync(0xffffffffu, r);
+    };
     while (ok && sc.next(item)) {
       int bh, qt, half, n;
-      decode_item<C::DVS, CAUSAL>(item, p, bh, qt, half, n);
+      decode_item<DSPLIT ? 1 : C::DVS, CAUSAL>(item, p, bh, qt, half, n);
+      if (DSPLIT) half = static_cast<int>(rank);
       float m_used = 0.f, l = 0.f;
       for (int t = 0; t < n; ++t, ++g) {
         const uint32_t sb = g % C::NSB;
@@ -508,7 +555,50 @@ __global__ void __launch_bounds__(256, 1)
           return true;
         };
         bool rescaled = false;
-        if constexpr (P_TMEM) {
+        if constexpr (DSPLIT) {
+          // S = this CTA's partial (its half of head_dim) + the peer's.  Send this row's
+          // partial into the peer's buffer once the peer has read the previous one, take
+          // the peer's out of this CTA's buffer, add (partial + partial in either CTA: the
+          // same sum, so both run the same softmax), and free the buffer for the peer.
+          const uint32_t s_row = tmem + lane_base + sb * 128u;
+          uint32_t ra[64], rb[64];
+          tmem_ld32x64_async(s_row, ra);
+          tmem_ld32x64_async(s_row + 64, rb);
+          tmem_wait_ld_fence64(ra);
+          tmem_wait_ld_fence64(rb);
+          if (g > 0 && !(ok = wait_warp_cluster(BAR(C::B_RFREE), (g - 1) & 1u))) break;
+          const uint32_t peer_row = mapa_shared(recv_s + row * 512, rank ^ 1u);
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            st_cluster_v4(peer_row + ((c ^ (row & 7)) << 4), ra[4 * c], ra[4 * c + 1], ra[4 * c + 2], ra[4 * c + 3]);
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            st_cluster_v4(peer_row + (((16 + c) ^ (row & 7)) << 4), rb[4 * c], rb[4 * c + 1], rb[4 * c + 2],
+                          rb[4 * c + 3]);
+          mbar_arrive_cluster(mapa_shared(BAR(C::B_RECV), rank ^ 1u));
+          if (!(ok = wait_warp_cluster(BAR(C::B_RECV), g & 1u))) break;
+          const uint32_t my_row = recv_s + row * 512;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const uint4 x = ld_shared_v4(my_row + ((c ^ (row & 7)) << 4));
+            ra[4 * c] = __float_as_uint(__uint_as_float(ra[4 * c]) + __uint_as_float(x.x));
+            ra[4 * c + 1] = __float_as_uint(__uint_as_float(ra[4 * c + 1]) + __uint_as_float(x.y));
+            ra[4 * c + 2] = __float_as_uint(__uint_as_float(ra[4 * c + 2]) + __uint_as_float(x.z));
+            ra[4 * c + 3] = __float_as_uint(__uint_as_float(ra[4 * c + 3]) + __uint_as_float(x.w));
+          }
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const uint4 x = ld_shared_v4(my_row + (((16 + c) ^ (row & 7)) << 4));
+            rb[4 * c] = __float_as_uint(__uint_as_float(rb[4 * c]) + __uint_as_float(x.x));
+            rb[4 * c + 1] = __float_as_uint(__uint_as_float(rb[4 * c + 1]) + __uint_as_float(x.y));
+            rb[4 * c + 2] = __float_as_uint(__uint_as_float(rb[4 * c + 2]) + __uint_as_float(x.z));
+            rb[4 * c + 3] = __float_as_uint(__uint_as_float(rb[4 * c + 3]) + __uint_as_float(x.w));
+          }
+          mbar_arrive_cluster(mapa_shared(BAR(C::B_RFREE), rank ^ 1u));
+          if (!(ok = softmax_regs<C::DV>(ra, rb, s_row, tmem + lane_base + C::O_COL, lim, c2, t == 0, m_used, l,
+                                         wait_prev_pv, &rescaled)))
+            break;
+        } else if constexpr (P_TMEM) {
           if (!(ok = softmax_tile<C::DV>(tmem + lane_base + sb * 128u, tmem + lane_base + C::O_COL, lim, c2, t == 0,
                                          m_used, l, wait_prev_pv, &rescaled)))
             break;
@@ -589,6 +679,8 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  // A CTA of a pair stays until the other has stopped writing into its shared memory.
+  if constexpr (DSPLIT) cluster_sync_all();
 }
 
 // Launch with programmatic stream serialization: the kernel may begin (prologue only, see
@@ -613,16 +705,47 @@ struct FwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_o;
   FwdParams p;
   const SchedTable *tbl;
-  int grid;
+  int grid;     // CTAs (pairs of CTAs with dsplit)
   bool causal;
   bool p_smem;
+  bool dsplit;  // head_dim 512 split over the two CTAs of a cluster
   cudaStream_t stream;
 };
+
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_dsplit(const FwdLaunch &a) {
+  using C = FwdCfg<D, true, true>;
+  auto *kern = attn_fwd_kernel<D, CAUSAL, true, true>;
+  static int configured_mask = 0;  // one bit per device ordinal < 31
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 31 || !(configured_mask & (1 << dev))) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev < 31) configured_mask |= (1 << dev);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2u * static_cast<unsigned>(a.grid));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = static_cast<size_t>(C::SMEM_BYTES);
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p, *a.tbl);
+}
 
 template <int D, bool CAUSAL, bool P_TMEM>
 cudaError_t launch_fwd_variant(const FwdLaunch &a) {
   using C = FwdCfg<D, P_TMEM>;
-  auto *kern = attn_fwd_kernel<D, CAUSAL, P_TMEM>;
+  auto *kern = attn_fwd_kernel<D, CAUSAL, P_TMEM, false>;
   static int configured_mask = 0;  // one bit per device ordinal < 31
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -640,6 +763,9 @@ cudaError_t launch_fwd_d(const FwdLaunch &a) {
   if constexpr (D <= 128) {
     if (a.p_smem)
       return a.causal ? launch_fwd_variant<D, true, false>(a) : launch_fwd_variant<D, false, false>(a);
+  }
+  if constexpr (D == 512) {
+    if (a.dsplit) return a.causal ? launch_fwd_dsplit<D, true>(a) : launch_fwd_dsplit<D, false>(a);
   }
   return a.causal ? launch_fwd_variant<D, true, true>(a) : launch_fwd_variant<D, false, true>(a);
 }

@@ -99,7 +99,11 @@ int encode_bhld(CUtensorMap *tm, const void *ptr, int BH, int L, int D, int box_
 
 // ------------------------------------------------------------------ work schedule
 // The kernels a launch can use.
-enum Kind { kSingle = 0, kPair = 1 };
+// kDSplit: the single-tile kernel at head_dim 512 with head_dim split over the two CTAs
+// of a cluster (an option: slower on GB300, whose distributed shared memory moves the
+// partial logits at ~17 B per cycle per SM); its schedule deals (head, query tile) items
+// to clusters.
+enum Kind { kSingle = 0, kPair = 1, kDSplit = 2 };
 
 // Cost of a work item in units of one 128 x 128 tile step of one query tile in the
 // two-tile kernel (it runs two such steps at once, one per query tile of its item), plus
@@ -120,6 +124,7 @@ struct SchedKey {
 long long count_items(const SchedKey &k) {
   return k.kind == kPair ? static_cast<long long>(k.BH) * k.nQB : static_cast<long long>(k.BH) * k.nQ * k.dvs;
 }
+// (kDSplit keys have dvs = 1: one item per head and query tile.)
 
 // Cost of item r, mirroring the kernels' item decoding (decode_item / pp_decode).
 double item_cost(const SchedKey &k, int r) {
@@ -218,7 +223,10 @@ int choose_plan(int BH, int L, int d, int causal, int sm_count, int flags, int g
   int grid = sm_count;
   if (grid_limit > 0 && grid_limit < grid) grid = grid_limit;
   int kind;
-  if (flags & (GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE) || d > 128) {
+  if (flags & GBATTN_FLAG_DSPLIT) {
+    kind = kDSplit;  // clusters of two CTAs: the schedule's lanes are the clusters
+    grid = std::max(1, grid / 2);
+  } else if (flags & (GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE) || d > 128) {
     kind = kSingle;
   } else if (flags & GBATTN_FLAG_TWO_TILE) {
     kind = kPair;
@@ -256,10 +264,13 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // The option bits of attn_fwd_ex: known bits only, the two-tile kernel not together with
 // a single-tile option, and the two-tile kernel and shared-memory P only for d <= 128.
 int check_flags(int flags, int d) {
-  if (flags & ~(GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE | GBATTN_FLAG_TWO_TILE)) return GBATTN_ERR_FLAGS;
+  if (flags & ~(GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE | GBATTN_FLAG_TWO_TILE | GBATTN_FLAG_DSPLIT))
+    return GBATTN_ERR_FLAGS;
   if ((flags & GBATTN_FLAG_TWO_TILE) && (flags & (GBATTN_FLAG_SINGLE_TILE | GBATTN_FLAG_P_SMEM)))
     return GBATTN_ERR_FLAGS;
+  if ((flags & GBATTN_FLAG_DSPLIT) && (flags & ~GBATTN_FLAG_DSPLIT)) return GBATTN_ERR_FLAGS;
   if ((flags & (GBATTN_FLAG_P_SMEM | GBATTN_FLAG_TWO_TILE)) && d > 128) return GBATTN_ERR_HEAD_DIM;
+  if ((flags & GBATTN_FLAG_DSPLIT) && d != 512) return GBATTN_ERR_HEAD_DIM;
   return GBATTN_OK;
 }
 
@@ -317,7 +328,7 @@ extern "C" int attn_fwd_ex(const void *q, const void *k, const void *v, void *o,
   SchedKey key;
   double makespan = 0.0;
   if ((rc = choose_plan(BH, L, d, causal, di->sm_count, flags, grid_limit, key, makespan)) != GBATTN_OK) return rc;
-  const bool two_tile = key.kind != kSingle;
+  const bool two_tile = key.kind == kPair;
 
   FwdLaunch a;
   SchedTable tbl;
@@ -329,6 +340,7 @@ extern "C" int attn_fwd_ex(const void *q, const void *k, const void *v, void *o,
   get_schedule(key, &tbl);
   a.causal = causal != 0;
   a.p_smem = p_smem;
+  a.dsplit = key.kind == kDSplit;
   a.stream = static_cast<cudaStream_t>(stream);
   a.p.lse = lse;
   a.p.status = di->status;
@@ -626,8 +638,11 @@ extern "C" int attn_debug_schedule(int B, int H, int L, int d, int causal, int g
   if (grid <= 0 || grid > kSchedMaxCtas) return GBATTN_ERR_DIMS;
   if (!start || !items) return GBATTN_ERR_NULL;
   // The schedule of the kernel the flags name (no flag, d <= 128: the two-tile kernel;
-  // the automatic choice of attn_fwd is not applied here).
-  const int kind = ((flags & (GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE)) || d > 128) ? kSingle : kPair;
+  // the head_dim split's `grid` lanes are clusters of two CTAs; the automatic choice of
+  // attn_fwd is not applied here).
+  const int kind = (flags & GBATTN_FLAG_DSPLIT) ? kDSplit
+                   : ((flags & (GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE)) || d > 128) ? kSingle
+                                                                                           : kPair;
   SchedKey key{kind, B * H, (L + 127) / 128, (L + 255) / 256, kind == kSingle && d > 256 ? d / 256 : 1,
                causal != 0 ? 1 : 0, grid};
   if (count_items(key) > INT_MAX) return GBATTN_ERR_DIMS;

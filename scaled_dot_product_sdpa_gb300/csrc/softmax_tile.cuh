@@ -31,16 +31,13 @@ namespace gbattn {
 struct NoWait {
   __device__ bool operator()() const { return true; }
 };
+// The step on a row of S already in registers (ra: columns 0-63, rb: 64-127, fp32 bits);
+// P still goes to s_tmem.
 template <int DV, class Hook = NoWait>
-__device__ __forceinline__ bool softmax_tile(uint32_t s_tmem, uint32_t o_tmem, int lim, float c2, bool first,
-                                             float &m_used, float &l, const Hook &before_rescale = Hook(),
+__device__ __forceinline__ bool softmax_regs(uint32_t (&ra)[64], uint32_t (&rb)[64], uint32_t s_tmem,
+                                             uint32_t o_tmem, int lim, float c2, bool first, float &m_used,
+                                             float &l, const Hook &before_rescale = Hook(),
                                              bool *rescaled = nullptr) {
-  uint32_t ra[64], rb[64];
-  // Both halves of S in flight at once, then one wait.
-  tmem_ld32x64_async(s_tmem, ra);
-  tmem_ld32x64_async(s_tmem + 64, rb);
-  tmem_wait_ld_fence64(ra);
-  tmem_wait_ld_fence64(rb);
   float *sa = reinterpret_cast<float *>(ra);
   if (lim < 64) {
 #pragma unroll
@@ -121,6 +118,19 @@ __device__ __forceinline__ bool softmax_tile(uint32_t s_tmem, uint32_t o_tmem, i
   tmem_wait_st_fence32(pa);
   tmem_wait_st_fence32(pb);
   return true;
+}
+
+template <int DV, class Hook = NoWait>
+__device__ __forceinline__ bool softmax_tile(uint32_t s_tmem, uint32_t o_tmem, int lim, float c2, bool first,
+                                             float &m_used, float &l, const Hook &before_rescale = Hook(),
+                                             bool *rescaled = nullptr) {
+  uint32_t ra[64], rb[64];
+  // Both halves of S in flight at once, then one wait.
+  tmem_ld32x64_async(s_tmem, ra);
+  tmem_ld32x64_async(s_tmem + 64, rb);
+  tmem_wait_ld_fence64(ra);
+  tmem_wait_ld_fence64(rb);
+  return softmax_regs<DV>(ra, rb, s_tmem, o_tmem, lim, c2, first, m_used, l, before_rescale, rescaled);
 }
 
 }  // namespace gbattn

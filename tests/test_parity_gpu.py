@@ -128,9 +128,9 @@ def test_fwd_persistent_loop_with_few_ctas(grid, d, flags):
     """Few CTAs => many items per CTA: exercises the cross-item pipeline and the phase
     bookkeeping of every barrier over long runs."""
     if d > 128:
-        if flags == 4:
-            pytest.skip("head_dim 512 has only the single-tile kernel")
-        flags = 0
+        # head_dim 512: the single-tile kernel, and its head_dim split (flags 8, where
+        # `grid` CTAs make grid // 2 clusters of two, at least one).
+        flags = 2 if flags == 2 else gb.FLAG_DSPLIT
     L = 640 if d < 512 else 384
     q, k, v = inputs.qkv(1, 3, L, d, seed=grid * 100 + d, sigma=0.5 if d == 512 else 1.0)
     scale = 1.0 / math.sqrt(d)
@@ -140,7 +140,7 @@ def test_fwd_persistent_loop_with_few_ctas(grid, d, flags):
         _check(o, lse, o_ref, lse_ref, f"grid={grid} causal={causal}")
 
 
-@pytest.mark.parametrize("d,flags", [(64, 4), (64, 2), (128, 4), (128, 2), (512, 0)])
+@pytest.mark.parametrize("d,flags", [(64, 4), (64, 2), (128, 4), (128, 2), (512, 0), (512, 8)])
 def test_fwd_large_logits_force_rescale(d, flags):
     """Keys whose logits grow along the sequence force the lazy O rescale path."""
     B, H, L = 1, 2, 512
@@ -174,8 +174,8 @@ _ORACLE_CACHE = {}
 @pytest.mark.parametrize("name", list(WORKLOADS))
 def test_workload_full_size_matches_oracle(name, flags):
     w = WORKLOADS[name]
-    if w.d > 128 and flags:
-        pytest.skip("head_dim 512 has only the single-tile kernel")
+    if w.d > 128 and flags == 4:
+        flags = gb.FLAG_DSPLIT  # no two-tile kernel at head_dim 512: its head_dim split instead
     q, k, v = inputs.qkv(w.B, w.H, w.L, w.d, w.seed, w.sigma)
     o, lse = _run(*_dev(q, k, v), w.causal, w.scale, flags=flags)
     if name not in _ORACLE_CACHE:
@@ -286,3 +286,31 @@ def test_cpu_tensors_are_rejected_loudly():
     q, k, v = inputs.qkv(1, 1, 128, 64, seed=1)
     with pytest.raises(ValueError):
         gb.attn_fwd(q, k, v)
+
+
+def test_dsplit_repeats_bitwise_and_replays_from_a_graph():
+    """head_dim 512 with the head_dim split (two CTAs of a cluster exchange partial
+    logits): repeated calls and a CUDA-graph replay give the same bits; both CTAs of a
+    pair compute the same softmax, so the output halves agree with the single-tile
+    kernel within tolerance as well."""
+    w = WORKLOADS["hd512"]
+    q, k, v = _dev(*inputs.qkv(1, 4, 1000, 512, 21, 0.5))
+    o1, l1 = _run(q, k, v, True, w.scale, flags=gb.FLAG_DSPLIT)
+    o2, l2 = _run(q, k, v, True, w.scale, flags=gb.FLAG_DSPLIT)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 4, 1000, dtype=torch.float32, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        gb.attn_fwd(q, k, v, causal=True, scale=w.scale, o=o, lse=lse, stream=s, flags=gb.FLAG_DSPLIT)
+        s.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            gb.attn_fwd(q, k, v, causal=True, scale=w.scale, o=o, lse=lse, stream=s, flags=gb.FLAG_DSPLIT)
+        o.zero_()
+        g.replay()
+    s.synchronize()
+    assert torch.equal(o, o1) and torch.equal(lse, l1)
+    o3, l3 = _run(q, k, v, True, w.scale, flags=gb.FLAG_SINGLE_TILE)
+    assert (o3.float() - o1.float()).abs().max().item() < 2e-2
+    assert (l3 - l1).abs().max().item() < 1e-3

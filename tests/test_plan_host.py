@@ -23,6 +23,8 @@ def _items(kind, B, H, L, d):
     nQ, nQB = math.ceil(L / 128), math.ceil(L / 256)
     if kind == 1:
         return B * H * nQB
+    if kind == 2:
+        return B * H * nQ
     return B * H * nQ * (d // 256 if d > 256 else 1)
 
 
@@ -45,6 +47,10 @@ def test_flags_force_the_variant(B, H, L, d, causal, flags, kind):
 @pytest.mark.parametrize("B,H,L,d,causal", SHAPES)
 def test_auto_plan(B, H, L, d, causal):
     p = gb.attn_debug_plan(B, H, L, d, causal, SM)
+    if d == 512:  # the head_dim split only on request: clusters of two CTAs
+        q = gb.attn_debug_plan(B, H, L, d, causal, SM, flags=gb.FLAG_DSPLIT)
+        n = _items(2, B, H, L, d)
+        assert (q["kind"], q["items"], q["grid"]) == (2, n, min(SM // 2, n))
     if d > 128:
         assert p["kind"] == 0
         return
@@ -55,6 +61,19 @@ def test_auto_plan(B, H, L, d, causal):
     # Few blocks: the kernel with the shorter estimated schedule.
     alternatives = [gb.attn_debug_plan(B, H, L, d, causal, SM, flags=f)["makespan"] for f in (4, 2)]
     assert p["makespan"] == min(m for m in alternatives if m >= 0)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_dsplit_flag_only_at_512(d):
+    with pytest.raises(gb.GbattnError):
+        gb.attn_debug_plan(1, 2, 256, d, True, SM, flags=gb.FLAG_DSPLIT)
+
+
+def test_dsplit_flag_alone():
+    assert gb.attn_debug_plan(1, 2, 256, 512, True, SM, flags=gb.FLAG_DSPLIT)["kind"] == 2
+    for other in (1, 2, 4):
+        with pytest.raises(gb.GbattnError):
+            gb.attn_debug_plan(1, 2, 256, 512, True, SM, flags=gb.FLAG_DSPLIT | other)
 
 
 def test_grid_limit_caps_the_ctas():

@@ -9,6 +9,8 @@ import scaled_dot_product_sdpa_gb300 as gb
 
 
 def _kind(d, flags):
+    if flags & 8:
+        return "dsplit"  # one item per head and query tile, dealt to clusters of two CTAs
     return "single" if d > 128 or flags & 3 else "pair"
 
 
@@ -21,7 +23,7 @@ def _units(B, H, L, d, causal, flags, r):
             return 2 * nQ
         qb = nQB - 1 - r // BH
         return (2 * qb + 1) + min(2 * qb + 2, nQ)
-    dvs = d // 256 if d > 256 else 1
+    dvs = d // 256 if d > 256 and kind == "single" else 1
     if not causal:
         return nQ
     return nQ - 1 - r // (BH * dvs) + 1
@@ -32,12 +34,15 @@ def _n_items(B, H, L, d, flags):
     kind = _kind(d, flags)
     if kind == "pair":
         return BH * nQB
+    if kind == "dsplit":
+        return BH * nQ
     return BH * nQ * (d // 256 if d > 256 else 1)
 
 
 CASES = [(8, 32, 512, 128, True, 0), (1, 32, 1024, 128, True, 0), (1, 16, 512, 64, True, 0),
          (1, 8, 128, 64, False, 0), (1, 8, 2048, 512, True, 0), (8, 32, 512, 128, True, 2),
-         (2, 3, 1000, 64, False, 0), (1, 5, 777, 128, True, 1)]
+         (2, 3, 1000, 64, False, 0), (1, 5, 777, 128, True, 1), (1, 8, 2048, 512, True, 2),
+         (2, 3, 1000, 512, False, 8)]
 
 
 @pytest.mark.parametrize("B,H,L,d,causal,flags", CASES)
