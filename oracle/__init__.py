@@ -14,6 +14,10 @@ Definitions followed (cited by page title and section):
 * STAGE_D.md (nvfp4-megamoe-kernel), section 4: the row log-sum-exp (LSE) output;
   section 2: head_dim sub-tiles are additive in logit space (S = S_0 + S_1) and an
   "external merge" of softmax outputs over partial dot products is not the attention.
+* "Validating Memory-Optimal Transformer Kernels on Real Hardware", section 4 ("Paper
+  II: Backward Pass and Fused Forward+Backward"): the gradients of the attention output
+  with respect to Q, K and V (GQ, GK, GV, through the score gradient GS); ``sdpa_bwd``
+  computes them for a given upstream gradient dO by differentiating the definition.
 * "Validating Memory-Optimal Transformer Kernels on Real Hardware", section 5 ("Paper
   III: Inference (Decode)"): decoding, one new query row per sequence against the whole
   cached key/value sequence; ``decode`` computes it by the same definition with every key
@@ -63,6 +67,8 @@ def _load():
         lib.oracle_softmax.restype = None
         lib.oracle_pv.argtypes = [dp, dp, dp, i, i, i, i]
         lib.oracle_pv.restype = None
+        lib.oracle_sdpa_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, ctypes.c_double, i]
+        lib.oracle_sdpa_bwd.restype = i
         u16p = ctypes.POINTER(ctypes.c_uint16)
         lib.oracle_f16_to_f64.argtypes = [u16p, dp, ctypes.c_long]
         lib.oracle_f16_to_f64.restype = None
@@ -202,3 +208,19 @@ def decode(q, k, v, scale: float, heads=None, nthreads: int = 0):
     if rc < 0:
         raise MemoryError("oracle scratch allocation failed")
     return o, lse
+
+
+def sdpa_bwd(q, k, v, dout, causal: bool, scale: float, nthreads: int = 0):
+    """Gradients (dQ, dK, dV), each [B, H, L, d] float64, of O = SDPA(q, k, v) for the
+    upstream gradient dout, by differentiating the plain definition (the full L x L
+    score, probability and score-gradient matrices of each head are formed)."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, H, L, d = _shape4(q)
+    if k.shape != q.shape or v.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("q, k, v, dout must share one [B, H, L, d] shape")
+    dq, dk, dv = (np.empty((B, H, L, d), np.float64) for _ in range(3))
+    rc = _load().oracle_sdpa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, H, L, d,
+                                 int(bool(causal)), float(scale), int(nthreads))
+    if rc < 0:
+        raise MemoryError("oracle scratch allocation failed")
+    return dq, dk, dv

@@ -31,6 +31,11 @@
  * Layout of every tensor: [B, H, L, d] (or [B, H, L, L] for scores), contiguous, the
  * layout of PyTorch's scaled_dot_product_attention, which the first page gates against.
  *
+ * Backward ("Validating Memory-Optimal Transformer Kernels on Real Hardware", section 4,
+ * "Paper II: Backward Pass and Fused Forward+Backward": the gradients GQ, GK, GV of the
+ * attention output, through the gradient GS of the scores) is the derivative of the same
+ * definition for a given upstream gradient dO; see oracle_sdpa_bwd.
+ *
  * Decode ("Validating Memory-Optimal Transformer Kernels on Real Hardware", section 5,
  * "Paper III: Inference (Decode)": one new token per sequence attends to the whole cached
  * sequence, at O(n) cost in the sequence length n) is the same definition with a single
@@ -311,4 +316,95 @@ int oracle_decode_f16(const uint16_t *q, const uint16_t *k, const uint16_t *v, d
     }
     free(scratch);
     return bad ? -2 : nt;
+}
+
+/* Backward pass of the forward definition above: for an upstream gradient dO of O
+ * (every tensor [B, H, L, d], float64), per head, with S, P the scaled masked logits and
+ * their row softmax:
+ *     dV = P^T dO
+ *     dP = dO V^T
+ *     dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik)        (the softmax's Jacobian; 0 where masked)
+ *     dQ = scale * dS K,      dK = scale * dS^T Q
+ * Straight from the definition: the full L x L matrices of one head are formed (heap
+ * buffers), sums in ascending index order.  Heads are spread over `nthreads` threads.
+ * Returns the thread count used, or -1 if scratch allocation failed. */
+int oracle_sdpa_bwd(const double *q, const double *k, const double *v, const double *dout, double *dq,
+                    double *dk, double *dv, int B, int H, int L, int d, int causal, double scale, int nthreads)
+{
+    int nt = resolve_threads(nthreads);
+    long nbh = (long)B * H;
+    size_t ll = (size_t)L * (size_t)L;
+    double *scratch = (double *)malloc(sizeof(double) * (size_t)nt * 2 * (ll > 0 ? ll : 1));
+    if (!scratch)
+        return -1;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 1)
+    for (long bh = 0; bh < nbh; ++bh) {
+        int tid = 0;
+#ifdef _OPENMP
+        tid = omp_get_thread_num();
+#endif
+        double *P = scratch + (size_t)tid * 2 * ll;
+        double *dS = P + ll;
+        const double *qh = q + bh * L * d, *kh = k + bh * L * d, *vh = v + bh * L * d, *doh = dout + bh * L * d;
+        double *dqh = dq + bh * L * d, *dkh = dk + bh * L * d, *dvh = dv + bh * L * d;
+        /* P: row softmax of the scaled, masked logits (masked entries 0) */
+        for (long i = 0; i < L; ++i) {
+            long jmax = causal ? i + 1 : L;
+            double m = -INFINITY;
+            for (long j = 0; j < jmax; ++j) {
+                double acc = 0.0;
+                for (long t = 0; t < d; ++t)
+                    acc += qh[i * d + t] * kh[j * d + t];
+                P[i * L + j] = scale * acc;
+                if (P[i * L + j] > m)
+                    m = P[i * L + j];
+            }
+            double l = 0.0;
+            for (long j = 0; j < jmax; ++j) {
+                P[i * L + j] = exp(P[i * L + j] - m);
+                l += P[i * L + j];
+            }
+            for (long j = 0; j < jmax; ++j)
+                P[i * L + j] /= l;
+            for (long j = jmax; j < L; ++j)
+                P[i * L + j] = 0.0;
+        }
+        /* dP = dO V^T and dS = P (dP - rowsum(P dP)) */
+        for (long i = 0; i < L; ++i) {
+            long jmax = causal ? i + 1 : L;
+            double rs = 0.0;
+            for (long j = 0; j < jmax; ++j) {
+                double acc = 0.0;
+                for (long t = 0; t < d; ++t)
+                    acc += doh[i * d + t] * vh[j * d + t];
+                dS[i * L + j] = acc;
+                rs += P[i * L + j] * acc;
+            }
+            for (long j = 0; j < jmax; ++j)
+                dS[i * L + j] = P[i * L + j] * (dS[i * L + j] - rs);
+            for (long j = jmax; j < L; ++j)
+                dS[i * L + j] = 0.0;
+        }
+        /* dV = P^T dO,  dK = scale dS^T Q */
+        for (long j = 0; j < L; ++j)
+            for (long t = 0; t < d; ++t) {
+                double av = 0.0, ak = 0.0;
+                for (long i = 0; i < L; ++i) {
+                    av += P[i * L + j] * doh[i * d + t];
+                    ak += dS[i * L + j] * qh[i * d + t];
+                }
+                dvh[j * d + t] = av;
+                dkh[j * d + t] = scale * ak;
+            }
+        /* dQ = scale dS K */
+        for (long i = 0; i < L; ++i)
+            for (long t = 0; t < d; ++t) {
+                double aq = 0.0;
+                for (long j = 0; j < L; ++j)
+                    aq += dS[i * L + j] * kh[j * d + t];
+                dqh[i * d + t] = scale * aq;
+            }
+    }
+    free(scratch);
+    return nt;
 }
