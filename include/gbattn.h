@@ -132,6 +132,23 @@ int attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *l
 size_t attn_fwd_host_workspace_size(int B, int H, int L, int d);
 
 /*
+ * attn_bwd -- the backward pass: gradients of O = SDPA(q, k, v) (as attn_fwd computes it)
+ * for an upstream gradient dout ("Validating Memory-Optimal Transformer Kernels on Real
+ * Hardware", section 4, "Paper II: Backward Pass and Fused Forward+Backward"):
+ *     P = softmax(scale * q k^T + mask),  D_i = dout_i . o_i,
+ *     dv = P^T dout,  dS = P * (dout v^T - D),  dq = scale dS k,  dk = scale dS^T q.
+ *   q, k, v, o, dout : const fp16 [B, H, L, d], device, 16-byte aligned (o: attn_fwd's output).
+ *   lse              : const fp32 [B, H, L] (attn_fwd's LSE output).
+ *   dq, dk, dv       : fp16 [B, H, L, d] outputs, device, 16-byte aligned, overlapping no
+ *                      input and no other output (else GBATTN_ERR_ALIAS).
+ *   d : 64 or 128 (else GBATTN_ERR_HEAD_DIM).  causal, scale, stream, errors: as attn_fwd.
+ * Two kernels without atomics (one per key tile for dk and dv, one per query tile for dq),
+ * enqueued on `stream`; P is recomputed from lse, nothing else is allocated or kept.
+ */
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
+             void *dq, void *dk, void *dv, int B, int H, int L, int d, int causal, float scale, void *stream);
+
+/*
  * attn_decode -- decoding: one query row per (b, h) against all L cached keys, every key
  * visible ("Validating Memory-Optimal Transformer Kernels on Real Hardware", section 5,
  * "Paper III: Inference (Decode)"):

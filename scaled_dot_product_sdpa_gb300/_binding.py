@@ -62,6 +62,8 @@ def load_library(path: str | None = None):
     lib.attn_fwd_host_workspace_size.restype = sz
     lib.attn_debug_plan.argtypes = [i, i, i, i, i, i, i, i, ip]
     lib.attn_debug_plan.restype = i
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.attn_bwd.restype = i
     lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, vp]
     lib.attn_decode.restype = i
     lib.attn_debug_decode_plan.argtypes = [i, i, i, i, i, i, ip]
@@ -123,6 +125,35 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, 
     if rc != 0:
         raise GbattnError(rc, "attn_fwd")
     return o, lse
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
+             stream=None):
+    """Gradients (dq, dk, dv) of O = SDPA(q, k, v) for the upstream gradient dout, from the
+    forward pass's o and lse (as attn_fwd returns them).  fp16 [B, H, L, d] tensors, d 64 or
+    128; outputs allocated by torch on q's device unless given.  Enqueued on `stream`."""
+    B, H, L, d = _check_qkv(q, k, v)
+    for t in (o, dout):
+        if not t.is_cuda or t.dtype != torch.float16 or t.shape != q.shape or not t.is_contiguous():
+            raise ValueError("gbattn: o and dout must be contiguous float16 like q")
+    if not lse.is_cuda or lse.dtype != torch.float32 or lse.shape != (B, H, L) or not lse.is_contiguous():
+        raise ValueError("gbattn: lse must be contiguous float32 [B, H, L]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for t in (dq, dk, dv):
+        if t.shape != q.shape or t.dtype != torch.float16 or not t.is_contiguous():
+            raise ValueError("gbattn: dq, dk, dv must be contiguous float16 like q")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, L, d, int(bool(causal)), float(scale),
+                          _stream_handle(stream))
+    if rc != 0:
+        raise GbattnError(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_decode(q, k, v, scale: float | None = None, o=None, lse=None, stream=None):

@@ -164,6 +164,9 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (lane == 0) red[warp] = mx;
+    // The previous tile's stage is refilled by TMA (async proxy) after this barrier: order
+    // this thread's generic-proxy reads of it before that.
+    fence_proxy_async_smem();
     if (__syncthreads_or(!got)) {  // every thread leaves together when a load timed out
       ok = false;
       break;

@@ -15,6 +15,7 @@
 #include <queue>
 #include <vector>
 
+#include "attn_bwd.cuh"
 #include "attn_decode.cuh"
 #include "attn_fwd_kernel.cuh"
 #include "attn_fwd_pp.cuh"
@@ -506,6 +507,51 @@ extern "C" int attn_fwd_host(const void *q, const void *k, const void *v, void *
     if (cudaStreamWaitEvent(user, hp->out_done[(c - 1) & 1], 0) != cudaSuccess) return GBATTN_ERR_LAUNCH;
   }
   return GBATTN_OK;
+}
+
+extern "C" int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                        const void *dout, void *dq, void *dk, void *dv, int B, int H, int L, int d, int causal,
+                        float scale, void *stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return GBATTN_ERR_NULL;
+  int rc = check_shape(B, H, L, d);
+  if (rc != GBATTN_OK) return rc;
+  if (d != 64 && d != 128) return GBATTN_ERR_HEAD_DIM;
+  const void *ins[6] = {q, k, v, o, lse, dout};
+  void *outs[3] = {dq, dk, dv};
+  for (const void *x : ins)
+    if (!aligned16(x)) return GBATTN_ERR_ALIGN;
+  for (const void *x : outs)
+    if (!aligned16(x)) return GBATTN_ERR_ALIGN;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return GBATTN_ERR_SCALE;
+  const long long BH = static_cast<long long>(B) * H;
+  const size_t tb = static_cast<size_t>(BH) * L * d * 2u, lb = static_cast<size_t>(BH) * L * 4u;
+  const size_t in_sz[6] = {tb, tb, tb, tb, lb, tb};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 6; ++j)
+      if (overlaps(outs[i], tb, ins[j], in_sz[j])) return GBATTN_ERR_ALIAS;
+    for (int j = i + 1; j < 3; ++j)
+      if (overlaps(outs[i], tb, outs[j], tb)) return GBATTN_ERR_ALIAS;
+  }
+  DevInfo *di = nullptr;
+  if ((rc = device_info(&di)) != GBATTN_OK) return rc;
+  BwdLaunch a;
+  const int bh = static_cast<int>(BH);
+  if (encode_bhld(&a.tm_q, q, bh, L, d) || encode_bhld(&a.tm_k, k, bh, L, d) || encode_bhld(&a.tm_v, v, bh, L, d) ||
+      encode_bhld(&a.tm_o, o, bh, L, d) || encode_bhld(&a.tm_do, dout, bh, L, d) ||
+      encode_bhld(&a.tm_dq, dq, bh, L, d) || encode_bhld(&a.tm_dk, dk, bh, L, d) || encode_bhld(&a.tm_dv, dv, bh, L, d))
+    return GBATTN_ERR_TENSORMAP;
+  a.p.lse = lse;
+  a.p.status = di->status;
+  a.p.wait_limit = kWaitLimitCycles;
+  a.p.BH = bh;
+  a.p.L = L;
+  a.p.nQ = (L + 127) / 128;
+  a.p.c2 = scale * 1.4426950408889634f;
+  a.p.scale = scale;
+  a.causal = causal != 0;
+  a.stream = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = d == 64 ? launch_bwd_64(a) : launch_bwd_128(a);
+  return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_LAUNCH;
 }
 
 extern "C" int attn_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int L,

@@ -187,3 +187,29 @@ def test_decode_without_gpu_fails_cleanly(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present; the fake addresses must never reach a launch")
     assert _dec(lib) in (_codes()["GBATTN_ERR_LAUNCH"], _codes()["GBATTN_ERR_DEVICE"])
+
+
+DO_, DQ, DK, DV = 0x60000000, 0x70000000, 0x80000000, 0x90000000
+
+
+def _bwd(lib, q=Q, k=K, v=V, o=O, lse=LSE, do=DO_, dq=DQ, dk=DK, dv=DV, B=1, H=2, L=128, d=64, causal=0, scale=0.125):
+    return lib.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, L, d, causal, scale, None)
+
+
+def test_bwd_validation(lib):
+    c = _codes()
+    for kw in ("q", "k", "v", "o", "lse", "do", "dq", "dk", "dv"):
+        assert _bwd(lib, **{kw: 0}) == c["GBATTN_ERR_NULL"], kw
+    for B, H, L in [(0, 1, 1), (1, 0, 1), (1, 1, 0)]:
+        assert _bwd(lib, B=B, H=H, L=L) == c["GBATTN_ERR_DIMS"]
+    for d in (32, 96, 256, 512):
+        assert _bwd(lib, d=d) == c["GBATTN_ERR_HEAD_DIM"], d
+    for kw in ("q", "do", "dq", "dv", "lse"):
+        base = {"q": Q, "do": DO_, "dq": DQ, "dv": DV, "lse": LSE}[kw]
+        assert _bwd(lib, **{kw: base + 8}) == c["GBATTN_ERR_ALIGN"], kw
+    for scale in (0.0, float("nan")):
+        assert _bwd(lib, scale=scale) == c["GBATTN_ERR_SCALE"]
+    assert _bwd(lib, dq=Q) == c["GBATTN_ERR_ALIAS"]
+    assert _bwd(lib, dk=DO_ + 64) == c["GBATTN_ERR_ALIAS"]
+    assert _bwd(lib, dv=DK) == c["GBATTN_ERR_ALIAS"]
+    assert _bwd(lib, dq=LSE) == c["GBATTN_ERR_ALIAS"]
