@@ -23,7 +23,8 @@ overlaps the copies of one chunk of heads with the kernels of the others).
 
 `per_config` times every forward workload; `decode` times the decode workloads (one
 query row per head against 8192 and 1,048,576 cached keys) and reports them against the
-HBM roofline (K and V are read once).
+HBM roofline (K and V are read once); `backward` times the backward pass (attn_bwd) of
+caseC and caseD.  `--backward NAME` times one backward alone (for profiler runs).
 
 `cpu_baseline` (rank 0, N=1 only) times the float64 CPU oracle (test infrastructure) on
 the same workload on the host cores; `--impl reference` times that oracle as the
@@ -350,6 +351,47 @@ def bench_decode(device, torch, gb, inputs, hbm_peak, only=None):
     return out
 
 
+def bench_backward(device, torch, gb, inputs, tensor_peak, names=("caseC", "caseD")):
+    """The backward pass (attn_bwd) of forward workloads: mean time per call over 30
+    graph-replayed calls, CUDA events on the replay stream.  FLOPs are the usual 2.5x the
+    forward's (five products of 2*L^2*d per head, halved when causal); the kernels execute
+    seven such products."""
+    from scaled_dot_product_sdpa_gb300.configs import WORKLOADS
+    out = {}
+    for name in names:
+        w = WORKLOADS[name]
+        q, k, v = (t.to(device) for t in inputs.qkv(w.B, w.H, w.L, w.d, w.seed, w.sigma))
+        do = inputs.upstream_grad(w.B, w.H, w.L, w.d, w.seed + 100, device=device)
+        o, lse = gb.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
+        grads = [torch.empty_like(q) for _ in range(3)]
+        stream = torch.cuda.Stream(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                gb.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, dq=grads[0], dk=grads[1],
+                            dv=grads[2], stream=stream)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(10):
+                    gb.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, dq=grads[0], dk=grads[1],
+                                dv=grads[2], stream=stream)
+            g.replay()
+            stream.synchronize()
+            a.record(stream)
+            for _ in range(3):
+                g.replay()
+            b.record(stream)
+        b.synchronize()
+        t = a.elapsed_time(b) * 1e-3 / 30
+        fl = 2.5 * w.flops()
+        out[name] = {"shape": w.describe(), "kernels": ["attn_bwd_dkdv_kernel", "attn_bwd_dq_kernel"],
+                     "us": round(t * 1e6, 2), "tflops": round(fl / t / 1e12, 1),
+                     "pct_fp16_peak": round(100 * fl / t / 1e12 / tensor_peak, 2)}
+        del g
+    return out
+
+
 def decode_only(name):
     """`--decode NAME`: the decode timing of one workload alone, as a JSON line."""
     import torch
@@ -368,6 +410,27 @@ def decode_only(name):
     if status != 0:
         raise RuntimeError(f"device status {status}: {gb.attn_strerror(status)}")
     print(json.dumps({"decode": res}), flush=True)
+
+
+def backward_only(name):
+    """`--backward NAME`: the backward timing of one forward workload alone, as a JSON line."""
+    import torch
+    import scaled_dot_product_sdpa_gb300 as gb
+    from scaled_dot_product_sdpa_gb300 import build as gbuild
+    from scaled_dot_product_sdpa_gb300 import inputs
+    from scaled_dot_product_sdpa_gb300.configs import WORKLOADS
+    if name not in WORKLOADS or WORKLOADS[name].d > 128:
+        raise SystemExit(f"no backward for {name!r} (head_dim 64 or 128 workloads: "
+                         f"{sorted(n for n, w in WORKLOADS.items() if w.d <= 128)})")
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    gb.load_library(gbuild.build())
+    peaks, _ = load_peaks()
+    res = bench_backward(device, torch, gb, inputs, peaks["bf16_tflops"], names=(name,))
+    status = gb.attn_last_device_error()
+    if status != 0:
+        raise RuntimeError(f"device status {status}: {gb.attn_strerror(status)}")
+    print(json.dumps({"backward": res}), flush=True)
 
 
 def cpu_oracle_baseline(w, min_seconds=10.0, max_reps=20):
@@ -506,6 +569,7 @@ def bench_ours(args):
                                      "per_call_*: 300 single calls interleaved across the configs, CUDA events "
                                      "around each call behind a GPU-side sleep")
         line["decode"] = bench_decode(device, torch, gb, inputs, hbm_peak)
+        line["backward"] = bench_backward(device, torch, gb, inputs, fp16_peak)
         status = gb.attn_last_device_error()
         if status != 0:
             raise RuntimeError(f"device status {status}: {gb.attn_strerror(status)}")
@@ -580,11 +644,14 @@ def main(argv=None):
     ap.add_argument("--quick", action="store_true", help="timed region only (for profiler runs)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--decode", metavar="NAME", help="time only this decode workload (diagnostic; for profiler runs)")
+    ap.add_argument("--backward", metavar="NAME", help="time only the backward pass of this workload (diagnostic)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.decode:
         decode_only(args.decode)
+    elif args.backward:
+        backward_only(args.backward)
     elif args.impl == "reference":
         bench_reference(args)
     else:

@@ -6,6 +6,9 @@ V, each as ``torch.randn(B, H, L, d, dtype=float32) * sigma`` rounded to fp16.  
 are i.i.d. normal, as in the workloads of "An Optimal Mapper Meets a Real GPU",
 "Experiment one" (Cases A-D); no dataset is involved.
 
+The upstream gradient dO of the backward pass is drawn the same way by
+``upstream_grad`` (its own generator, seeded with ``seed``; standard normal, fp16).
+
 Decode inputs (one query row per head, a long key/value sequence) follow the same recipe
 with q drawn as [B, H, 1, d]; for very long sequences the draw may run on the GPU (a
 CUDA ``torch.Generator`` seeded the same way), so that no multi-GB tensor is drawn on the
@@ -36,3 +39,9 @@ def decode_qkv(B: int, H: int, L: int, d: int, seed: int, sigma: float = 1.0, de
         t = torch.randn(*shape, generator=g, dtype=torch.float32, device=gdev) * float(sigma)
         out.append(t.to(torch.float16).to(device).contiguous())
     return tuple(out)
+
+
+def upstream_grad(B: int, H: int, L: int, d: int, seed: int, device="cpu"):
+    """Return an fp16 upstream gradient dO [B, H, L, d], standard normal, on `device`."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    return torch.randn(B, H, L, d, generator=g, dtype=torch.float32).to(torch.float16).to(device).contiguous()
