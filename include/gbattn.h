@@ -141,12 +141,27 @@ size_t attn_fwd_host_workspace_size(int B, int H, int L, int d);
  *   lse              : const fp32 [B, H, L] (attn_fwd's LSE output).
  *   dq, dk, dv       : fp16 [B, H, L, d] outputs, device, 16-byte aligned, overlapping no
  *                      input and no other output (else GBATTN_ERR_ALIAS).
+ *   workspace        : device memory of attn_bwd_workspace_bytes(B, H, L) bytes, 16-byte
+ *                      aligned, overlapping no input and no output (GBATTN_ERR_NULL,
+ *                      GBATTN_ERR_ALIGN, GBATTN_ERR_ALIAS); owned by the caller, its
+ *                      contents on entry do not matter and are overwritten.
  *   d : 64 or 128 (else GBATTN_ERR_HEAD_DIM).  causal, scale, stream, errors: as attn_fwd.
- * Two kernels without atomics (one per key tile for dk and dv, one per query tile for dq),
- * enqueued on `stream`; P is recomputed from lse, nothing else is allocated or kept.
+ * Two persistent kernels without atomics, enqueued on `stream`: the first computes dq one
+ * 128-row query tile at a time and writes each query row's statistics LSE log2(e) and
+ * D_i to the workspace (8 bytes per row); the second computes dk and dv one 128-row key
+ * tile at a time, streaming the query rows with those statistics.  P is recomputed from
+ * lse; nothing is allocated or kept.
  */
 int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
-             void *dq, void *dk, void *dv, int B, int H, int L, int d, int causal, float scale, void *stream);
+             void *dq, void *dk, void *dv, void *workspace, int B, int H, int L, int d, int causal, float scale,
+             void *stream);
+
+/*
+ * attn_bwd_workspace_bytes -- bytes of workspace attn_bwd needs for B x H heads of L rows:
+ * 8 * B * H * Lp with Lp = L rounded up to a multiple of 128.  Host-only; returns a
+ * negative GBATTN_ERR_DIMS when B, H or L is not positive or the shape is too large.
+ */
+long long attn_bwd_workspace_bytes(int B, int H, int L);
 
 /*
  * attn_decode -- decoding: one query row per (b, h) against all L cached keys, every key

@@ -62,8 +62,10 @@ def load_library(path: str | None = None):
     lib.attn_fwd_host_workspace_size.restype = sz
     lib.attn_debug_plan.argtypes = [i, i, i, i, i, i, i, i, ip]
     lib.attn_debug_plan.restype = i
-    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.attn_bwd.restype = i
+    lib.attn_bwd_workspace_bytes.argtypes = [i, i, i]
+    lib.attn_bwd_workspace_bytes.restype = ctypes.c_longlong
     lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, vp]
     lib.attn_decode.restype = i
     lib.attn_debug_decode_plan.argtypes = [i, i, i, i, i, i, ip]
@@ -127,11 +129,21 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, 
     return o, lse
 
 
+def attn_bwd_workspace_bytes(B: int, H: int, L: int) -> int:
+    """Bytes of device workspace attn_bwd needs (8 per query row, rows padded to 128)."""
+    n = load_library().attn_bwd_workspace_bytes(int(B), int(H), int(L))
+    if n < 0:
+        raise GbattnError(int(n), "attn_bwd_workspace_bytes")
+    return int(n)
+
+
 def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
-             stream=None):
+             stream=None, workspace=None):
     """Gradients (dq, dk, dv) of O = SDPA(q, k, v) for the upstream gradient dout, from the
     forward pass's o and lse (as attn_fwd returns them).  fp16 [B, H, L, d] tensors, d 64 or
-    128; outputs allocated by torch on q's device unless given.  Enqueued on `stream`."""
+    128; outputs allocated by torch on q's device unless given, and so is the workspace
+    (attn_bwd_workspace_bytes(B, H, L) bytes) unless `workspace` (a contiguous CUDA tensor
+    at least that large) is given.  Enqueued on `stream`."""
     B, H, L, d = _check_qkv(q, k, v)
     for t in (o, dout):
         if not t.is_cuda or t.dtype != torch.float16 or t.shape != q.shape or not t.is_contiguous():
@@ -147,10 +159,18 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
         if t.shape != q.shape or t.dtype != torch.float16 or not t.is_contiguous():
             raise ValueError("gbattn: dq, dk, dv must be contiguous float16 like q")
     lib = load_library()
+    nbytes = attn_bwd_workspace_bytes(B, H, L)
+    if workspace is None:
+        workspace = torch.empty(nbytes // 4, dtype=torch.float32, device=q.device)
+        if isinstance(stream, torch.cuda.Stream):
+            workspace.record_stream(stream)  # freed only once the kernels on `stream` are done
+    elif (not workspace.is_cuda or not workspace.is_contiguous()
+          or workspace.numel() * workspace.element_size() < nbytes):
+        raise ValueError(f"gbattn: workspace must be a contiguous CUDA tensor of at least {nbytes} bytes")
     with torch.cuda.device(q.device):
         rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
-                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, L, d, int(bool(causal)), float(scale),
-                          _stream_handle(stream))
+                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), B, H, L, d,
+                          int(bool(causal)), float(scale), _stream_handle(stream))
     if rc != 0:
         raise GbattnError(rc, "attn_bwd")
     return dq, dk, dv

@@ -1,6 +1,7 @@
-// Instantiations and launches of the backward kernels (attn_bwd.cuh): the dK/dV kernel
-// and the dQ kernel, one after the other on the caller's stream (the dQ kernel does not
-// depend on the first; programmatic dependent launch lets its prologue overlap).
+// Instantiations and launches of the backward kernels (attn_bwd.cuh): the dQ kernel, then
+// the dK/dV kernel, on the caller's stream, each a persistent grid of one CTA per SM
+// (programmatic dependent launch lets the second one's prologue overlap the first one's
+// tail; its loads wait until the first one has completed).
 #include "attn_bwd.cuh"
 
 namespace gbattn {
@@ -21,11 +22,11 @@ cudaError_t launch_bwd_variant(const BwdLaunch &a) {
       return e;
     if (dev < 31) configured_mask |= (1 << dev);
   }
-  const int items = a.p.BH * a.p.nQ;
-  e = launch_pdl(kdkdv, items, 256, C::KV_SMEM, a.stream, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.tm_do, a.tm_dk, a.tm_dv,
+  // The dQ kernel first: it writes the row statistics the dK/dV kernel reads.
+  e = launch_pdl(kdq, a.grid, C::THREADS, C::Q_SMEM, a.stream, a.tm_q128, a.tm_k64, a.tm_v64, a.tm_do128, a.tm_o128,
                  a.p);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kdq, items, 256, C::Q_SMEM, a.stream, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.tm_do, a.tm_dq, a.p);
+  return launch_pdl(kdkdv, a.grid, C::THREADS, C::KV_SMEM, a.stream, a.tm_q64, a.tm_k128, a.tm_v128, a.tm_do64, a.p);
 }
 
 cudaError_t launch_bwd_64(const BwdLaunch &a) {

@@ -509,15 +509,24 @@ extern "C" int attn_fwd_host(const void *q, const void *k, const void *v, void *
   return GBATTN_OK;
 }
 
+extern "C" long long attn_bwd_workspace_bytes(int B, int H, int L) {
+  if (B <= 0 || H <= 0 || L <= 0) return GBATTN_ERR_DIMS;
+  const long long BH = static_cast<long long>(B) * H, Lp = (static_cast<long long>(L) + 127) / 128 * 128;
+  if (BH * Lp > INT_MAX) return GBATTN_ERR_DIMS;
+  return 8 * BH * Lp;
+}
+
 extern "C" int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
-                        const void *dout, void *dq, void *dk, void *dv, int B, int H, int L, int d, int causal,
-                        float scale, void *stream) {
-  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return GBATTN_ERR_NULL;
+                        const void *dout, void *dq, void *dk, void *dv, void *workspace, int B, int H, int L, int d,
+                        int causal, float scale, void *stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return GBATTN_ERR_NULL;
   int rc = check_shape(B, H, L, d);
   if (rc != GBATTN_OK) return rc;
   if (d != 64 && d != 128) return GBATTN_ERR_HEAD_DIM;
+  const long long wsb = attn_bwd_workspace_bytes(B, H, L);
+  if (wsb < 0) return GBATTN_ERR_DIMS;
   const void *ins[6] = {q, k, v, o, lse, dout};
-  void *outs[3] = {dq, dk, dv};
+  void *outs[4] = {dq, dk, dv, workspace};
   for (const void *x : ins)
     if (!aligned16(x)) return GBATTN_ERR_ALIGN;
   for (const void *x : outs)
@@ -526,28 +535,40 @@ extern "C" int attn_bwd(const void *q, const void *k, const void *v, const void 
   const long long BH = static_cast<long long>(B) * H;
   const size_t tb = static_cast<size_t>(BH) * L * d * 2u, lb = static_cast<size_t>(BH) * L * 4u;
   const size_t in_sz[6] = {tb, tb, tb, tb, lb, tb};
-  for (int i = 0; i < 3; ++i) {
+  const size_t out_sz[4] = {tb, tb, tb, static_cast<size_t>(wsb)};
+  for (int i = 0; i < 4; ++i) {
     for (int j = 0; j < 6; ++j)
-      if (overlaps(outs[i], tb, ins[j], in_sz[j])) return GBATTN_ERR_ALIAS;
-    for (int j = i + 1; j < 3; ++j)
-      if (overlaps(outs[i], tb, outs[j], tb)) return GBATTN_ERR_ALIAS;
+      if (overlaps(outs[i], out_sz[i], ins[j], in_sz[j])) return GBATTN_ERR_ALIAS;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlaps(outs[i], out_sz[i], outs[j], out_sz[j])) return GBATTN_ERR_ALIAS;
   }
   DevInfo *di = nullptr;
   if ((rc = device_info(&di)) != GBATTN_OK) return rc;
   BwdLaunch a;
   const int bh = static_cast<int>(BH);
-  if (encode_bhld(&a.tm_q, q, bh, L, d) || encode_bhld(&a.tm_k, k, bh, L, d) || encode_bhld(&a.tm_v, v, bh, L, d) ||
-      encode_bhld(&a.tm_o, o, bh, L, d) || encode_bhld(&a.tm_do, dout, bh, L, d) ||
-      encode_bhld(&a.tm_dq, dq, bh, L, d) || encode_bhld(&a.tm_dk, dk, bh, L, d) || encode_bhld(&a.tm_dv, dv, bh, L, d))
+  if (encode_bhld(&a.tm_q128, q, bh, L, d) || encode_bhld(&a.tm_do128, dout, bh, L, d) ||
+      encode_bhld(&a.tm_o128, o, bh, L, d) || encode_bhld(&a.tm_k128, k, bh, L, d) ||
+      encode_bhld(&a.tm_v128, v, bh, L, d) ||
+      encode_bhld(&a.tm_q64, q, bh, L, d, 64) || encode_bhld(&a.tm_do64, dout, bh, L, d, 64) ||
+      encode_bhld(&a.tm_k64, k, bh, L, d, 64) || encode_bhld(&a.tm_v64, v, bh, L, d, 64))
     return GBATTN_ERR_TENSORMAP;
   a.p.lse = lse;
+  a.p.dq = static_cast<__half *>(dq);
+  a.p.dk = static_cast<__half *>(dk);
+  a.p.dv = static_cast<__half *>(dv);
   a.p.status = di->status;
   a.p.wait_limit = kWaitLimitCycles;
   a.p.BH = bh;
   a.p.L = L;
-  a.p.nQ = (L + 127) / 128;
+  a.p.n128 = (L + 127) / 128;
+  a.p.n64 = (L + 63) / 64;
+  a.p.Lp = a.p.n128 * 128;
+  a.p.ws_lse2 = static_cast<float *>(workspace);
+  a.p.ws_d = a.p.ws_lse2 + static_cast<long long>(bh) * a.p.Lp;
+  a.p.items = bh * a.p.n128;
   a.p.c2 = scale * 1.4426950408889634f;
   a.p.scale = scale;
+  a.grid = std::min(a.p.items, di->sm_count);
   a.causal = causal != 0;
   a.stream = static_cast<cudaStream_t>(stream);
   const cudaError_t e = d == 64 ? launch_bwd_64(a) : launch_bwd_128(a);

@@ -130,6 +130,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm,
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
+// Untiled bulk copy global -> shared of `bytes` bytes (a multiple of 16; both addresses
+// 16-byte aligned), completion signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
 // Same, with an L2 cache-policy hint (a createpolicy value).
 __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *tm, int x,
                                                  int y, int z, uint32_t bar, uint64_t policy) {

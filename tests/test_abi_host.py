@@ -189,23 +189,33 @@ def test_decode_without_gpu_fails_cleanly(lib):
     assert _dec(lib) in (_codes()["GBATTN_ERR_LAUNCH"], _codes()["GBATTN_ERR_DEVICE"])
 
 
-DO_, DQ, DK, DV = 0x60000000, 0x70000000, 0x80000000, 0x90000000
+DO_, DQ, DK, DV, WS = 0x60000000, 0x70000000, 0x80000000, 0x90000000, 0xA0000000
 
 
-def _bwd(lib, q=Q, k=K, v=V, o=O, lse=LSE, do=DO_, dq=DQ, dk=DK, dv=DV, B=1, H=2, L=128, d=64, causal=0, scale=0.125):
-    return lib.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, L, d, causal, scale, None)
+def _bwd(lib, q=Q, k=K, v=V, o=O, lse=LSE, do=DO_, dq=DQ, dk=DK, dv=DV, ws=WS, B=1, H=2, L=128, d=64, causal=0,
+         scale=0.125):
+    return lib.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, ws, B, H, L, d, causal, scale, None)
+
+
+def test_bwd_workspace_bytes(lib):
+    """8 bytes per query row, rows padded to a multiple of 128."""
+    for B, H, L in [(1, 1, 1), (1, 2, 128), (2, 3, 129), (8, 32, 512), (1, 1, 1000)]:
+        assert lib.attn_bwd_workspace_bytes(B, H, L) == 8 * B * H * (-(-L // 128) * 128)
+    c = _codes()
+    for B, H, L in [(0, 1, 1), (1, 0, 1), (1, 1, 0), (1 << 16, 1 << 14, 1 << 10)]:
+        assert lib.attn_bwd_workspace_bytes(B, H, L) == c["GBATTN_ERR_DIMS"]
 
 
 def test_bwd_validation(lib):
     c = _codes()
-    for kw in ("q", "k", "v", "o", "lse", "do", "dq", "dk", "dv"):
+    for kw in ("q", "k", "v", "o", "lse", "do", "dq", "dk", "dv", "ws"):
         assert _bwd(lib, **{kw: 0}) == c["GBATTN_ERR_NULL"], kw
     for B, H, L in [(0, 1, 1), (1, 0, 1), (1, 1, 0)]:
         assert _bwd(lib, B=B, H=H, L=L) == c["GBATTN_ERR_DIMS"]
     for d in (32, 96, 256, 512):
         assert _bwd(lib, d=d) == c["GBATTN_ERR_HEAD_DIM"], d
-    for kw in ("q", "do", "dq", "dv", "lse"):
-        base = {"q": Q, "do": DO_, "dq": DQ, "dv": DV, "lse": LSE}[kw]
+    for kw in ("q", "do", "dq", "dv", "lse", "ws"):
+        base = {"q": Q, "do": DO_, "dq": DQ, "dv": DV, "lse": LSE, "ws": WS}[kw]
         assert _bwd(lib, **{kw: base + 8}) == c["GBATTN_ERR_ALIGN"], kw
     for scale in (0.0, float("nan")):
         assert _bwd(lib, scale=scale) == c["GBATTN_ERR_SCALE"]
@@ -213,3 +223,6 @@ def test_bwd_validation(lib):
     assert _bwd(lib, dk=DO_ + 64) == c["GBATTN_ERR_ALIAS"]
     assert _bwd(lib, dv=DK) == c["GBATTN_ERR_ALIAS"]
     assert _bwd(lib, dq=LSE) == c["GBATTN_ERR_ALIAS"]
+    assert _bwd(lib, ws=DV + 1024) == c["GBATTN_ERR_ALIAS"]  # inside dv
+    assert _bwd(lib, ws=O) == c["GBATTN_ERR_ALIAS"]
+    assert _bwd(lib, dk=WS + 2048 - 16) == c["GBATTN_ERR_ALIAS"]  # workspace is 2048 bytes here

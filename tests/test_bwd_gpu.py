@@ -83,3 +83,44 @@ def test_bwd_is_deterministic_and_replays_from_a_graph():
         g.replay()
     s.synchronize()
     assert all(torch.equal(x, y) for x, y in zip(outs, a))
+
+
+@pytest.mark.parametrize("B,H,L,d,causal", [
+    (2, 40, 512, 64, True),      # 320 items per kernel: every CTA of the persistent grid runs two or more
+    (1, 160, 300, 128, False),   # ragged L (300 = 2 x 128 + 44 = 4 x 64 + 44), 480 items
+    (2, 48, 1000, 128, True),    # causal, ragged, uneven item lengths across the snake order
+])
+def test_bwd_many_items_per_cta(B, H, L, d, causal):
+    """Workloads with more items than SMs: each persistent CTA carries its pipeline state
+    (ring stages, tensor-memory buffers, barrier phases) across items.  Six sampled heads
+    are compared with the oracle; every head is checked for finiteness."""
+    seed = 97 + L + d
+    q, k, v = inputs.qkv(B, H, L, d, seed)
+    do = inputs.upstream_grad(B, H, L, d, seed + 1)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = gb.attn_fwd(qd, kd, vd, causal=causal, scale=scale)
+    got = gb.attn_bwd(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert all(torch.isfinite(t).all() for t in got)
+    BH = B * H
+    heads = sorted(set(np.random.default_rng(seed).integers(0, BH, 6).tolist()) | {0, BH - 1})
+    pick = lambda t: t.reshape(BH, L, d)[heads].reshape(1, len(heads), L, d)
+    ref = oracle.sdpa_bwd(pick(q), pick(k), pick(v), pick(do), causal, float(np.float32(scale)))
+    _check([pick(t.cpu()) for t in got], ref, f"{B}x{H}x{L}x{d} causal={causal}")
+
+
+def test_bwd_workspace_contents_do_not_matter():
+    """The workspace is written before it is read: a caller's workspace full of NaN gives the
+    same gradients, bit for bit, as a fresh one."""
+    B, H, L, d = 2, 3, 300, 128
+    q, k, v = (t.cuda() for t in inputs.qkv(B, H, L, d, 21))
+    do = inputs.upstream_grad(B, H, L, d, 22, device="cuda")
+    o, lse = gb.attn_fwd(q, k, v, causal=True)
+    ref = gb.attn_bwd(q, k, v, o, lse, do, causal=True)
+    ws = torch.full((gb.attn_bwd_workspace_bytes(B, H, L) // 4,), float("nan"), device="cuda")
+    got = gb.attn_bwd(q, k, v, o, lse, do, causal=True, workspace=ws)
+    torch.cuda.synchronize()
+    assert all(torch.equal(x, y) for x, y in zip(got, ref))
+    with pytest.raises(ValueError):
+        gb.attn_bwd(q, k, v, o, lse, do, causal=True, workspace=ws[:16])
