@@ -47,6 +47,7 @@ extern "C" {
 #define GBATTN_ERR_TENSORMAP (-9)   /* the driver rejected a TMA descriptor                  */
 #define GBATTN_ERR_FLAGS (-10)      /* attn_fwd_ex: unknown bits in flags                    */
 #define GBATTN_ERR_WORKSPACE (-11)  /* attn_fwd_host: device workspace too small             */
+#define GBATTN_ERR_SCRATCH (-12)    /* attn_bwd_noalloc: shape needs more than its fixed buffer */
 
 /* Device-side status codes reported by attn_last_device_error() (positive). */
 #define GBATTN_DEV_TIMEOUT_LOAD 1    /* the TMA producer's wait for a free buffer timed out  */
@@ -162,6 +163,30 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const f
  * negative GBATTN_ERR_DIMS when B, H or L is not positive or the shape is too large.
  */
 long long attn_bwd_workspace_bytes(int B, int H, int L);
+
+/*
+ * attn_bwd_noalloc -- attn_bwd for callers that cannot allocate device memory (a plug-in
+ * inside a host application that owns every device allocation, or a latency-critical
+ * path where cudaMalloc, which may synchronise the device, is not allowed).  The paper
+ * has no counterpart: this is a deployment variant, not part of the method.
+ *   Same arguments, results and errors as attn_bwd, without `workspace`: the workspace is
+ *   a fixed buffer of attn_bwd_noalloc_max_bytes() = 16 MiB compiled into the library
+ *   (every GPU that loads it holds the buffer until the process exits).  Shapes whose
+ *   attn_bwd_workspace_bytes(B, H, L) exceeds it (more than 2,097,152 query rows after
+ *   padding L to a multiple of 128) return GBATTN_ERR_SCRATCH before anything is enqueued.
+ *   No device memory is allocated or freed.
+ *   The first call on each device looks up the buffer's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call before any
+ *   stream capture.  All calls on a device share the one buffer: calls that can run at the
+ *   same time on the GPU (on streams not ordered against each other) race and must be
+ *   serialised by the caller.  Nothing in the buffer needs to start at zero.
+ */
+int attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                     const void *dout, void *dq, void *dk, void *dv, int B, int H, int L, int d, int causal,
+                     float scale, void *stream);
+
+/* attn_bwd_noalloc_max_bytes -- the size in bytes of attn_bwd_noalloc's fixed buffer. */
+long long attn_bwd_noalloc_max_bytes(void);
 
 /*
  * attn_decode -- decoding: one query row per (b, h) against all L cached keys, every key

@@ -66,6 +66,10 @@ def load_library(path: str | None = None):
     lib.attn_bwd.restype = i
     lib.attn_bwd_workspace_bytes.argtypes = [i, i, i]
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_longlong
+    lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.attn_bwd_noalloc.restype = i
+    lib.attn_bwd_noalloc_max_bytes.argtypes = []
+    lib.attn_bwd_noalloc_max_bytes.restype = ctypes.c_longlong
     lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, vp]
     lib.attn_decode.restype = i
     lib.attn_debug_decode_plan.argtypes = [i, i, i, i, i, i, ip]

@@ -688,6 +688,7 @@ extern "C" const char *attn_strerror(int code) {
     case GBATTN_ERR_TENSORMAP: return "the driver rejected a TMA tensor-map descriptor";
     case GBATTN_ERR_FLAGS: return "flags holds bits that name no option";
     case GBATTN_ERR_WORKSPACE: return "the device workspace is smaller than attn_fwd_host_workspace_size()";
+    case GBATTN_ERR_SCRATCH: return "the shape needs more workspace than attn_bwd_noalloc's fixed buffer holds";
     case GBATTN_DEV_TIMEOUT_LOAD: return "device: the TMA producer's wait timed out";
     case GBATTN_DEV_TIMEOUT_MMA: return "device: the MMA issuer's wait timed out";
     case GBATTN_DEV_TIMEOUT_SOFTMAX: return "device: a softmax warp's wait timed out";
