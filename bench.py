@@ -61,13 +61,23 @@ def load_peaks():
         return dict(FALLBACK), "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of every source the kernels are built from (to tell whether a stored ncu
-    capture still describes the current kernel)."""
+# The sources each kernel family is built from (its own files, the shared PTX helpers, and
+# the C ABI, whose launch plan decides how the kernel runs).
+KERNEL_SOURCES = {
+    "fwd": ("attn_fwd_d", "attn_fwd_pp_d", "attn_fwd_kernel.cuh", "attn_fwd_pp.cuh", "softmax_tile.cuh"),
+    "decode": ("attn_decode", "attn_fwd_kernel.cuh"),
+    "bwd": ("attn_bwd.cu", "attn_bwd.cuh", "attn_fwd_kernel.cuh"),
+}
+SHARED_SOURCES = ("ptx.cuh", "tmem_ldst.inc", "gbattn_abi.cu")
+
+
+def kernel_source_hash(kind: str = "fwd") -> str:
+    """Hash of the sources a kernel family (fwd, decode, bwd) is built from, to tell
+    whether a stored ncu capture still describes the current kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "scaled_dot_product_sdpa_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".inc")):
+        if name.startswith(KERNEL_SOURCES[kind]) or name in SHARED_SOURCES:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode())
                 h.update(f.read())
