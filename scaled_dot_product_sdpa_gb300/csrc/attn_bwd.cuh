@@ -93,7 +93,7 @@ struct BwdCfg {
   static constexpr int KV_OFF_BAR = KV_OFF_RING + NS * STAGE;
   static constexpr int KB_KVFULL = 0, KB_IDONE = 1, KB_FULL = 2, KB_EMPTY = 2 + NS, KB_SFULL = 2 + 2 * NS,
                        KB_DPFULL = KB_SFULL + 2, KB_PFULL = KB_DPFULL + 2, KB_DSFULL = KB_PFULL + 2,
-                       KB_DRAIN = KB_DSFULL + 2, KB_N = KB_DRAIN + 1;
+                       KB_KVFREE = KB_DSFULL + 2, KB_DRAIN = KB_KVFREE + 1, KB_N = KB_DRAIN + 1;
   static constexpr int KV_SMEM = 1024 + KV_OFF_BAR + 8 * KB_N + 16;
   // dQ kernel: [Q][dO][O][ring: NS x (K, V)][row stats: lse 128 | D 128 fp32][barriers]
   static constexpr int Q_OFF_RING = 3 * RTILE;
@@ -101,7 +101,11 @@ struct BwdCfg {
   static constexpr int Q_OFF_BAR = Q_OFF_ST + 256 * 4;
   static constexpr int QB_QFULL = 0, QB_IDONE = 1, QB_RFULL = 2, QB_FULL = 3, QB_EMPTY = 3 + NS,
                        QB_SFULL = 3 + 2 * NS, QB_DPFULL = QB_SFULL + 2, QB_DSFULL = QB_DPFULL + 2,
-                       QB_DRAIN = QB_DSFULL + 2, QB_N = QB_DRAIN + 1;
+                       QB_QFREE = QB_DSFULL + 2, QB_DRAIN = QB_QFREE + 1, QB_N = QB_DRAIN + 1;
+  // QFREE: the item's Q, dO and O buffers may be refilled: the MMA warp's commit after its
+  // last S and dP products, every statistics thread (done reading dO and O) and every
+  // elementwise thread (done reading the statistics).
+  static constexpr int QFREE_COUNT = 1 + 64 + 256;
   static constexpr int Q_SMEM = 1024 + Q_OFF_BAR + 8 * QB_N + 16;
   static_assert(KV_SMEM <= 232448 && Q_SMEM <= 232448, "shared memory budget");
   static_assert(256 + 2 * D <= TMEM_COLS, "tensor memory budget");
@@ -238,6 +242,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(BAR(C::KB_PFULL + i), 256);
       mbar_init(BAR(C::KB_DSFULL + i), 256);
     }
+    mbar_init(BAR(C::KB_KVFREE), 1);
     mbar_init(BAR(C::KB_DRAIN), 1);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -289,8 +294,9 @@ __global__ void __launch_bounds__(384, 1)
           bulk_load(stage + C::ST_OFF + 256, p.ws_d + wrow, 256, BAR(C::KB_FULL + st));
           ++issued;
           if (s == 0) {
-            // K and V of this item, once every product of the previous item is complete.
-            if (kv_loads > 0 && !(ok = wait_bounded(BAR(C::KB_IDONE), (kv_loads - 1) & 1, abort_flag, p.status,
+            // K and V of this item, once the previous item's last S^T and dP^T products (the
+            // only readers of K and V) are complete: up to two steps before that item ends.
+            if (kv_loads > 0 && !(ok = wait_bounded(BAR(C::KB_KVFREE), (kv_loads - 1) & 1, abort_flag, p.status,
                                                     kDevTimeoutLoad, LIM)))
               break;
             mbar_arrive_expect_tx(BAR(C::KB_KVFULL), 2 * C::RTILE);
@@ -352,6 +358,7 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_after();
           issue_sdp(g + 1);
         }
+        if (nsteps <= 2) umma_commit(BAR(C::KB_KVFREE));  // the item's last S^T, dP^T are issued
         for (int s = 0; s < nsteps; ++s, ++g) {
           const uint32_t stage = stage_addr(g);
           const uint32_t pb = (static_cast<uint32_t>(g) >> 1) & 1u;
@@ -376,6 +383,7 @@ __global__ void __launch_bounds__(384, 1)
             if (!(ok = stage_ready(g + 2))) break;
             tc_fence_after();
             issue_sdp(g + 2);  // into this step's buffers, read in order after dV, dK above
+            if (s + 3 == nsteps) umma_commit(BAR(C::KB_KVFREE));
           }
         }
         if (!ok) break;
@@ -514,6 +522,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(BAR(C::QB_DPFULL + i), 1);
       mbar_init(BAR(C::QB_DSFULL + i), 256);
     }
+    mbar_init(BAR(C::QB_QFREE), C::QFREE_COUNT);
     mbar_init(BAR(C::QB_DRAIN), 1);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -561,8 +570,9 @@ __global__ void __launch_bounds__(384, 1)
           }
           ++issued;
           if (s == 0) {
-            // Q, dO and O of this item, once every product of the previous item is complete.
-            if (q_loads > 0 && !(ok = wait_bounded(BAR(C::QB_IDONE), (q_loads - 1) & 1, abort_flag, p.status,
+            // Q, dO and O of this item, once the previous item's last S and dP products are
+            // complete and its statistics are formed and read (up to two steps before it ends).
+            if (q_loads > 0 && !(ok = wait_bounded(BAR(C::QB_QFREE), (q_loads - 1) & 1, abort_flag, p.status,
                                                    kDevTimeoutLoad, LIM)))
               break;
             mbar_arrive_expect_tx(BAR(C::QB_QFULL), 3 * C::RTILE);
@@ -623,6 +633,7 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_after();
           issue_sdp(g + 1);
         }
+        if (nsteps <= 2) umma_commit(BAR(C::QB_QFREE));  // the item's last S, dP are issued
         for (int s = 0; s < nsteps; ++s, ++g) {
           // dQ += dS K
           if (!(ok = wait(C::QB_DSFULL + (g & 1), (static_cast<uint32_t>(g) >> 1) & 1u))) break;
@@ -637,6 +648,7 @@ __global__ void __launch_bounds__(384, 1)
             if (!(ok = stage_ready(g + 2))) break;
             tc_fence_after();
             issue_sdp(g + 2);  // into this step's buffers, read in order after dQ above
+            if (s + 3 == nsteps) umma_commit(BAR(C::QB_QFREE));
           }
         }
         if (!ok) break;
@@ -679,6 +691,7 @@ __global__ void __launch_bounds__(384, 1)
       bwd_row_stats<D>(p, bh, qt * 128, do_s, o_s, stat_s, 64 * w, lane, lse_cur);
       fence_proxy_async_smem();  // dO and O are refilled by TMA for the next item
       mbar_arrive(BAR(C::QB_RFULL));
+      mbar_arrive(BAR(C::QB_QFREE));
       ++it;
     }
   } else {
@@ -700,6 +713,7 @@ __global__ void __launch_bounds__(384, 1)
       decode(idx, bh, qt, nsteps);
       if (!(ok = wait_warp(C::QB_RFULL, it & 1))) break;
       const float lrow = stat_s[row], drow = stat_s[128 + row];
+      mbar_arrive(BAR(C::QB_QFREE));  // the statistics buffer may take the next item's
       const int qrow = qt * 128 + row;
       for (int s = 0; s < nsteps; ++s, ++g) {
         const uint32_t pb = (static_cast<uint32_t>(g) >> 1) & 1u;
