@@ -350,12 +350,13 @@ def bench_decode(device, torch, gb, inputs, hbm_peak, only=None):
             b.record(stream)
         b.synchronize()
         t = a.elapsed_time(b) * 1e-3 / 30
-        plan = gb.attn_debug_decode_plan(w.B, w.H, w.L, w.d, sm_count)
+        plan = gb.attn_debug_decode_plan(w.B, w.H, w.L, w.d, sm_count, grouped=True)
         gbs = w.bytes() / t / 1e9
-        out[name] = {"shape": w.describe(), "kernel": "attn_decode_kernel", "us": round(t * 1e6, 2),
-                     "hbm_gbs": round(gbs, 1), "pct_hbm_peak": round(100 * gbs / hbm_peak, 2),
-                     "tflops": round(w.flops() / t / 1e12, 2), "ctas_per_head": plan["ranks"],
-                     "keys_per_cta": plan["keys_per_rank"]}
+        out[name] = {"shape": w.describe(),
+                     "kernels": ["attn_decode_kernel"] + (["attn_decode_merge_kernel"] if plan["groups"] > 1 else []),
+                     "us": round(t * 1e6, 2), "hbm_gbs": round(gbs, 1), "pct_hbm_peak": round(100 * gbs / hbm_peak, 2),
+                     "tflops": round(w.flops() / t / 1e12, 2), "ctas_per_cluster": plan["ranks"],
+                     "clusters_per_head": plan["groups"], "keys_per_cta": plan["keys_per_rank"]}
         del q, k, v, g
         torch.cuda.empty_cache()
     return out

@@ -194,27 +194,40 @@ long long attn_bwd_noalloc_max_bytes(void);
  * "Paper III: Inference (Decode)"):
  *     o[b,h,:] = sum_j softmax_j(scale * q[b,h] . k[b,h,j]) v[b,h,j,:]
  *     lse[b,h] = log sum_j exp(scale * q[b,h] . k[b,h,j])                (natural log)
- *   q       : const fp16 [B, H, d] (the [B, H, 1, d] query), device, 16-byte aligned.
- *   k, v    : const fp16 [B, H, L, d], device, 16-byte aligned.
- *   o       : fp16 [B, H, d] output;  lse : fp32 [B, H] output.
+ *   q         : const fp16 [B, H, d] (the [B, H, 1, d] query), device, 16-byte aligned.
+ *   k, v      : const fp16 [B, H, L, d], device, 16-byte aligned.
+ *   o         : fp16 [B, H, d] output;  lse : fp32 [B, H] output.
+ *   workspace : NULL, or device memory of attn_decode_workspace_bytes(B, H, d) bytes,
+ *               16-byte aligned, overlapping no input or output; owned by the caller, its
+ *               contents on entry do not matter.
  *   B, H, L : > 0.  d : 64, 128, 256 or 512.  scale : finite and > 0.
  * Ownership, stream, return values and errors as for attn_fwd.  Each head's keys are
  * split over the CTAs of one thread-block cluster (up to 16), which merge their partial
- * results in distributed shared memory: no global scratch memory is used.  The work is
- * bound by the HBM reads of K and V (when B * H is below about ten, the clusters cannot
- * occupy every SM).
+ * results in distributed shared memory.  With few heads (B * H below about ten) one
+ * cluster per head cannot occupy every SM: given a workspace, each head's keys are then
+ * also split over several clusters, each cluster writes its normalised partial (o, lse)
+ * to the workspace, and a second small kernel merges them.  Without a workspace the
+ * launch keeps one cluster per head.  The work is bound by the HBM reads of K and V.
  */
-int attn_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int L, int d,
-                float scale, void *stream);
+int attn_decode(const void *q, const void *k, const void *v, void *o, float *lse, void *workspace, int B, int H,
+                int L, int d, float scale, void *stream);
+
+/*
+ * attn_decode_workspace_bytes -- bytes of the optional attn_decode workspace for B x H heads
+ * at head_dim d: B * H * 32 * (d + 2) * 4 (at most 32 clusters per head).  Host-only;
+ * negative GBATTN_ERR_DIMS or GBATTN_ERR_HEAD_DIM on bad arguments.
+ */
+long long attn_decode_workspace_bytes(int B, int H, int d);
 
 /*
  * attn_debug_decode_plan -- test hook (host-only): the split attn_decode uses for this
- * shape on a GPU with `sm_count` SMs whose clusters hold at most `max_ranks` CTAs (1..16):
- * out[0] = CTAs per head (a power of two; at most 16, 8, 4 for d <= 128, 256, 512),
- * out[1] = keys per CTA (whole key tiles of 8192 / d keys).  Returns 0 or a negative
- * GBATTN_ERR_* code.
+ * shape on a GPU with `sm_count` SMs whose clusters hold at most `max_ranks` CTAs (1..16),
+ * with a workspace (`grouped` != 0) or without: out[0] = CTAs per cluster (a power of
+ * two; at most 16, 8, 4 for d <= 128, 256, 512), out[1] = keys per CTA (whole key tiles
+ * of 8192 / d keys), out[2] = clusters per head (1 without a workspace; at most 32).
+ * Returns 0 or a negative GBATTN_ERR_* code.
  */
-int attn_debug_decode_plan(int B, int H, int L, int d, int sm_count, int max_ranks, int *out);
+int attn_debug_decode_plan(int B, int H, int L, int d, int sm_count, int max_ranks, int grouped, int *out);
 
 /*
  * attn_debug_scores -- test hook: the raw scaled logits s[b,h,i,j] = scale * q_i . k_j

@@ -70,9 +70,11 @@ def load_library(path: str | None = None):
     lib.attn_bwd_noalloc.restype = i
     lib.attn_bwd_noalloc_max_bytes.argtypes = []
     lib.attn_bwd_noalloc_max_bytes.restype = ctypes.c_longlong
-    lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, vp]
+    lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, vp]
     lib.attn_decode.restype = i
-    lib.attn_debug_decode_plan.argtypes = [i, i, i, i, i, i, ip]
+    lib.attn_decode_workspace_bytes.argtypes = [i, i, i]
+    lib.attn_decode_workspace_bytes.restype = ctypes.c_longlong
+    lib.attn_debug_decode_plan.argtypes = [i, i, i, i, i, i, i, ip]
     lib.attn_debug_decode_plan.restype = i
     lib.attn_version.argtypes = []
     lib.attn_version.restype = i
@@ -180,10 +182,12 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     return dq, dk, dv
 
 
-def attn_decode(q, k, v, scale: float | None = None, o=None, lse=None, stream=None):
+def attn_decode(q, k, v, scale: float | None = None, o=None, lse=None, stream=None, grouped: bool = True):
     """Decode: O [B, H, d] and LSE [B, H] for one fp16 query row q ([B, H, d] or
     [B, H, 1, d]) per head against fp16 k, v [B, H, L, d], every key visible.  Outputs are
-    allocated by torch on q's device unless given.  Enqueued on `stream`."""
+    allocated by torch on q's device unless given, and so is the small workspace that lets
+    a head's keys be split over several clusters (`grouped`; without it, one cluster per
+    head).  Enqueued on `stream`."""
     for t in (q, k, v):
         if not t.is_cuda:
             raise ValueError("gbattn: tensors must be on a CUDA device (no CPU path exists)")
@@ -205,21 +209,32 @@ def attn_decode(q, k, v, scale: float | None = None, o=None, lse=None, stream=No
     if lse.numel() != B * H or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("gbattn: lse must be contiguous float32 [B, H]")
     lib = load_library()
+    ws = None
+    if grouped:
+        nbytes = lib.attn_decode_workspace_bytes(B, H, d)
+        if nbytes < 0:
+            raise GbattnError(int(nbytes), "attn_decode_workspace_bytes")
+        ws = torch.empty(nbytes // 4, dtype=torch.float32, device=q.device)
+        if isinstance(stream, torch.cuda.Stream):
+            ws.record_stream(stream)  # freed only once the kernels on `stream` are done
     with torch.cuda.device(q.device):
-        rc = lib.attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, L, d,
-                             float(scale), _stream_handle(stream))
+        rc = lib.attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                             ws.data_ptr() if ws is not None else None, B, H, L, d, float(scale),
+                             _stream_handle(stream))
     if rc != 0:
         raise GbattnError(rc, "attn_decode")
     return o, lse
 
 
-def attn_debug_decode_plan(B: int, H: int, L: int, d: int, sm_count: int, max_ranks: int = 16) -> dict:
-    """The split attn_decode uses (host-only): CTAs per head and keys per CTA."""
-    out = (ctypes.c_int * 2)()
-    rc = load_library().attn_debug_decode_plan(B, H, L, d, sm_count, max_ranks, out)
+def attn_debug_decode_plan(B: int, H: int, L: int, d: int, sm_count: int, max_ranks: int = 16,
+                           grouped: bool = False) -> dict:
+    """The split attn_decode uses (host-only): CTAs per cluster, keys per CTA and clusters
+    per head (more than one only with a workspace, `grouped`)."""
+    out = (ctypes.c_int * 3)()
+    rc = load_library().attn_debug_decode_plan(B, H, L, d, sm_count, max_ranks, int(bool(grouped)), out)
     if rc != 0:
         raise GbattnError(rc, "attn_debug_decode_plan")
-    return {"ranks": out[0], "keys_per_rank": out[1]}
+    return {"ranks": out[0], "keys_per_rank": out[1], "groups": out[2]}
 
 
 def attn_debug_scores(q, k, scale: float | None = None, s=None, stream=None):

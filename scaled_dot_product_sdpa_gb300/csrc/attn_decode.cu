@@ -1,7 +1,8 @@
 // attn_decode.cu -- the decode kernel (see attn_decode.cuh) and its launches.
 //
-// One thread-block cluster per head, `ranks` CTAs in it; rank r owns the keys
-// [r * keys_per_rank, min(L, (r + 1) * keys_per_rank)).  A CTA of 256 threads:
+// `groups` thread-block clusters per head, `ranks` CTAs in each; rank r of group g owns the
+// keys [(g ranks + r) keys_per_rank, min(L, (g ranks + r + 1) keys_per_rank)).  A CTA of 256
+// threads:
 //   - streams its K and V tiles (KT keys each) through a 3-stage ring with TMA, 128-byte
 //     swizzled, so that the row reads below spread over all shared-memory banks (two CTAs
 //     fit on an SM: one CTA's tile loop, about 1.2 k cycles per 32 KB tile, is bound by its
@@ -13,7 +14,9 @@
 //   - at the end reduces its partial (m, l, o) over its threads, writes it into rank 0's
 //     shared memory (distributed shared memory) and arrives on rank 0's barrier.
 // Rank 0 waits (bounded) for every rank, merges M = max_r m_r, w_r = 2^(m_r - M),
-// o = sum_r w_r o_r / sum_r w_r l_r, lse = (M + log2 sum_r w_r l_r) ln 2, and stores them.
+// o = sum_r w_r o_r / sum_r w_r l_r, lse = (M + log2 sum_r w_r l_r) ln 2, and stores them
+// (one group per head), or stores o and the base-2 lse as the group's partial in the
+// workspace, for attn_decode_merge_kernel (several groups).
 // Arithmetic as in the forward kernels: fp16 inputs, fp32 products and sums, 2^x on the
 // special-function unit, o rounded to fp16 to nearest even.
 #include <cuda_fp16.h>
@@ -82,8 +85,9 @@ __global__ void __launch_bounds__(256, 2)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
-  const int bh = static_cast<int>(blockIdx.x) / p.ranks;
-  const int k0 = static_cast<int>(rank) * p.keys_per_rank;
+  const int cl = static_cast<int>(blockIdx.x) / p.ranks;  // cluster
+  const int bh = cl / p.groups, grp = cl - bh * p.groups;
+  const int k0 = (grp * p.ranks + static_cast<int>(rank)) * p.keys_per_rank;
   const int k1 = min(p.L, k0 + p.keys_per_rank);
   const int ntiles = k1 > k0 ? (k1 - k0 + C::KT - 1) / C::KT : 0;
 
@@ -255,6 +259,23 @@ __global__ void __launch_bounds__(256, 2)
   float Lsum = 0.f;
   for (int r = 0; r < p.ranks; ++r)
     Lsum += ex2_approx(parts[r * C::PART_FLOATS + D] - M) * parts[r * C::PART_FLOATS + D + 1];
+  if (p.groups > 1) {
+    // This group's partial: o normalised over the group's keys and its base-2 lse.  A group
+    // without keys (M = -inf: every rank's range is empty) writes o = 0, lse = -inf, which
+    // the merge weighs 0.
+    float *const row = p.ws + static_cast<size_t>(cl) * (D + 2);
+    const bool empty = !(M > -INFINITY);
+    const float inv = empty ? 0.f : 1.0f / Lsum;
+    for (int c = tid; c < D; c += C::NT) {
+      float o = 0.f;
+      if (!empty)
+        for (int r = 0; r < p.ranks; ++r)
+          o += ex2_approx(parts[r * C::PART_FLOATS + D] - M) * parts[r * C::PART_FLOATS + c];
+      row[c] = o * inv;
+    }
+    if (tid == 0) row[D] = empty ? -INFINITY : M + __log2f(Lsum);
+    return;
+  }
   const float inv = 1.0f / Lsum;
   __half *const og = static_cast<__half *>(p.o) + static_cast<size_t>(bh) * D;
   for (int c = tid; c < D; c += C::NT) {
@@ -264,6 +285,28 @@ __global__ void __launch_bounds__(256, 2)
     og[c] = __float2half_rn(o * inv);
   }
   if (tid == 0) p.lse[bh] = (M + __log2f(Lsum)) * 0.69314718055994531f;
+}
+
+// Merge of the groups' partials, one CTA of D threads per head (launched after the decode
+// kernel, whose partials it waits for).
+template <int D>
+__global__ void __launch_bounds__(D, 1) attn_decode_merge_kernel(const DecParams p) {
+  grid_launch_dependents();
+  grid_wait_prior();
+  const int bh = static_cast<int>(blockIdx.x), c = threadIdx.x;
+  const float *const rows = p.ws + static_cast<size_t>(bh) * p.groups * (D + 2);
+  float M = -INFINITY;
+  for (int g = 0; g < p.groups; ++g) M = fmaxf(M, rows[g * (D + 2) + D]);
+  float wsum = 0.f, o = 0.f;
+  for (int g = 0; g < p.groups; ++g) {
+    const float lg = rows[g * (D + 2) + D];
+    if (!(lg > -INFINITY)) continue;  // a group without keys
+    const float w = ex2_approx(lg - M);
+    wsum += w;
+    o += w * rows[g * (D + 2) + c];
+  }
+  static_cast<__half *>(p.o)[static_cast<size_t>(bh) * D + c] = __float2half_rn(o / wsum);
+  if (c == 0) p.lse[bh] = (M + __log2f(wsum)) * 0.69314718055994531f;
 }
 
 template <int D>
@@ -282,7 +325,7 @@ cudaError_t launch_decode_d(const DecLaunch &a) {
     if (dev < 31) configured_mask |= (1 << dev);
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(a.p.BH) * static_cast<unsigned>(a.p.ranks));
+  cfg.gridDim = dim3(static_cast<unsigned>(a.p.BH) * static_cast<unsigned>(a.p.groups * a.p.ranks));
   cfg.blockDim = dim3(C::NT);
   cfg.dynamicSmemBytes = static_cast<size_t>(C::SMEM_BYTES);
   cfg.stream = a.stream;
@@ -295,7 +338,15 @@ cudaError_t launch_decode_d(const DecLaunch &a) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, a.tm_k, a.tm_v, a.p);
+  e = cudaLaunchKernelEx(&cfg, kern, a.tm_k, a.tm_v, a.p);
+  if (e != cudaSuccess || a.p.groups == 1) return e;
+  cudaLaunchConfig_t mcfg = {};
+  mcfg.gridDim = dim3(static_cast<unsigned>(a.p.BH));
+  mcfg.blockDim = dim3(D);
+  mcfg.stream = a.stream;
+  mcfg.attrs = attr + 1;  // programmatic dependent launch only
+  mcfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&mcfg, attn_decode_merge_kernel<D>, a.p);
 }
 
 // The widest cluster (at most dec_max_ranks_for(D)) the device can run.

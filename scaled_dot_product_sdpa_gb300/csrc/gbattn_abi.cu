@@ -286,15 +286,28 @@ int check_shape(int B, int H, int L, int d) {
 // Decode launch plan: the CTAs per head (one cluster, a power of two) and the keys each
 // one streams (whole key tiles).  Enough CTAs for two waves of two CTAs per SM, at most
 // max_ranks (and the head_dim's own bound), and at least one key tile per CTA.
-void decode_plan(long long BH, int L, int d, int sm_count, int max_ranks, int &ranks, int &keys_per_rank) {
+// When the widest cluster still leaves the SMs short of CTAs (few heads) and a workspace
+// is given, each head's keys are also split over `groups` clusters of at most 8 CTAs: as
+// many as one wave of two CTAs per SM holds, at least one key tile per CTA, at most
+// kDecMaxGroups.  (Measured on GB300, 1 x 8 heads x 1M keys at d = 128: clusters of 16 CTAs
+// 870 us, of 8 588 us, of 4 643 us; 1 x 1 x 1M: 107, 85, 115 us.)
+void decode_plan(long long BH, int L, int d, int sm_count, int max_ranks, bool grouped, int &ranks, int &groups,
+                 int &keys_per_rank) {
   max_ranks = std::min(max_ranks, dec_max_ranks_for(d));
   const int kt = dec_key_tile(d);
   const long long tiles = (static_cast<long long>(L) + kt - 1) / kt;
   const long long want = (4LL * sm_count + BH - 1) / BH;
   int r = 1;
   while (r < want && 2 * r <= max_ranks && 2 * r <= tiles) r *= 2;
+  long long g = 1;
+  if (grouped && r < want) {
+    r = std::min(r, kDecGroupedRanks);
+    g = std::max(1LL, 2LL * sm_count / (BH * r));
+    g = std::min({g, static_cast<long long>(kDecMaxGroups), std::max(1LL, tiles / r)});
+  }
   ranks = r;
-  keys_per_rank = static_cast<int>((tiles + r - 1) / r) * kt;
+  groups = static_cast<int>(g);
+  keys_per_rank = static_cast<int>((tiles + g * r - 1) / (g * r)) * kt;
 }
 
 int dec_dim_index(int d) { return d == 64 ? 0 : d == 128 ? 1 : d == 256 ? 2 : 3; }
@@ -575,12 +588,19 @@ extern "C" int attn_bwd(const void *q, const void *k, const void *v, const void 
   return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_LAUNCH;
 }
 
-extern "C" int attn_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int L,
-                           int d, float scale, void *stream) {
+extern "C" long long attn_decode_workspace_bytes(int B, int H, int d) {
+  if (B <= 0 || H <= 0) return GBATTN_ERR_DIMS;
+  if (d != 64 && d != 128 && d != 256 && d != 512) return GBATTN_ERR_HEAD_DIM;
+  return dec_workspace_bytes(static_cast<long long>(B) * H, d);
+}
+
+extern "C" int attn_decode(const void *q, const void *k, const void *v, void *o, float *lse, void *workspace, int B,
+                           int H, int L, int d, float scale, void *stream) {
   if (!q || !k || !v || !o || !lse) return GBATTN_ERR_NULL;
   int rc = check_shape(B, H, L, d);
   if (rc != GBATTN_OK) return rc;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return GBATTN_ERR_ALIGN;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace))
+    return GBATTN_ERR_ALIGN;
   if (!std::isfinite(scale) || !(scale > 0.f)) return GBATTN_ERR_SCALE;
   const long long BH = static_cast<long long>(B) * H;
   const size_t qbytes = static_cast<size_t>(BH) * d * 2u, kvbytes = qbytes * static_cast<size_t>(L),
@@ -589,6 +609,12 @@ extern "C" int attn_decode(const void *q, const void *k, const void *v, void *o,
       overlaps(lse, lbytes, q, qbytes) || overlaps(lse, lbytes, k, kvbytes) || overlaps(lse, lbytes, v, kvbytes) ||
       overlaps(lse, lbytes, o, qbytes))
     return GBATTN_ERR_ALIAS;
+  if (workspace) {
+    const size_t wb = static_cast<size_t>(dec_workspace_bytes(BH, d));
+    if (overlaps(workspace, wb, q, qbytes) || overlaps(workspace, wb, k, kvbytes) ||
+        overlaps(workspace, wb, v, kvbytes) || overlaps(workspace, wb, o, qbytes) || overlaps(workspace, wb, lse, lbytes))
+      return GBATTN_ERR_ALIAS;
+  }
   DevInfo *di = nullptr;
   if ((rc = device_info(&di)) != GBATTN_OK) return rc;
   int &max_ranks = di->dec_max_ranks[dec_dim_index(d)];
@@ -601,7 +627,8 @@ extern "C" int attn_decode(const void *q, const void *k, const void *v, void *o,
   const int kt = dec_key_tile(d);
   if (encode_bhld(&a.tm_k, k, static_cast<int>(BH), L, d, kt) || encode_bhld(&a.tm_v, v, static_cast<int>(BH), L, d, kt))
     return GBATTN_ERR_TENSORMAP;
-  decode_plan(BH, L, d, di->sm_count, max_ranks, a.p.ranks, a.p.keys_per_rank);
+  decode_plan(BH, L, d, di->sm_count, max_ranks, workspace != nullptr, a.p.ranks, a.p.groups, a.p.keys_per_rank);
+  a.p.ws = static_cast<float *>(workspace);
   a.p.q = q;
   a.p.o = o;
   a.p.lse = lse;
@@ -621,12 +648,13 @@ extern "C" int attn_decode(const void *q, const void *k, const void *v, void *o,
   return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_LAUNCH;
 }
 
-extern "C" int attn_debug_decode_plan(int B, int H, int L, int d, int sm_count, int max_ranks, int *out) {
+extern "C" int attn_debug_decode_plan(int B, int H, int L, int d, int sm_count, int max_ranks, int grouped,
+                                      int *out) {
   if (!out) return GBATTN_ERR_NULL;
   const int rc = check_shape(B, H, L, d);
   if (rc != GBATTN_OK) return rc;
   if (sm_count <= 0 || max_ranks < 1 || max_ranks > kDecMaxRanks) return GBATTN_ERR_DIMS;
-  decode_plan(static_cast<long long>(B) * H, L, d, sm_count, max_ranks, out[0], out[1]);
+  decode_plan(static_cast<long long>(B) * H, L, d, sm_count, max_ranks, grouped != 0, out[0], out[2], out[1]);
   return GBATTN_OK;
 }
 

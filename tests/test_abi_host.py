@@ -159,8 +159,26 @@ def test_host_workspace_size(lib):
     assert lib.attn_fwd_host_workspace_size(1, 1, 0, 64) == 0
 
 
-def _dec(lib, q=Q, k=K, v=V, o=O, lse=LSE, B=1, H=2, L=128, d=64, scale=0.125):
-    return lib.attn_decode(q, k, v, o, lse, B, H, L, d, scale, None)
+DWS = 0xB0000000
+
+
+def _dec(lib, q=Q, k=K, v=V, o=O, lse=LSE, ws=None, B=1, H=2, L=128, d=64, scale=0.125):
+    return lib.attn_decode(q, k, v, o, lse, ws, B, H, L, d, scale, None)
+
+
+def test_decode_workspace_bytes(lib):
+    for B, H, d in [(1, 1, 64), (1, 8, 128), (8, 32, 512)]:
+        assert lib.attn_decode_workspace_bytes(B, H, d) == B * H * 32 * (d + 2) * 4
+    c = _codes()
+    assert lib.attn_decode_workspace_bytes(0, 1, 64) == c["GBATTN_ERR_DIMS"]
+    assert lib.attn_decode_workspace_bytes(1, 1, 96) == c["GBATTN_ERR_HEAD_DIM"]
+
+
+def test_decode_workspace_validation(lib):
+    c = _codes()
+    assert _dec(lib, ws=DWS + 8) == c["GBATTN_ERR_ALIGN"]
+    assert _dec(lib, ws=O) == c["GBATTN_ERR_ALIAS"]
+    assert _dec(lib, ws=K + 4096) == c["GBATTN_ERR_ALIAS"]  # inside k
 
 
 def test_decode_validation(lib):

@@ -118,3 +118,24 @@ def test_decode_workloads_full_size(name):
     vh = v.reshape(BH, w.L, w.d)[heads].cpu().reshape(1, len(heads), w.L, w.d)
     o_ref, lse_ref = oracle.decode(qh, kh, vh, float(np.float32(w.scale)))
     _check(o.reshape(BH, w.d)[heads], lse.reshape(BH)[heads], o_ref, lse_ref, name)
+
+
+@pytest.mark.parametrize("B,H,L,d", [
+    (1, 1, 19457, 128),   # 32 clusters of 8 CTAs per head, the last ones without keys
+    (1, 2, 40000, 128),   # several clusters per head, ragged last tile
+    (1, 1, 70000, 256),   # head_dim 256: clusters of 8
+])
+def test_decode_grouped_and_single_cluster_agree_with_oracle(B, H, L, d):
+    """Few heads: with a workspace each head's keys are split over several clusters and the
+    clusters' partials merged by a second kernel; without one, one cluster per head.  Both
+    match the oracle."""
+    plan = gb.attn_debug_decode_plan(B, H, L, d, torch.cuda.get_device_properties(0).multi_processor_count,
+                                     grouped=True)
+    assert plan["groups"] > 1
+    q, k, v = inputs.decode_qkv(B, H, L, d, seed=77 + L + d)
+    scale = 1.0 / np.sqrt(d)
+    o_ref, lse_ref = oracle.decode(q, k, v, float(np.float32(scale)))
+    for grouped in (True, False):
+        o, lse = gb.attn_decode(q.cuda(), k.cuda(), v.cuda(), scale=scale, grouped=grouped)
+        torch.cuda.synchronize()
+        _check(o, lse, o_ref, lse_ref, f"{B}x{H}x{L}x{d} grouped={grouped}")

@@ -94,28 +94,37 @@ def test_rejects_bad_arguments():
 # ----------------------------------------------------------------------------- decode
 @pytest.mark.parametrize("B,H,L,d", [(8, 32, 8192, 128), (1, 8, 1 << 20, 128), (1, 1, 1, 64), (1, 1, 5, 64),
                                      (2, 3, 300, 64), (1, 1, 65, 512), (1, 2, 1000, 256), (64, 64, 4096, 64),
-                                     (1, 1, 1 << 20, 512)])
+                                     (1, 1, 1 << 20, 512), (1, 1, 100000, 64), (2, 2, 40000, 128)])
 @pytest.mark.parametrize("max_ranks", [8, 16])
-def test_decode_plan_covers_every_key(B, H, L, d, max_ranks):
-    """Every key is owned by exactly one CTA of its head's cluster: the ranks' ranges
-    [r*kpr, (r+1)*kpr) tile [0, L) (the last ranks may be empty), in whole key tiles, with
-    a power-of-two cluster no larger than allowed and no more CTAs than key tiles."""
-    pl = gb.attn_debug_decode_plan(B, H, L, d, 152, max_ranks)
-    r, kpr = pl["ranks"], pl["keys_per_rank"]
+@pytest.mark.parametrize("grouped", [False, True])
+def test_decode_plan_covers_every_key(B, H, L, d, max_ranks, grouped):
+    """Every key is owned by exactly one CTA of its head's clusters: the ranges
+    [c*kpr, (c+1)*kpr) of the head's groups*ranks CTAs tile [0, L) (the last ones may be
+    empty), in whole key tiles, with power-of-two clusters no larger than allowed, no more
+    CTAs per head than key tiles, and one cluster per head without a workspace."""
+    pl = gb.attn_debug_decode_plan(B, H, L, d, 152, max_ranks, grouped=grouped)
+    r, kpr, g = pl["ranks"], pl["keys_per_rank"], pl["groups"]
     kt = 8192 // d
     tiles = -(-L // kt)
     assert r & (r - 1) == 0 and 1 <= r <= min(max_ranks, {64: 16, 128: 16, 256: 8, 512: 4}[d]) and r <= tiles
+    assert 1 <= g <= 32 and (grouped or g == 1) and g * r <= max(tiles, r) and (g == 1 or r <= 8)
     assert kpr % kt == 0 and kpr > 0
-    assert r * kpr >= L
-    assert kpr <= -(-tiles // r) * kt
+    assert g * r * kpr >= L
+    assert kpr <= -(-tiles // (g * r)) * kt
 
 
 def test_decode_plan_fills_the_gpu():
-    """Few heads get the widest clusters; many heads stay at one CTA per head."""
+    """Few heads get the widest clusters, and with a workspace several clusters per head
+    (up to one wave of two CTAs per SM); many heads stay at one CTA per head."""
     assert gb.attn_debug_decode_plan(1, 8, 1 << 20, 128, 152, 16)["ranks"] == 16
     assert gb.attn_debug_decode_plan(1, 8, 1 << 20, 128, 152, 8)["ranks"] == 8
     assert gb.attn_debug_decode_plan(8, 32, 8192, 128, 152, 16)["ranks"] == 4
     assert gb.attn_debug_decode_plan(64, 64, 4096, 64, 152, 16)["ranks"] == 1
+    p = gb.attn_debug_decode_plan(1, 8, 1 << 20, 128, 152, 16, grouped=True)
+    assert (p["ranks"], p["groups"]) == (8, 4)  # 8 heads x 4 clusters x 8 CTAs = 256 <= 304
+    p = gb.attn_debug_decode_plan(1, 1, 100000, 64, 152, 16, grouped=True)
+    assert (p["ranks"], p["groups"]) == (8, 32)
+    assert gb.attn_debug_decode_plan(8, 32, 8192, 128, 152, 16, grouped=True)["groups"] == 1
 
 
 def test_decode_plan_validation():
