@@ -14,11 +14,13 @@
 // save; here no atomics are used at all: two kernels, one per output side, run in this
 // order:
 //
-//   attn_bwd_dq_kernel: work item = (head, 128-query tile i), Q_i, dO_i and O_i resident,
-//     the key rows streamed in 64-row tiles j:  S = Q_i K_j^T and dP = dO_i V_j^T on the
-//     tensor core; dS is formed; then dQ_i += dS K_j.  It also forms the row statistics
-//     LSE_i log2(e) and D_i = dO_i . O_i of its tile and writes them to a workspace of
-//     8 bytes per query row (the only memory beyond the inputs and outputs).
+//   attn_bwd_dq_kernel: work item = (head, 128-query tile i), Q_i and dO_i resident (Q in
+//     two buffers, so that the next item's loads early), the key rows streamed in 64-row
+//     tiles j:  S = Q_i K_j^T and dP = dO_i V_j^T on the tensor core; dS is formed; then
+//     dQ_i += dS K_j.  Its elementwise warps also form the row statistics LSE_i log2(e)
+//     and D_i = dO_i . O_i (O and LSE read from global memory one item ahead) and write
+//     them to a workspace of 8 bytes per query row (the only memory beyond the inputs and
+//     outputs).
 //   attn_bwd_dkdv_kernel: work item = (head, 128-key tile j), K_j and V_j resident, the
 //     query rows streamed in 64-row tiles i together with their row statistics:
 //     S^T = K_j Q_i^T and dP^T = V_j dO_i^T; P^T and dS^T are formed in fp16 over the
@@ -38,9 +40,9 @@
 // not held up by a staging buffer.
 //
 // Warp roles (384 threads): warp 0 TMA producer; warp 1 tensor-memory owner and MMA
-// issuer; warps 2-3 the row statistics (dQ kernel only; idle in the other); warps 4-7 and
-// 8-11 two elementwise warpgroups, each taking one half of the 64 columns of every S / dP
-// tile, and the epilogue.
+// issuer; warps 2-3 idle; warps 4-7 and 8-11 two elementwise warpgroups, each taking one
+// half of the 64 columns of every S / dP tile (and, in the dQ kernel, one half of every
+// row of the row statistics), and the epilogue.
 // Every wait is bounded (about two seconds of SM clock), as in the forward kernels.
 #pragma once
 
@@ -52,6 +54,7 @@ namespace gbattn {
 
 struct BwdParams {
   const float *lse;        // [BH, L] forward LSE (natural log)
+  const __half *o;         // [BH, L, D] forward output
   __half *dq, *dk, *dv;    // [BH, L, D] outputs
   float *ws_lse2, *ws_d;   // workspace [BH, Lp] each: LSE log2(e) (+inf past L) and D
   unsigned *status;
@@ -66,7 +69,7 @@ struct BwdParams {
 
 struct BwdLaunch {
   // Resident operands use 128-row boxes, streamed operands 64-row boxes.
-  CUtensorMap tm_q128, tm_do128, tm_o128, tm_k128, tm_v128, tm_q64, tm_do64, tm_k64, tm_v64;
+  CUtensorMap tm_q128, tm_do128, tm_k128, tm_v128, tm_q64, tm_do64, tm_k64, tm_v64;
   BwdParams p;
   int grid;  // persistent CTAs (<= items)
   bool causal;
@@ -95,17 +98,21 @@ struct BwdCfg {
                        KB_DPFULL = KB_SFULL + 2, KB_PFULL = KB_DPFULL + 2, KB_DSFULL = KB_PFULL + 2,
                        KB_KVFREE = KB_DSFULL + 2, KB_DRAIN = KB_KVFREE + 1, KB_N = KB_DRAIN + 1;
   static constexpr int KV_SMEM = 1024 + KV_OFF_BAR + 8 * KB_N + 16;
-  // dQ kernel: [Q][dO][O][ring: NS x (K, V)][row stats: lse 128 | D 128 fp32][barriers]
-  static constexpr int Q_OFF_RING = 3 * RTILE;
-  static constexpr int Q_OFF_ST = Q_OFF_RING + NS * 2 * STILE;
+  // dQ kernel (128-key steps): [Q][dO][K ring: NKS x 128-row tiles][V ring: NVS x 128-row
+  // tiles][D halves: 2 x 128 fp32][barriers]
+  static constexpr int NKS = D == 64 ? 6 : 3, NVS = D == 64 ? 4 : 2;
+  static constexpr uint32_t IDESC_S128 = idesc_f16_f32(128, 128, 0, 0);
+  static constexpr int Q_OFF_K = 2 * RTILE;
+  static constexpr int Q_OFF_V = Q_OFF_K + NKS * RTILE;
+  static constexpr int Q_OFF_ST = Q_OFF_V + NVS * RTILE;
   static constexpr int Q_OFF_BAR = Q_OFF_ST + 256 * 4;
-  static constexpr int QB_QFULL = 0, QB_IDONE = 1, QB_RFULL = 2, QB_FULL = 3, QB_EMPTY = 3 + NS,
-                       QB_SFULL = 3 + 2 * NS, QB_DPFULL = QB_SFULL + 2, QB_DSFULL = QB_DPFULL + 2,
-                       QB_QFREE = QB_DSFULL + 2, QB_DRAIN = QB_QFREE + 1, QB_N = QB_DRAIN + 1;
-  // QFREE: the item's Q, dO and O buffers may be refilled: the MMA warp's commit after its
-  // last S and dP products, every statistics thread (done reading dO and O) and every
-  // elementwise thread (done reading the statistics).
-  static constexpr int QFREE_COUNT = 1 + 64 + 256;
+  static constexpr int QB_QFULL = 0, QB_QFREE = 1, QB_DOFULL = 2, QB_DOFREE = 3, QB_DPART = 4, QB_IDONE = 5,
+                       QB_KFULL = 6, QB_KEMPTY = 6 + NKS, QB_VFULL = 6 + 2 * NKS, QB_VEMPTY = QB_VFULL + NVS,
+                       QB_SFULL = QB_VEMPTY + NVS, QB_DPFULL = QB_SFULL + 2, QB_DSFULL = QB_DPFULL + 1,
+                       QB_DRAIN = QB_DSFULL + 1, QB_N = QB_DRAIN + 1;
+  // DOFREE: the dO buffer may be refilled: the MMA warp's commit after the item's last dP
+  // product and every elementwise thread (done reading dO for D).
+  static constexpr int DOFREE_COUNT = 1 + 256;
   static constexpr int Q_SMEM = 1024 + Q_OFF_BAR + 8 * QB_N + 16;
   static_assert(KV_SMEM <= 232448 && Q_SMEM <= 232448, "shared memory budget");
   static_assert(256 + 2 * D <= TMEM_COLS, "tensor memory budget");
@@ -138,46 +145,6 @@ __device__ __forceinline__ float bwd_dot8(uint4 a, uint4 b) {
     acc1 = fmaf(x.y, y.y, acc1);
   }
   return acc0 + acc1;
-}
-
-// LSE of rows row0 + lane and row0 + 32 + lane of the 128-row query tile at query q0
-// (+inf past L), for bwd_row_stats; loaded ahead of the tile's shared-memory work.
-__device__ __forceinline__ void bwd_row_lse(const BwdParams &p, int bh, int q0, int row0, int lane, float (&l)[2]) {
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int qrow = q0 + row0 + 32 * i + lane;
-    l[i] = qrow < p.L ? __ldg(p.lse + static_cast<long long>(bh) * p.L + qrow) : INFINITY;
-  }
-}
-
-// Row statistics of rows [row0, row0 + 64) of the 128-row query tile at query q0 (one
-// warp; lane l takes rows row0 + l and row0 + 32 + l), from their LSE (bwd_row_lse) and
-// the swizzled dO and O tiles in shared memory: stat[r] = LSE_r log2(e) (+inf past L, so
-// that P = 0 there) and stat[128 + r] = D_r = dO_r . O_r, also written to the workspace
-// (row r of the padded [BH, Lp] layout).
-template <int D>
-__device__ __forceinline__ void bwd_row_stats(const BwdParams &p, int bh, int q0, uint32_t do_tile, uint32_t o_tile,
-                                              float *stat, int row0, int lane, const float (&lse)[2]) {
-  constexpr int CH = BwdCfg<D>::RCHUNK;
-  constexpr float kLog2e = 1.4426950408889634f;
-  const long long wrow0 = static_cast<long long>(bh) * p.Lp + q0;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int row = row0 + 32 * i + lane;
-    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-    for (int c = 0; c < D / 8; c += 2) {
-      acc0 += bwd_dot8(ld_shared_v4(bwd_chunk_addr(do_tile, CH, row, c)),
-                       ld_shared_v4(bwd_chunk_addr(o_tile, CH, row, c)));
-      acc1 += bwd_dot8(ld_shared_v4(bwd_chunk_addr(do_tile, CH, row, c + 1)),
-                       ld_shared_v4(bwd_chunk_addr(o_tile, CH, row, c + 1)));
-    }
-    const float dd = acc0 + acc1, ls = lse[i] * kLog2e;
-    stat[row] = ls;
-    stat[128 + row] = dd;
-    p.ws_lse2[wrow0 + row] = ls;
-    p.ws_d[wrow0 + row] = dd;
-  }
 }
 
 // Epilogue: NC columns of an fp32 accumulator row in tensor memory, times `mult`, to fp16
@@ -480,18 +447,20 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // ======================================================================== dQ
+// Steps of 128 key rows: K and V stream through rings of their own (K is read by S and by
+// the dQ product of its step, V only by dP), S is double-buffered in tensor memory.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       const __grid_constant__ CUtensorMap tm_o, const BwdParams p) {
+                       const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *const base_ptr = smem_raw + (base - raw);
-  const uint32_t q_s = base, do_s = base + C::RTILE, o_s = base + 2 * C::RTILE, ring_s = base + C::Q_OFF_RING;
-  float *const stat_s = reinterpret_cast<float *>(base_ptr + C::Q_OFF_ST);  // [lse 128 | D 128]
+  const uint32_t q_s = base, do_s = base + C::RTILE, k_ring = base + C::Q_OFF_K, v_ring = base + C::Q_OFF_V;
+  float *const dpart = reinterpret_cast<float *>(base_ptr + C::Q_OFF_ST);  // [half][128 rows]
   const uint32_t bar_s = base + C::Q_OFF_BAR;
   uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + C::Q_OFF_BAR + 8 * C::QB_N);
   volatile uint32_t *const abort_flag = tmem_slot + 1;
@@ -500,29 +469,35 @@ __global__ void __launch_bounds__(384, 1)
   const long long LIM = p.wait_limit;
   const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
   // Item idx: query tile qt of head bh, longest first (causal: the last query tiles see the
-  // most key tiles); its steps are the 64-row key tiles 0 .. nsteps-1.
+  // most key tiles); its steps are the 128-row key tiles 0 .. nsteps-1.
   auto decode = [&](int idx, int &bh, int &qt, int &nsteps) {
     const int grp = idx / p.BH;
     bh = idx - grp * p.BH;
     qt = CAUSAL ? p.n128 - 1 - grp : grp;
-    nsteps = CAUSAL ? min(p.n64, 2 * qt + 2) : p.n64;
+    nsteps = CAUSAL ? qt + 1 : p.n128;
   };
-  auto stage_addr = [&](int gg) -> uint32_t { return ring_s + (gg % C::NS) * 2 * C::STILE; };
+  auto k_tile = [&](int gg) -> uint32_t { return k_ring + (gg % C::NKS) * C::RTILE; };
+  auto v_tile = [&](int gg) -> uint32_t { return v_ring + (gg % C::NVS) * C::RTILE; };
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::QB_QFULL), 1);
+    mbar_init(BAR(C::QB_QFREE), 1);
+    mbar_init(BAR(C::QB_DOFULL), 1);
+    mbar_init(BAR(C::QB_DOFREE), C::DOFREE_COUNT);
+    mbar_init(BAR(C::QB_DPART), 256);
     mbar_init(BAR(C::QB_IDONE), 1);
-    mbar_init(BAR(C::QB_RFULL), 64);
-    for (int i = 0; i < C::NS; ++i) {
-      mbar_init(BAR(C::QB_FULL + i), 1);
-      mbar_init(BAR(C::QB_EMPTY + i), 1);
+    for (int i = 0; i < C::NKS; ++i) {
+      mbar_init(BAR(C::QB_KFULL + i), 1);
+      mbar_init(BAR(C::QB_KEMPTY + i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(BAR(C::QB_SFULL + i), 1);
-      mbar_init(BAR(C::QB_DPFULL + i), 1);
-      mbar_init(BAR(C::QB_DSFULL + i), 256);
+    for (int i = 0; i < C::NVS; ++i) {
+      mbar_init(BAR(C::QB_VFULL + i), 1);
+      mbar_init(BAR(C::QB_VEMPTY + i), 1);
     }
-    mbar_init(BAR(C::QB_QFREE), C::QFREE_COUNT);
+    mbar_init(BAR(C::QB_SFULL), 1);
+    mbar_init(BAR(C::QB_SFULL + 1), 1);
+    mbar_init(BAR(C::QB_DPFULL), 1);
+    mbar_init(BAR(C::QB_DSFULL), 256);
     mbar_init(BAR(C::QB_DRAIN), 1);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -530,7 +505,6 @@ __global__ void __launch_bounds__(384, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
-    tma_prefetch_desc(&tm_o);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -542,52 +516,66 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
   grid_launch_dependents();
   grid_wait_prior();
-  // Tensor memory: step buffer b holds S at [128 b, 128 b + 64) and dP at [128 b + 64,
-  // 128 b + 128) (dS packed over the first 16 columns of each 32-column half); dQ [256, 256+D).
-  constexpr uint32_t C_DQ = 256;
+  // Tensor memory: S of step gg at [128 (gg & 1), +128), dP at [256, 384) (dS packed over
+  // [256, 288) and [320, 352)), dQ at [384, 384 + D).
+  constexpr uint32_t C_DP = 256, C_DQ = 384;
+  static_assert(C_DQ + D <= BwdCfg<D>::TMEM_COLS, "tensor memory budget");
   auto c_s = [](int gg) -> uint32_t { return static_cast<uint32_t>(gg & 1) * 128u; };
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
       bool ok = true;
-      int g = 0, issued = 0, q_loads = 0;
+      int g = 0, nk = 0, nv = 0, it = 0;  // K and V tiles issued, items whose Q and dO are issued
+      bool q_pending = false;              // this item's Q is issued, its dO not yet
       for (int r = 0; ok && r * G < p.items; ++r) {
         const int idx = bwd_item(r, cta, G);
         if (idx >= p.items) continue;
         int bh, qt, nsteps;
         decode(idx, bh, qt, nsteps);
         for (int s = 0; s < nsteps; ++s, ++g) {
-          const int st = g % C::NS;
-          if (!(ok = wait_bounded(BAR(C::QB_EMPTY + st), ((g / C::NS) & 1) ^ 1u, abort_flag, p.status, kDevTimeoutLoad,
-                                  LIM)))
+          if (!(ok = wait_bounded(BAR(C::QB_KEMPTY + g % C::NKS), ((g / C::NKS) & 1) ^ 1u, abort_flag, p.status,
+                                  kDevTimeoutLoad, LIM)))
             break;
-          const uint32_t stage = stage_addr(g);
-          mbar_arrive_expect_tx(BAR(C::QB_FULL + st), 2 * C::STILE);
-          for (int c = 0; c < C::NCH; ++c) {
-            tma_load_3d(stage + c * C::SCHUNK, &tm_k, c * 64, s * 64, bh, BAR(C::QB_FULL + st));
-            tma_load_3d(stage + C::STILE + c * C::SCHUNK, &tm_v, c * 64, s * 64, bh, BAR(C::QB_FULL + st));
-          }
-          ++issued;
+          mbar_arrive_expect_tx(BAR(C::QB_KFULL + g % C::NKS), C::RTILE);
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(k_tile(g) + c * C::RCHUNK, &tm_k, c * 64, s * 128, bh, BAR(C::QB_KFULL + g % C::NKS));
+          ++nk;
           if (s == 0) {
-            // Q, dO and O of this item, once the previous item's last S and dP products are
-            // complete and its statistics are formed and read (up to two steps before it ends).
-            if (q_loads > 0 && !(ok = wait_bounded(BAR(C::QB_QFREE), (q_loads - 1) & 1, abort_flag, p.status,
-                                                   kDevTimeoutLoad, LIM)))
+            // Q and dO of this item, once the previous item's last S (Q) and last dP and D
+            // (dO) are complete.
+            if (it >= 1 && !(ok = wait_bounded(BAR(C::QB_QFREE), (it - 1) & 1, abort_flag, p.status, kDevTimeoutLoad,
+                                               LIM)))
               break;
-            mbar_arrive_expect_tx(BAR(C::QB_QFULL), 3 * C::RTILE);
-            for (int c = 0; c < C::NCH; ++c) {
+            mbar_arrive_expect_tx(BAR(C::QB_QFULL), C::RTILE);
+            for (int c = 0; c < C::NCH; ++c)
               tma_load_3d(q_s + c * C::RCHUNK, &tm_q, c * 64, qt * 128, bh, BAR(C::QB_QFULL));
-              tma_load_3d(do_s + c * C::RCHUNK, &tm_do, c * 64, qt * 128, bh, BAR(C::QB_QFULL));
-              tma_load_3d(o_s + c * C::RCHUNK, &tm_o, c * 64, qt * 128, bh, BAR(C::QB_QFULL));
-            }
-            ++q_loads;
+            q_pending = true;
+            if (it >= 1 && !(ok = wait_bounded(BAR(C::QB_DOFREE), (it - 1) & 1, abort_flag, p.status, kDevTimeoutLoad,
+                                               LIM)))
+              break;
+            mbar_arrive_expect_tx(BAR(C::QB_DOFULL), C::RTILE);
+            for (int c = 0; c < C::NCH; ++c)
+              tma_load_3d(do_s + c * C::RCHUNK, &tm_do, c * 64, qt * 128, bh, BAR(C::QB_DOFULL));
+            q_pending = false;
+            ++it;
           }
+          if (!(ok = wait_bounded(BAR(C::QB_VEMPTY + g % C::NVS), ((g / C::NVS) & 1) ^ 1u, abort_flag, p.status,
+                                  kDevTimeoutLoad, LIM)))
+            break;
+          mbar_arrive_expect_tx(BAR(C::QB_VFULL + g % C::NVS), C::RTILE);
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(v_tile(g) + c * C::RCHUNK, &tm_v, c * 64, s * 128, bh, BAR(C::QB_VFULL + g % C::NVS));
+          ++nv;
         }
       }
-      if (q_loads > 0) wait_drain(BAR(C::QB_QFULL), (q_loads - 1) & 1, LIM);
-      for (int s = issued > C::NS ? issued - C::NS : 0; s < issued; ++s)
-        wait_drain(BAR(C::QB_FULL + s % C::NS), (s / C::NS) & 1, LIM);
+      // Drain: every load issued lands before the CTA may exit.
+      if (it + (q_pending ? 1 : 0) > 0) wait_drain(BAR(C::QB_QFULL), (it + (q_pending ? 1 : 0) - 1) & 1, LIM);
+      if (it > 0) wait_drain(BAR(C::QB_DOFULL), (it - 1) & 1, LIM);
+      for (int i = nk > C::NKS ? nk - C::NKS : 0; i < nk; ++i)
+        wait_drain(BAR(C::QB_KFULL + i % C::NKS), (i / C::NKS) & 1, LIM);
+      for (int i = nv > C::NVS ? nv - C::NVS : 0; i < nv; ++i)
+        wait_drain(BAR(C::QB_VFULL + i % C::NVS), (i / C::NVS) & 1, LIM);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -599,157 +587,192 @@ __global__ void __launch_bounds__(384, 1)
         return wait_bounded(BAR(b), ph, abort_flag, p.status, kDevTimeoutMma, LIM);
       };
       const SDesc qa = sdesc_split(sdesc_sw128(q_s, 16, 1024)), doa = sdesc_split(sdesc_sw128(do_s, 16, 1024));
-      // S = Q K^T and dP = dO V^T of global step gg into its buffer.
-      auto issue_sdp = [&](int gg) {
-        const uint32_t stage = stage_addr(gg);
-        const SDesc kb = sdesc_split(sdesc_sw128(stage, 16, 1024));
-        const SDesc vb = sdesc_split(sdesc_sw128(stage + C::STILE, 16, 1024));
+      auto k_ready = [&](int gg) { return wait(C::QB_KFULL + gg % C::NKS, (gg / C::NKS) & 1); };
+      auto v_ready = [&](int gg) { return wait(C::QB_VFULL + gg % C::NVS, (gg / C::NVS) & 1); };
+      // S = Q K^T of global step gg into its buffer.
+      auto issue_s = [&](int gg) {
+        const SDesc kb = sdesc_split(sdesc_sw128(k_tile(gg), 16, 1024));
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_ss_off(tmem + c_s(gg), qa, c * C::RCHUNK + kk * 32, kb, c * C::SCHUNK + kk * 32, C::IDESC_S,
+            umma_ss_off(tmem + c_s(gg), qa, c * C::RCHUNK + kk * 32, kb, c * C::RCHUNK + kk * 32, C::IDESC_S128,
                         (c | kk) != 0 ? 1u : 0u);
         umma_commit(BAR(C::QB_SFULL + (gg & 1)));
+      };
+      // dP = dO V^T of global step gg; its V tile is free once this completes.
+      auto issue_dp = [&](int gg) {
+        const SDesc vb = sdesc_split(sdesc_sw128(v_tile(gg), 16, 1024));
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_ss_off(tmem + c_s(gg) + 64, doa, c * C::RCHUNK + kk * 32, vb, c * C::SCHUNK + kk * 32, C::IDESC_S,
+            umma_ss_off(tmem + C_DP, doa, c * C::RCHUNK + kk * 32, vb, c * C::RCHUNK + kk * 32, C::IDESC_S128,
                         (c | kk) != 0 ? 1u : 0u);
-        umma_commit(BAR(C::QB_DPFULL + (gg & 1)));
+        umma_commit(BAR(C::QB_DPFULL));
+        umma_commit(BAR(C::QB_VEMPTY + gg % C::NVS));
       };
-      auto stage_ready = [&](int gg) { return wait(C::QB_FULL + gg % C::NS, (gg / C::NS) & 1); };
       for (int r = 0; ok && r * G < p.items; ++r) {
         const int idx = bwd_item(r, cta, G);
         if (idx >= p.items) continue;
         int bh, qt, nsteps;
         decode(idx, bh, qt, nsteps);
-        if (!(ok = wait(C::QB_QFULL, it & 1) && stage_ready(g))) break;
+        if (!(ok = wait(C::QB_QFULL, it & 1) && k_ready(g))) break;
         tc_fence_after();
-        issue_sdp(g);
+        issue_s(g);
+        if (!(ok = wait(C::QB_DOFULL, it & 1) && v_ready(g))) break;
+        tc_fence_after();
+        issue_dp(g);
         if (nsteps > 1) {
-          if (!(ok = stage_ready(g + 1))) break;
+          if (!(ok = k_ready(g + 1))) break;
           tc_fence_after();
-          issue_sdp(g + 1);
+          issue_s(g + 1);
         }
-        if (nsteps <= 2) umma_commit(BAR(C::QB_QFREE));  // the item's last S, dP are issued
+        if (nsteps <= 2) umma_commit(BAR(C::QB_QFREE));  // the item's last S is issued
+        if (nsteps <= 1) umma_commit(BAR(C::QB_DOFREE));  // and its last dP
         for (int s = 0; s < nsteps; ++s, ++g) {
           // dQ += dS K
-          if (!(ok = wait(C::QB_DSFULL + (g & 1), (static_cast<uint32_t>(g) >> 1) & 1u))) break;
+          if (!(ok = wait(C::QB_DSFULL, g & 1))) break;
           tc_fence_after();
-          const SDesc km = sdesc_split(sdesc_sw128(stage_addr(g), C::SCHUNK, 1024));
+          const SDesc km = sdesc_split(sdesc_sw128(k_tile(g), C::RCHUNK, 1024));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_ts_off(tmem + C_DQ, tmem + c_s(g) + 64 + bwd_a_col(kk), km, kk * 2048, C::IDESC_ACC,
-                        (s > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(BAR(C::QB_EMPTY + g % C::NS));
-          if (s + 2 < nsteps) {
-            if (!(ok = stage_ready(g + 2))) break;
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts_off(tmem + C_DQ, tmem + C_DP + static_cast<uint32_t>((kk >> 2) * 64 + (kk & 3) * 8), km,
+                        kk * 2048, C::IDESC_ACC, (s > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(BAR(C::QB_KEMPTY + g % C::NKS));
+          if (s + 1 < nsteps) {
+            if (!(ok = v_ready(g + 1))) break;
             tc_fence_after();
-            issue_sdp(g + 2);  // into this step's buffers, read in order after dQ above
+            issue_dp(g + 1);  // into the dP columns, read in order after dQ above
+            if (s + 2 == nsteps) umma_commit(BAR(C::QB_DOFREE));
+          }
+          if (s + 2 < nsteps) {
+            if (!(ok = k_ready(g + 2))) break;
+            tc_fence_after();
+            issue_s(g + 2);  // into this step's S buffer (its P was consumed before dS)
             if (s + 3 == nsteps) umma_commit(BAR(C::QB_QFREE));
           }
         }
         if (!ok) break;
-        umma_commit(BAR(C::QB_IDONE));  // Q, dO free; dQ final
+        umma_commit(BAR(C::QB_IDONE));  // dQ final
         ++it;
       }
       umma_commit(BAR(C::QB_DRAIN));
       wait_drain(BAR(C::QB_DRAIN), 0, LIM);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // ------------------------------------------------------------------ row statistics
-    const int w = warp - 2;  // rows [64 w, 64 w + 64) of the item's query tile
-    int it = 0;
-    float lse_next[2];
-    bool have_next = false;
-    for (int r = 0; r * G < p.items; ++r) {
-      const int idx = bwd_item(r, cta, G);
-      if (idx >= p.items) continue;
-      int bh, qt, nsteps;
-      decode(idx, bh, qt, nsteps);
-      float lse_cur[2];
-      if (have_next) {
-        lse_cur[0] = lse_next[0];
-        lse_cur[1] = lse_next[1];
-      } else {
-        bwd_row_lse(p, bh, qt * 128, 64 * w, lane, lse_cur);
-      }
-      // The next item's LSE is loaded while this item runs.
-      const int nidx = bwd_item(r + 1, cta, G);
-      have_next = nidx < p.items;
-      if (have_next) {
-        int nbh, nqt, nn;
-        decode(nidx, nbh, nqt, nn);
-        bwd_row_lse(p, nbh, nqt * 128, 64 * w, lane, lse_next);
-      }
-      const bool ok = __all_sync(0xffffffffu, wait_bounded(BAR(C::QB_QFULL), it & 1, abort_flag, p.status,
-                                                           kDevTimeoutSoftmax, LIM));
-      if (!ok) break;
-      bwd_row_stats<D>(p, bh, qt * 128, do_s, o_s, stat_s, 64 * w, lane, lse_cur);
-      fence_proxy_async_smem();  // dO and O are refilled by TMA for the next item
-      mbar_arrive(BAR(C::QB_RFULL));
-      mbar_arrive(BAR(C::QB_QFREE));
-      ++it;
-    }
-  } else {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------------ elementwise warpgroups
-    const int h = (warp - 4) >> 2;        // key columns [32 h, 32 h + 32) of every tile
+    const int h = (warp - 4) >> 2;        // key columns [64 h, 64 h + 64) of every tile;
+                                          // head_dim columns [h D/2, (h+1) D/2) of D and dQ
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;  // query row of the tile == tensor-memory lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const float c2 = p.c2;
+    constexpr float kLog2e = 1.4426950408889634f;
+    constexpr int CPH = D / 16;           // 16-byte chunks of half a row
     auto wait_warp = [&](int b, uint32_t ph) -> bool {
       return __all_sync(0xffffffffu, wait_bounded(BAR(b), ph, abort_flag, p.status, kDevTimeoutSoftmax, LIM));
     };
+    // This thread's half row of O and its row's LSE, for the item at list round r (loaded
+    // one item ahead of their use).
+    uint4 o_reg[CPH];
+    float lse_reg = INFINITY;
+    auto fetch = [&](int r) {
+      const int idx = bwd_item(r, cta, G);
+      if (idx >= p.items) return;
+      int fbh, fqt, fn;
+      decode(idx, fbh, fqt, fn);
+      const int qrow = fqt * 128 + row;
+      if (qrow < p.L) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.o + (static_cast<long long>(fbh) * p.L + qrow) * D) + CPH * h;
+#pragma unroll
+        for (int i = 0; i < CPH; ++i) o_reg[i] = __ldg(src + i);
+        lse_reg = __ldg(p.lse + static_cast<long long>(fbh) * p.L + qrow);
+      } else {
+#pragma unroll
+        for (int i = 0; i < CPH; ++i) o_reg[i] = make_uint4(0u, 0u, 0u, 0u);
+        lse_reg = INFINITY;
+      }
+    };
     bool ok = true;
     int g = 0, it = 0;
+    fetch(0);  // the first item of this CTA (round 0: bwd_item(0, cta, G) = cta < G <= items)
     for (int r = 0; ok && r * G < p.items; ++r) {
       const int idx = bwd_item(r, cta, G);
       if (idx >= p.items) continue;
       int bh, qt, nsteps;
       decode(idx, bh, qt, nsteps);
-      if (!(ok = wait_warp(C::QB_RFULL, it & 1))) break;
-      const float lrow = stat_s[row], drow = stat_s[128 + row];
-      mbar_arrive(BAR(C::QB_QFREE));  // the statistics buffer may take the next item's
       const int qrow = qt * 128 + row;
+      // Row statistics: D = dO . O, each warpgroup over its half of the row, the halves
+      // added through shared memory; LSE log2(e).  Both go to the workspace.
+      if (!(ok = wait_warp(C::QB_DOFULL, it & 1))) break;
+      float part0 = 0.f, part1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < CPH; i += 2) {
+        part0 += bwd_dot8(ld_shared_v4(bwd_chunk_addr(do_s, C::RCHUNK, row, CPH * h + i)), o_reg[i]);
+        part1 += bwd_dot8(ld_shared_v4(bwd_chunk_addr(do_s, C::RCHUNK, row, CPH * h + i + 1)), o_reg[i + 1]);
+      }
+      dpart[h * 128 + row] = part0 + part1;
+      const float lrow = lse_reg * kLog2e;
+      mbar_arrive(BAR(C::QB_DPART));
+      if (!(ok = wait_warp(C::QB_DPART, it & 1))) break;
+      const float drow = dpart[row] + dpart[128 + row];
+      if (h == 0) {
+        const long long w = static_cast<long long>(bh) * p.Lp + qt * 128 + row;
+        p.ws_lse2[w] = lrow;
+        p.ws_d[w] = drow;
+      }
+      // dO (read above, in the generic proxy) is refilled by TMA once this arrives.
+      fence_proxy_async_smem();
+      mbar_arrive(BAR(C::QB_DOFREE));
+      // The next item's O and LSE, while this item runs.
+      {
+        int rn = r + 1;
+        while (rn * G < p.items && bwd_item(rn, cta, G) >= p.items) ++rn;
+        fetch(rn);
+      }
       for (int s = 0; s < nsteps; ++s, ++g) {
-        const uint32_t pb = (static_cast<uint32_t>(g) >> 1) & 1u;
-        const uint32_t s_col = tmem + lane_base + c_s(g) + 32 * h, dp_col = s_col + 64;
+        const uint32_t s_col = tmem + lane_base + c_s(g) + 64 * h, dp_col = tmem + lane_base + C_DP + 64 * h;
         // P (registers only): P = exp2(S c2 - LSE log2 e), masked where the key comes after
-        // the query or lies past L.
-        if (!(ok = wait_warp(C::QB_SFULL + (g & 1), pb))) break;
+        // the query (diagonal tile) or lies past L.
+        if (!(ok = wait_warp(C::QB_SFULL + (g & 1), (static_cast<uint32_t>(g) >> 1) & 1u))) break;
         tc_fence_after();
-        const int key0 = s * 64 + 32 * h;
-        const bool edge = (CAUSAL && key0 + 31 > qt * 128) || key0 + 32 > p.L;
-        float pv[32];
-        {
+        const int key0 = s * 128 + 64 * h;
+        const bool edge = (CAUSAL && s == qt) || key0 + 64 > p.L;
+        float pv[64];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
           uint32_t sr[32];
-          tmem_ld32x32(s_col, sr);
+          tmem_ld32x32(s_col + 32 * half, sr);
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
+            const int col = 32 * half + c;
             float pp = ex2_approx(fmaf(__uint_as_float(sr[c]), c2, -lrow));
-            if (edge && ((CAUSAL && key0 + c > qrow) || key0 + c >= p.L)) pp = 0.f;
-            pv[c] = pp;
+            if (edge && ((CAUSAL && key0 + col > qrow) || key0 + col >= p.L)) pp = 0.f;
+            pv[col] = pp;
           }
         }
-        // dS = P (dP - D), packed to fp16 into the first 16 of its 32 columns.
-        if (!(ok = wait_warp(C::QB_DPFULL + (g & 1), pb))) break;
+        // dS = P (dP - D), packed to fp16 into the first 32 of its 64 columns.
+        if (!(ok = wait_warp(C::QB_DPFULL, g & 1))) break;
         tc_fence_after();
         {
-          uint32_t dr[32];
-          tmem_ld32x32(dp_col, dr);
-          uint32_t dk[16];
+          uint32_t dk[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            dk[i] = pack_f16x2(pv[2 * i] * (__uint_as_float(dr[2 * i]) - drow),
-                               pv[2 * i + 1] * (__uint_as_float(dr[2 * i + 1]) - drow));
-          tmem_st32x16(dp_col, dk);
+          for (int half = 0; half < 2; ++half) {
+            uint32_t dr[32];
+            tmem_ld32x32(dp_col + 32 * half, dr);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int col = 32 * half + 2 * i;
+              dk[16 * half + i] = pack_f16x2(pv[col] * (__uint_as_float(dr[2 * i]) - drow),
+                                             pv[col + 1] * (__uint_as_float(dr[2 * i + 1]) - drow));
+            }
+          }
+          tmem_st32x32(dp_col, dk);
         }
         tc_fence_before();
-        mbar_arrive(BAR(C::QB_DSFULL + (g & 1)));
+        mbar_arrive(BAR(C::QB_DSFULL));
       }
       if (!ok) break;
       // ---------------------------------------------------------------- epilogue
