@@ -56,6 +56,7 @@ extern "C" {
 #define GBATTN_DEV_TIMEOUT_EPILOGUE 4 /* the epilogue's wait for its staging tile timed out   */
 #define GBATTN_DEV_TIMEOUT_PROBE 5   /* the self-test wait of attn_debug_wait_probe ran out */
 #define GBATTN_DEV_TIMEOUT_MERGE 6   /* attn_decode: waiting for the other CTAs' partials ran out */
+#define GBATTN_DEV_SMEM_ALIGN 7      /* attn_bwd: dynamic shared memory not 1 KB aligned (kernel skipped) */
 
 /*
  * attn_fwd -- the fused forward pass.

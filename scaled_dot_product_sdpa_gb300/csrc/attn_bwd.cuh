@@ -22,18 +22,20 @@
 //     them to a workspace of 8 bytes per query row (the only memory beyond the inputs and
 //     outputs).
 //   attn_bwd_dkdv_kernel: work item = (head, 128-key tile j), K_j and V_j resident, the
-//     query rows streamed in 64-row tiles i together with their row statistics:
-//     S^T = K_j Q_i^T and dP^T = V_j dO_i^T; P^T and dS^T are formed in fp16 over the
-//     same tensor-memory columns; then dV_j += P^T dO_i and dK_j += dS^T Q_i.
+//     query rows streamed in 128-row tiles i (Q, dO and the row statistics in rings of
+//     their own):  S^T = K_j Q_i^T and dP^T = V_j dO_i^T; P^T and dS^T are formed in fp16
+//     over the same tensor-memory columns; then dV_j += P^T dO_i and dK_j += dS^T Q_i.
 // Both recompute P from the forward LSE (no L x L matrix is stored).  The tensor-core
 // operand forms are the forward kernels': K-major A and B from shared memory for the
-// logit-like products (N = 64), A from tensor memory with an MN-major B for the
+// logit-like products (N = 128), A from tensor memory with an MN-major B for the
 // accumulations (N = head_dim).
 //
-// Pipelining: S and dP are double-buffered in tensor memory, so the tensor core computes
-// step s+1's S and dP while the elementwise warps work on step s; the streamed tiles sit
-// in a ring deep enough (4 stages at head_dim 128, 8 at 64) for the loads to run two steps
-// ahead.  Both kernels are persistent: one CTA per SM walks the items longest first, in
+// Pipelining: every step is 128 streamed rows.  In the dQ kernel S is double-buffered in
+// tensor memory, so step s+1's S runs while the elementwise warps work on step s; in the
+// dK/dV kernel (whose tensor memory holds S^T, dP^T, dV and dK) the products are ordered
+// dV(s), S^T(s+1), dK(s), dP^T(s+1), so that each runs while the warps form the next
+// P or dS.  The streamed operands sit in rings deep enough for their loads to run about
+// two steps ahead.  Both kernels are persistent: one CTA per SM walks the items longest first, in
 // "snake" order (CTA b takes items b, 2G-1-b, 2G+b, ... of the sorted list, G = grid size),
 // so that the per-CTA totals even out.  The epilogue writes the accumulators from tensor
 // memory straight to global memory (each thread one row), so the next item's loads are
@@ -52,6 +54,8 @@
 
 namespace gbattn {
 
+constexpr unsigned kDevSmemAlign = 7;  // dynamic shared memory not 1 KB aligned
+
 struct BwdParams {
   const float *lse;        // [BH, L] forward LSE (natural log)
   const __half *o;         // [BH, L, D] forward output
@@ -61,15 +65,14 @@ struct BwdParams {
   long long wait_limit;
   int BH, L;
   int Lp;                  // L rounded up to a multiple of 128 (workspace row stride)
-  int n128, n64;           // ceil(L / 128), ceil(L / 64)
+  int n128;               // ceil(L / 128)
   int items;               // BH * n128 work items per kernel
   float c2;                // scale * log2(e)
   float scale;
 };
 
 struct BwdLaunch {
-  // Resident operands use 128-row boxes, streamed operands 64-row boxes.
-  CUtensorMap tm_q128, tm_do128, tm_k128, tm_v128, tm_q64, tm_do64, tm_k64, tm_v64;
+  CUtensorMap tm_q128, tm_do128, tm_k128, tm_v128;  // 128-row x 64-column boxes
   BwdParams p;
   int grid;  // persistent CTAs (<= items)
   bool causal;
@@ -80,28 +83,28 @@ template <int D>
 struct BwdCfg {
   static constexpr int THREADS = 384;
   static constexpr int NCH = D / 64;                  // 64-column chunks of a tile
-  static constexpr int RCHUNK = 128 * 128;            // resident tile: 128 rows x 64 fp16 columns
+  static constexpr int RCHUNK = 128 * 128;            // a tile: 128 rows x 64 fp16 columns per box
   static constexpr int RTILE = NCH * RCHUNK;
-  static constexpr int SCHUNK = 64 * 128;             // streamed tile: 64 rows x 64 fp16 columns
-  static constexpr int STILE = NCH * SCHUNK;
-  static constexpr int NS = D == 64 ? 8 : 4;          // ring stages
-  static constexpr uint32_t IDESC_S = idesc_f16_f32(128, 64, 0, 0);    // 128 x 64 logit-like
+  static constexpr uint32_t IDESC_S128 = idesc_f16_f32(128, 128, 0, 0);  // 128 x 128 logit-like
   static constexpr uint32_t IDESC_ACC = idesc_f16_f32(128, D, 0, 1);   // B MN-major, N = D
   static constexpr int TMEM_COLS = 512;
-  // dK/dV kernel: [K][V][ring: NS x stage][barriers]; a stage is [Q][dO][LSE log2 e: 64 fp32]
-  // [D: 64 fp32][pad to 1 KB] (the next stage's tiles stay 1 KB aligned for the swizzle).
-  static constexpr int ST_OFF = 2 * STILE;
-  static constexpr int STAGE = 2 * STILE + 1024;
-  static constexpr int KV_OFF_RING = 2 * RTILE;
-  static constexpr int KV_OFF_BAR = KV_OFF_RING + NS * STAGE;
-  static constexpr int KB_KVFULL = 0, KB_IDONE = 1, KB_FULL = 2, KB_EMPTY = 2 + NS, KB_SFULL = 2 + 2 * NS,
-                       KB_DPFULL = KB_SFULL + 2, KB_PFULL = KB_DPFULL + 2, KB_DSFULL = KB_PFULL + 2,
-                       KB_KVFREE = KB_DSFULL + 2, KB_DRAIN = KB_KVFREE + 1, KB_N = KB_DRAIN + 1;
-  static constexpr int KV_SMEM = 1024 + KV_OFF_BAR + 8 * KB_N + 16;
+  // dK/dV kernel (128-query steps): [K][V][Q ring: NQS tiles][dO ring: NDS tiles][row
+  // statistics: 2 x (LSE log2 e: 128 fp32, D: 128 fp32)][barriers].  No alignment slack:
+  // the dynamic shared memory starts 1 KB aligned (checked in the kernel).
+  static constexpr int NQS = D == 64 ? 6 : 3, NDS = D == 64 ? 4 : 2;
+  static constexpr int KV_OFF_Q = 2 * RTILE;
+  static constexpr int KV_OFF_DO = KV_OFF_Q + NQS * RTILE;
+  static constexpr int KV_OFF_ST = KV_OFF_DO + NDS * RTILE;
+  static constexpr int KV_OFF_BAR = KV_OFF_ST + 2 * 1024;
+  static constexpr int KB_KVFULL = 0, KB_KVFREE = 1, KB_IDONE = 2, KB_QFULL = 3, KB_QEMPTY = 3 + NQS,
+                       KB_DOFULL = 3 + 2 * NQS, KB_DOEMPTY = KB_DOFULL + NDS, KB_STFULL = KB_DOEMPTY + NDS,
+                       KB_STEMPTY = KB_STFULL + 2, KB_SFULL = KB_STEMPTY + 2, KB_DPFULL = KB_SFULL + 1,
+                       KB_PFULL = KB_DPFULL + 1, KB_DSFULL = KB_PFULL + 1, KB_DRAIN = KB_DSFULL + 1,
+                       KB_N = KB_DRAIN + 1;
+  static constexpr int KV_SMEM = KV_OFF_BAR + 8 * KB_N + 16;
   // dQ kernel (128-key steps): [Q][dO][K ring: NKS x 128-row tiles][V ring: NVS x 128-row
   // tiles][D halves: 2 x 128 fp32][barriers]
   static constexpr int NKS = D == 64 ? 6 : 3, NVS = D == 64 ? 4 : 2;
-  static constexpr uint32_t IDESC_S128 = idesc_f16_f32(128, 128, 0, 0);
   static constexpr int Q_OFF_K = 2 * RTILE;
   static constexpr int Q_OFF_V = Q_OFF_K + NKS * RTILE;
   static constexpr int Q_OFF_ST = Q_OFF_V + NVS * RTILE;
@@ -126,12 +129,6 @@ __device__ __forceinline__ uint32_t bwd_chunk_addr(uint32_t tile, int chunk, int
 
 // Item index of round r for CTA b of G (snake order over the longest-first list).
 __device__ __forceinline__ int bwd_item(int r, int b, int G) { return r * G + ((r & 1) ? G - 1 - b : b); }
-
-// Tensor-memory column offset of k-step kk (16 of the 64 reduction rows) of a P^T / dS^T /
-// dS operand: the warpgroup of column half h packs its 32 columns into [32 h, 32 h + 16).
-__device__ __forceinline__ uint32_t bwd_a_col(int kk) {
-  return static_cast<uint32_t>((kk >> 1) * 32 + (kk & 1) * 8);
-}
 
 // Sum of the 8 fp16 products of two 16-byte chunks (fp32).
 __device__ __forceinline__ float bwd_dot8(uint4 a, uint4 b) {
@@ -175,10 +172,15 @@ __global__ void __launch_bounds__(384, 1)
                          const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t *const base_ptr = smem_raw + (base - raw);
-  const uint32_t k_s = base, v_s = base + C::RTILE, ring_s = base + C::KV_OFF_RING;
+  const uint32_t base = smem_u32(smem_raw);
+  if (base & 1023u) {  // the layout has no alignment slack (every thread leaves here)
+    if (threadIdx.x == 0) atomicCAS(p.status, 0u, kDevSmemAlign);
+    return;
+  }
+  uint8_t *const base_ptr = smem_raw;
+  const uint32_t k_s = base, v_s = base + C::RTILE, q_ring = base + C::KV_OFF_Q, do_ring = base + C::KV_OFF_DO;
+  float *const stat_s = reinterpret_cast<float *>(base_ptr + C::KV_OFF_ST);  // [2][lse 128 | D 128]
+  const uint32_t stat_a = base + C::KV_OFF_ST;
   const uint32_t bar_s = base + C::KV_OFF_BAR;
   uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + C::KV_OFF_BAR + 8 * C::KB_N);
   volatile uint32_t *const abort_flag = tmem_slot + 1;
@@ -187,29 +189,36 @@ __global__ void __launch_bounds__(384, 1)
   const long long LIM = p.wait_limit;
   const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
   // Item idx: key tile kt of head bh (kt ascending = longest first when causal); its steps
-  // are the 64-row query tiles from q_first on.
+  // are the 128-row query tiles from q_first on.
   auto decode = [&](int idx, int &bh, int &kt, int &q_first, int &nsteps) {
     kt = idx / p.BH;
     bh = idx - kt * p.BH;
-    q_first = CAUSAL ? 2 * kt : 0;
-    nsteps = p.n64 - q_first;
+    q_first = CAUSAL ? kt : 0;
+    nsteps = p.n128 - q_first;
   };
-  auto stage_addr = [&](int gg) -> uint32_t { return ring_s + (gg % C::NS) * C::STAGE; };
+  auto q_tile = [&](int gg) -> uint32_t { return q_ring + (gg % C::NQS) * C::RTILE; };
+  auto do_tile = [&](int gg) -> uint32_t { return do_ring + (gg % C::NDS) * C::RTILE; };
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::KB_KVFULL), 1);
+    mbar_init(BAR(C::KB_KVFREE), 1);
     mbar_init(BAR(C::KB_IDONE), 1);
-    for (int i = 0; i < C::NS; ++i) {
-      mbar_init(BAR(C::KB_FULL + i), 1);
-      mbar_init(BAR(C::KB_EMPTY + i), 1);
+    for (int i = 0; i < C::NQS; ++i) {
+      mbar_init(BAR(C::KB_QFULL + i), 1);
+      mbar_init(BAR(C::KB_QEMPTY + i), 1);
+    }
+    for (int i = 0; i < C::NDS; ++i) {
+      mbar_init(BAR(C::KB_DOFULL + i), 1);
+      mbar_init(BAR(C::KB_DOEMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(BAR(C::KB_SFULL + i), 1);
-      mbar_init(BAR(C::KB_DPFULL + i), 1);
-      mbar_init(BAR(C::KB_PFULL + i), 256);
-      mbar_init(BAR(C::KB_DSFULL + i), 256);
+      mbar_init(BAR(C::KB_STFULL + i), 1);
+      mbar_init(BAR(C::KB_STEMPTY + i), 256);
     }
-    mbar_init(BAR(C::KB_KVFREE), 1);
+    mbar_init(BAR(C::KB_SFULL), 1);
+    mbar_init(BAR(C::KB_DPFULL), 1);
+    mbar_init(BAR(C::KB_PFULL), 256);
+    mbar_init(BAR(C::KB_DSFULL), 256);
     mbar_init(BAR(C::KB_DRAIN), 1);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -228,41 +237,33 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
   grid_launch_dependents();
   grid_wait_prior();
-  // Tensor memory: step buffer b (= global step & 1) holds S^T at [128 b, 128 b + 64) (P^T
-  // packed over its first 16 columns of each 32-column half) and dP^T at [128 b + 64,
-  // 128 b + 128) (dS^T likewise); dV [256, 256+D), dK [256+D, 256+2D).
-  constexpr uint32_t C_DV = 256, C_DK = 256 + D;
-  auto c_s = [](int gg) -> uint32_t { return static_cast<uint32_t>(gg & 1) * 128u; };
+  // Tensor memory: S^T [0,128) (P^T packed into [0,32) and [64,96)), dP^T [128,256) (dS^T
+  // likewise), dV [256, 256+D), dK [256+D, 256+2D).
+  constexpr uint32_t C_S = 0, C_DP = 128, C_DV = 256, C_DK = 256 + D;
+  auto a_col = [](int kk) -> uint32_t { return static_cast<uint32_t>((kk >> 2) * 64 + (kk & 3) * 8); };
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
       bool ok = true;
-      int g = 0, issued = 0, kv_loads = 0;
+      int g = 0, nq = 0, ndo = 0, nst = 0, kv_loads = 0;
       for (int r = 0; ok && r * G < p.items; ++r) {
         const int idx = bwd_item(r, cta, G);
         if (idx >= p.items) continue;
         int bh, kt, q_first, nsteps;
         decode(idx, bh, kt, q_first, nsteps);
         for (int s = 0; s < nsteps; ++s, ++g) {
-          const int st = g % C::NS;
-          if (!(ok = wait_bounded(BAR(C::KB_EMPTY + st), ((g / C::NS) & 1) ^ 1u, abort_flag, p.status, kDevTimeoutLoad,
-                                  LIM)))
+          const int qi = q_first + s;
+          if (!(ok = wait_bounded(BAR(C::KB_QEMPTY + g % C::NQS), ((g / C::NQS) & 1) ^ 1u, abort_flag, p.status,
+                                  kDevTimeoutLoad, LIM)))
             break;
-          const uint32_t stage = stage_addr(g);
-          const long long wrow = static_cast<long long>(bh) * p.Lp + (q_first + s) * 64;
-          mbar_arrive_expect_tx(BAR(C::KB_FULL + st), 2 * C::STILE + 512);
-          for (int c = 0; c < C::NCH; ++c) {
-            tma_load_3d(stage + c * C::SCHUNK, &tm_q, c * 64, (q_first + s) * 64, bh, BAR(C::KB_FULL + st));
-            tma_load_3d(stage + C::STILE + c * C::SCHUNK, &tm_do, c * 64, (q_first + s) * 64, bh, BAR(C::KB_FULL + st));
-          }
-          // The 64 rows' statistics, written by the dQ kernel (byte offsets multiples of 256).
-          bulk_load(stage + C::ST_OFF, p.ws_lse2 + wrow, 256, BAR(C::KB_FULL + st));
-          bulk_load(stage + C::ST_OFF + 256, p.ws_d + wrow, 256, BAR(C::KB_FULL + st));
-          ++issued;
+          mbar_arrive_expect_tx(BAR(C::KB_QFULL + g % C::NQS), C::RTILE);
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(q_tile(g) + c * C::RCHUNK, &tm_q, c * 64, qi * 128, bh, BAR(C::KB_QFULL + g % C::NQS));
+          ++nq;
           if (s == 0) {
             // K and V of this item, once the previous item's last S^T and dP^T products (the
-            // only readers of K and V) are complete: up to two steps before that item ends.
+            // only readers of K and V) are complete.
             if (kv_loads > 0 && !(ok = wait_bounded(BAR(C::KB_KVFREE), (kv_loads - 1) & 1, abort_flag, p.status,
                                                     kDevTimeoutLoad, LIM)))
               break;
@@ -273,12 +274,31 @@ __global__ void __launch_bounds__(384, 1)
             }
             ++kv_loads;
           }
+          if (!(ok = wait_bounded(BAR(C::KB_DOEMPTY + g % C::NDS), ((g / C::NDS) & 1) ^ 1u, abort_flag, p.status,
+                                  kDevTimeoutLoad, LIM)))
+            break;
+          mbar_arrive_expect_tx(BAR(C::KB_DOFULL + g % C::NDS), C::RTILE);
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(do_tile(g) + c * C::RCHUNK, &tm_do, c * 64, qi * 128, bh, BAR(C::KB_DOFULL + g % C::NDS));
+          ++ndo;
+          // The 128 rows' statistics, written by the dQ kernel (byte offsets multiples of 512).
+          if (!(ok = wait_bounded(BAR(C::KB_STEMPTY + (g & 1)), ((g >> 1) & 1) ^ 1u, abort_flag, p.status,
+                                  kDevTimeoutLoad, LIM)))
+            break;
+          const long long wrow = static_cast<long long>(bh) * p.Lp + qi * 128;
+          mbar_arrive_expect_tx(BAR(C::KB_STFULL + (g & 1)), 1024);
+          bulk_load(stat_a + (g & 1) * 1024, p.ws_lse2 + wrow, 512, BAR(C::KB_STFULL + (g & 1)));
+          bulk_load(stat_a + (g & 1) * 1024 + 512, p.ws_d + wrow, 512, BAR(C::KB_STFULL + (g & 1)));
+          ++nst;
         }
       }
       // Drain: every load issued lands before the CTA may exit.
       if (kv_loads > 0) wait_drain(BAR(C::KB_KVFULL), (kv_loads - 1) & 1, LIM);
-      for (int s = issued > C::NS ? issued - C::NS : 0; s < issued; ++s)
-        wait_drain(BAR(C::KB_FULL + s % C::NS), (s / C::NS) & 1, LIM);
+      for (int i = nq > C::NQS ? nq - C::NQS : 0; i < nq; ++i)
+        wait_drain(BAR(C::KB_QFULL + i % C::NQS), (i / C::NQS) & 1, LIM);
+      for (int i = ndo > C::NDS ? ndo - C::NDS : 0; i < ndo; ++i)
+        wait_drain(BAR(C::KB_DOFULL + i % C::NDS), (i / C::NDS) & 1, LIM);
+      for (int i = nst > 2 ? nst - 2 : 0; i < nst; ++i) wait_drain(BAR(C::KB_STFULL + (i & 1)), (i >> 1) & 1, LIM);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -290,71 +310,73 @@ __global__ void __launch_bounds__(384, 1)
         return wait_bounded(BAR(b), ph, abort_flag, p.status, kDevTimeoutMma, LIM);
       };
       const SDesc ka = sdesc_split(sdesc_sw128(k_s, 16, 1024)), va = sdesc_split(sdesc_sw128(v_s, 16, 1024));
-      // S^T = K Q^T and dP^T = V dO^T of global step gg into its buffer (head_dim summed
-      // over its 64-column chunks).
-      auto issue_sdp = [&](int gg) {
-        const uint32_t stage = stage_addr(gg);
-        const SDesc qb = sdesc_split(sdesc_sw128(stage, 16, 1024));
-        const SDesc dob = sdesc_split(sdesc_sw128(stage + C::STILE, 16, 1024));
+      auto q_ready = [&](int gg) { return wait(C::KB_QFULL + gg % C::NQS, (gg / C::NQS) & 1); };
+      auto do_ready = [&](int gg) { return wait(C::KB_DOFULL + gg % C::NDS, (gg / C::NDS) & 1); };
+      // S^T = K Q^T and dP^T = V dO^T of global step gg (head_dim summed over its chunks).
+      auto issue_s = [&](int gg) {
+        const SDesc qb = sdesc_split(sdesc_sw128(q_tile(gg), 16, 1024));
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_ss_off(tmem + c_s(gg), ka, c * C::RCHUNK + kk * 32, qb, c * C::SCHUNK + kk * 32, C::IDESC_S,
+            umma_ss_off(tmem + C_S, ka, c * C::RCHUNK + kk * 32, qb, c * C::RCHUNK + kk * 32, C::IDESC_S128,
                         (c | kk) != 0 ? 1u : 0u);
-        umma_commit(BAR(C::KB_SFULL + (gg & 1)));
-#pragma unroll
-        for (int c = 0; c < C::NCH; ++c)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_ss_off(tmem + c_s(gg) + 64, va, c * C::RCHUNK + kk * 32, dob, c * C::SCHUNK + kk * 32, C::IDESC_S,
-                        (c | kk) != 0 ? 1u : 0u);
-        umma_commit(BAR(C::KB_DPFULL + (gg & 1)));
+        umma_commit(BAR(C::KB_SFULL));
       };
-      auto stage_ready = [&](int gg) { return wait(C::KB_FULL + gg % C::NS, (gg / C::NS) & 1); };
+      auto issue_dp = [&](int gg) {
+        const SDesc dob = sdesc_split(sdesc_sw128(do_tile(gg), 16, 1024));
+#pragma unroll
+        for (int c = 0; c < C::NCH; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_ss_off(tmem + C_DP, va, c * C::RCHUNK + kk * 32, dob, c * C::RCHUNK + kk * 32, C::IDESC_S128,
+                        (c | kk) != 0 ? 1u : 0u);
+        umma_commit(BAR(C::KB_DPFULL));
+      };
       for (int r = 0; ok && r * G < p.items; ++r) {
         const int idx = bwd_item(r, cta, G);
         if (idx >= p.items) continue;
         int bh, kt, q_first, nsteps;
         decode(idx, bh, kt, q_first, nsteps);
-        if (!(ok = wait(C::KB_KVFULL, it & 1) && stage_ready(g))) break;
+        if (!(ok = wait(C::KB_KVFULL, it & 1) && q_ready(g))) break;
         tc_fence_after();
-        issue_sdp(g);
-        if (nsteps > 1) {
-          if (!(ok = stage_ready(g + 1))) break;
-          tc_fence_after();
-          issue_sdp(g + 1);
-        }
-        if (nsteps <= 2) umma_commit(BAR(C::KB_KVFREE));  // the item's last S^T, dP^T are issued
+        issue_s(g);
+        if (!(ok = do_ready(g))) break;
+        tc_fence_after();
+        issue_dp(g);
+        if (nsteps == 1) umma_commit(BAR(C::KB_KVFREE));  // the item's last S^T, dP^T are issued
         for (int s = 0; s < nsteps; ++s, ++g) {
-          const uint32_t stage = stage_addr(g);
-          const uint32_t pb = (static_cast<uint32_t>(g) >> 1) & 1u;
-          // dV += P^T dO
-          if (!(ok = wait(C::KB_PFULL + (g & 1), pb))) break;
+          const bool more = s + 1 < nsteps;
+          // dV += P^T dO; then this step's dO tile is free.
+          if (!(ok = wait(C::KB_PFULL, g & 1))) break;
           tc_fence_after();
-          const SDesc dom = sdesc_split(sdesc_sw128(stage + C::STILE, C::SCHUNK, 1024));
+          const SDesc dom = sdesc_split(sdesc_sw128(do_tile(g), C::RCHUNK, 1024));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_ts_off(tmem + C_DV, tmem + c_s(g) + bwd_a_col(kk), dom, kk * 2048, C::IDESC_ACC,
-                        (s > 0 || kk > 0) ? 1u : 0u);
-          // dK += dS^T Q
-          if (!(ok = wait(C::KB_DSFULL + (g & 1), pb))) break;
-          tc_fence_after();
-          const SDesc qm = sdesc_split(sdesc_sw128(stage, C::SCHUNK, 1024));
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_ts_off(tmem + C_DK, tmem + c_s(g) + 64 + bwd_a_col(kk), qm, kk * 2048, C::IDESC_ACC,
-                        (s > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(BAR(C::KB_EMPTY + g % C::NS));
-          if (s + 2 < nsteps) {
-            if (!(ok = stage_ready(g + 2))) break;
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts_off(tmem + C_DV, tmem + C_S + a_col(kk), dom, kk * 2048, C::IDESC_ACC, (s > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(BAR(C::KB_DOEMPTY + g % C::NDS));
+          if (more) {
+            if (!(ok = q_ready(g + 1))) break;
             tc_fence_after();
-            issue_sdp(g + 2);  // into this step's buffers, read in order after dV, dK above
-            if (s + 3 == nsteps) umma_commit(BAR(C::KB_KVFREE));
+            issue_s(g + 1);  // into S^T, read in order after dV above
+          }
+          // dK += dS^T Q; then this step's Q tile is free.
+          if (!(ok = wait(C::KB_DSFULL, g & 1))) break;
+          tc_fence_after();
+          const SDesc qm = sdesc_split(sdesc_sw128(q_tile(g), C::RCHUNK, 1024));
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts_off(tmem + C_DK, tmem + C_DP + a_col(kk), qm, kk * 2048, C::IDESC_ACC, (s > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(BAR(C::KB_QEMPTY + g % C::NQS));
+          if (more) {
+            if (!(ok = do_ready(g + 1))) break;
+            tc_fence_after();
+            issue_dp(g + 1);  // into dP^T, read in order after dK above
+            if (s + 2 == nsteps) umma_commit(BAR(C::KB_KVFREE));
           }
         }
         if (!ok) break;
-        umma_commit(BAR(C::KB_IDONE));  // K, V free; dV, dK final
+        umma_commit(BAR(C::KB_IDONE));  // dV, dK final
         ++it;
       }
       umma_commit(BAR(C::KB_DRAIN));  // every MMA issued so far is complete
@@ -363,7 +385,7 @@ __global__ void __launch_bounds__(384, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ elementwise warpgroups
-    const int h = (warp - 4) >> 2;        // query columns [32 h, 32 h + 32) of every tile
+    const int h = (warp - 4) >> 2;        // query columns [64 h, 64 h + 64) of every tile
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;  // key row of the tile == tensor-memory lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
@@ -379,51 +401,58 @@ __global__ void __launch_bounds__(384, 1)
       int bh, kt, q_first, nsteps;
       decode(idx, bh, kt, q_first, nsteps);
       for (int s = 0; s < nsteps; ++s, ++g) {
-        const int st = g % C::NS;
-        const uint32_t pb = (static_cast<uint32_t>(g) >> 1) & 1u;
-        const uint32_t s_col = tmem + lane_base + c_s(g) + 32 * h, dp_col = s_col + 64;
-        const float *const lse_h = reinterpret_cast<const float *>(base_ptr + (stage_addr(g) - base) + C::ST_OFF) + 32 * h;
-        const float *const dd_h = lse_h + 64;
-        // The stage (its statistics included) has landed: the S^T of this step is computed from it.
-        if (!(ok = wait_warp(C::KB_SFULL + (g & 1), pb) && wait_warp(C::KB_FULL + st, (g / C::NS) & 1))) break;
+        const float *const lse_h = stat_s + (g & 1) * 256 + 64 * h;
+        const float *const dd_h = lse_h + 128;
+        const uint32_t s_col = tmem + lane_base + C_S + 64 * h, dp_col = tmem + lane_base + C_DP + 64 * h;
+        if (!(ok = wait_warp(C::KB_SFULL, g & 1) && wait_warp(C::KB_STFULL + (g & 1), (g >> 1) & 1))) break;
         tc_fence_after();
-        // P phase: P^T = exp2(S^T c2 - LSE log2 e), masked on the two diagonal query tiles
-        // (query before key), packed to fp16 into the first 16 of its 32 columns.
-        const bool diag = CAUSAL && s < 2;
-        float pv[32];
-        {
+        // P phase: P^T = exp2(S^T c2 - LSE log2 e), masked on the diagonal tile (query
+        // before key), packed to fp16 into the first 32 of its 64 columns.
+        const bool diag = CAUSAL && s == 0;
+        float pv[64];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
           uint32_t sr[32];
-          tmem_ld32x32(s_col, sr);
+          tmem_ld32x32(s_col + 32 * half, sr);
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            float pp = ex2_approx(fmaf(__uint_as_float(sr[c]), c2, -lse_h[c]));
-            if (diag && s * 64 + 32 * h + c < row) pp = 0.f;
-            pv[c] = pp;
+            const int col = 32 * half + c;
+            float pp = ex2_approx(fmaf(__uint_as_float(sr[c]), c2, -lse_h[col]));
+            if (diag && 64 * h + col < row) pp = 0.f;
+            pv[col] = pp;
           }
-          uint32_t pk[16];
+        }
+        {
+          uint32_t pk[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_f16x2(pv[2 * i], pv[2 * i + 1]);
-          tmem_st32x16(s_col, pk);
+          for (int i = 0; i < 32; ++i) pk[i] = pack_f16x2(pv[2 * i], pv[2 * i + 1]);
+          tmem_st32x32(s_col, pk);
         }
         tc_fence_before();
-        mbar_arrive(BAR(C::KB_PFULL + (g & 1)));
+        mbar_arrive(BAR(C::KB_PFULL));
         // dS phase: dS^T = P^T (dP^T - D), packed likewise.
-        if (!(ok = wait_warp(C::KB_DPFULL + (g & 1), pb))) break;
+        if (!(ok = wait_warp(C::KB_DPFULL, g & 1))) break;
         tc_fence_after();
         {
-          uint32_t dr[32];
-          tmem_ld32x32(dp_col, dr);
-          uint32_t dk[16];
+          uint32_t dk[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            dk[i] = pack_f16x2(pv[2 * i] * (__uint_as_float(dr[2 * i]) - dd_h[2 * i]),
-                               pv[2 * i + 1] * (__uint_as_float(dr[2 * i + 1]) - dd_h[2 * i + 1]));
-          tmem_st32x16(dp_col, dk);
+          for (int half = 0; half < 2; ++half) {
+            uint32_t dr[32];
+            tmem_ld32x32(dp_col + 32 * half, dr);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int col = 32 * half + 2 * i;
+              dk[16 * half + i] = pack_f16x2(pv[col] * (__uint_as_float(dr[2 * i]) - dd_h[col]),
+                                             pv[col + 1] * (__uint_as_float(dr[2 * i + 1]) - dd_h[col + 1]));
+            }
+          }
+          tmem_st32x32(dp_col, dk);
         }
         tc_fence_before();
-        // The statistics read above sit in a stage that TMA refills once it is released.
+        // The statistics read above are refilled by a bulk copy (async proxy).
         fence_proxy_async_smem();
-        mbar_arrive(BAR(C::KB_DSFULL + (g & 1)));
+        mbar_arrive(BAR(C::KB_STEMPTY + (g & 1)));
+        mbar_arrive(BAR(C::KB_DSFULL));
       }
       if (!ok) break;
       // ---------------------------------------------------------------- epilogue

@@ -560,9 +560,7 @@ extern "C" int attn_bwd(const void *q, const void *k, const void *v, const void 
   BwdLaunch a;
   const int bh = static_cast<int>(BH);
   if (encode_bhld(&a.tm_q128, q, bh, L, d) || encode_bhld(&a.tm_do128, dout, bh, L, d) ||
-      encode_bhld(&a.tm_k128, k, bh, L, d) || encode_bhld(&a.tm_v128, v, bh, L, d) ||
-      encode_bhld(&a.tm_q64, q, bh, L, d, 64) || encode_bhld(&a.tm_do64, dout, bh, L, d, 64) ||
-      encode_bhld(&a.tm_k64, k, bh, L, d, 64) || encode_bhld(&a.tm_v64, v, bh, L, d, 64))
+      encode_bhld(&a.tm_k128, k, bh, L, d) || encode_bhld(&a.tm_v128, v, bh, L, d))
     return GBATTN_ERR_TENSORMAP;
   a.p.lse = lse;
   a.p.o = static_cast<const __half *>(o);
@@ -574,7 +572,6 @@ extern "C" int attn_bwd(const void *q, const void *k, const void *v, const void 
   a.p.BH = bh;
   a.p.L = L;
   a.p.n128 = (L + 127) / 128;
-  a.p.n64 = (L + 63) / 64;
   a.p.Lp = a.p.n128 * 128;
   a.p.ws_lse2 = static_cast<float *>(workspace);
   a.p.ws_d = a.p.ws_lse2 + static_cast<long long>(bh) * a.p.Lp;
@@ -723,6 +720,7 @@ extern "C" const char *attn_strerror(int code) {
     case GBATTN_DEV_TIMEOUT_EPILOGUE: return "device: the epilogue's wait timed out";
     case GBATTN_DEV_TIMEOUT_PROBE: return "device: the wait-probe barrier timed out (expected)";
     case GBATTN_DEV_TIMEOUT_MERGE: return "device: decode's wait for the other CTAs' partial results timed out";
+    case GBATTN_DEV_SMEM_ALIGN: return "device: the backward kernel's shared memory was not 1 KB aligned; it did nothing";
     default: return "unknown gbattn status code";
   }
 }
