@@ -726,7 +726,7 @@ __global__ void __launch_bounds__(384, 1)
     };
     bool ok = true;
     int g = 0, it = 0;
-    fetch(0);  // the first item of this CTA (round 0: bwd_item(0, cta, G) = cta < G <= items)
+    fetch(0);  // this CTA's first item: bwd_item(0, cta, G) = cta < G <= items
     for (int r = 0; ok && r * G < p.items; ++r) {
       const int idx = bwd_item(r, cta, G);
       if (idx >= p.items) continue;
