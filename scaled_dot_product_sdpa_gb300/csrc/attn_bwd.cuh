@@ -14,10 +14,9 @@
 // save; here no atomics are used at all: two kernels, one per output side, run in this
 // order:
 //
-//   attn_bwd_dq_kernel: work item = (head, 128-query tile i), Q_i and dO_i resident (Q in
-//     two buffers, so that the next item's loads early), the key rows streamed in 64-row
-//     tiles j:  S = Q_i K_j^T and dP = dO_i V_j^T on the tensor core; dS is formed; then
-//     dQ_i += dS K_j.  Its elementwise warps also form the row statistics LSE_i log2(e)
+//   attn_bwd_dq_kernel: work item = (head, 128-query tile i), Q_i and dO_i resident, the
+//     key rows streamed in 128-row tiles j (K and V in rings of their own):  S = Q_i K_j^T
+//     and dP = dO_i V_j^T on the tensor core; dS is formed; then dQ_i += dS K_j.  Its elementwise warps also form the row statistics LSE_i log2(e)
 //     and D_i = dO_i . O_i (O and LSE read from global memory one item ahead) and write
 //     them to a workspace of 8 bytes per query row (the only memory beyond the inputs and
 //     outputs).
@@ -35,15 +34,15 @@
 // dK/dV kernel (whose tensor memory holds S^T, dP^T, dV and dK) the products are ordered
 // dV(s), S^T(s+1), dK(s), dP^T(s+1), so that each runs while the warps form the next
 // P or dS.  The streamed operands sit in rings deep enough for their loads to run about
-// two steps ahead.  Both kernels are persistent: one CTA per SM walks the items longest first, in
-// "snake" order (CTA b takes items b, 2G-1-b, 2G+b, ... of the sorted list, G = grid size),
-// so that the per-CTA totals even out.  The epilogue writes the accumulators from tensor
+// two steps ahead.  Both kernels are persistent: one CTA per SM walks the items longest
+// first, in "snake" order (CTA b takes items b, 2G-1-b, 2G+b, ... of the sorted list,
+// G = grid size), so that the per-CTA totals even out.  The epilogue writes the accumulators from tensor
 // memory straight to global memory (each thread one row), so the next item's loads are
 // not held up by a staging buffer.
 //
 // Warp roles (384 threads): warp 0 TMA producer; warp 1 tensor-memory owner and MMA
 // issuer; warps 2-3 idle; warps 4-7 and 8-11 two elementwise warpgroups, each taking one
-// half of the 64 columns of every S / dP tile (and, in the dQ kernel, one half of every
+// half of the 128 columns of every S / dP tile (and, in the dQ kernel, one half of every
 // row of the row statistics), and the epilogue.
 // Every wait is bounded (about two seconds of SM clock), as in the forward kernels.
 #pragma once
