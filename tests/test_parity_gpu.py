@@ -314,3 +314,25 @@ def test_dsplit_repeats_bitwise_and_replays_from_a_graph():
     o3, l3 = _run(q, k, v, True, w.scale, flags=gb.FLAG_SINGLE_TILE)
     assert (o3.float() - o1.float()).abs().max().item() < 2e-2
     assert (l3 - l1).abs().max().item() < 1e-3
+
+
+@pytest.mark.parametrize("flags", [0, 4, 2], ids=["auto", "two_tile", "single_tile"])
+@pytest.mark.parametrize("B,H,L,d,causal", [(1, 2, 16384, 128, True), (1, 1, 8192, 64, False)])
+def test_long_sequence_matches_oracle_on_sampled_rows(B, H, L, d, causal, flags):
+    """Long rows: a query tile's loop runs over up to 128 key tiles (the running maximum,
+    the lazy rescale and the ring wrap around many times).  Sampled rows -- the first and
+    last of every head, rows around tile boundaries, random rows -- against the oracle;
+    every row finite and bounded by max |v| (a convex combination of value rows)."""
+    seed = 5 + L + d
+    q, k, v = inputs.qkv(B, H, L, d, seed)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(*_dev(q, k, v), causal, scale, flags=flags)
+    o, lse = o.reshape(B * H * L, d).cpu(), lse.reshape(B * H * L).cpu()
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    assert o.float().abs().max() <= v.float().abs().max() * (1 + 2e-3)
+    rng = np.random.default_rng(seed)
+    picks = {0, 127, 128, L - 129, L - 128, L - 1} | set(rng.integers(0, L, 24).tolist())
+    rows = sorted(h * L + i for h in range(B * H) for i in picks)
+    o_ref, lse_ref, _ = oracle.sdpa_fwd_rows(q, k, v, causal, float(np.float32(scale)), rows)
+    sel = torch.tensor(rows)
+    _check(o[sel], lse[sel], o_ref, lse_ref, f"{B}x{H}x{L}x{d} causal={causal}")
