@@ -124,3 +124,11 @@ def test_bwd_workspace_contents_do_not_matter():
     assert all(torch.equal(x, y) for x, y in zip(got, ref))
     with pytest.raises(ValueError):
         gb.attn_bwd(q, k, v, o, lse, do, causal=True, workspace=ws[:16])
+
+
+def test_bwd_long_sequence_matches_oracle():
+    """One head of 4096 rows, causal: the longest items run 32 steps (every ring wraps many
+    times within an item, and the dQ items of the last query tiles stream every key tile)."""
+    B, H, L, d = 1, 1, 4096, 128
+    got, ref = _grads(B, H, L, d, True, seed=4096)
+    _check(got, ref, f"{B}x{H}x{L}x{d} causal")
