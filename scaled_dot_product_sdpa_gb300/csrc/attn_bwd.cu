@@ -23,9 +23,11 @@ cudaError_t launch_bwd_variant(const BwdLaunch &a) {
     if (dev < 31) configured_mask |= (1 << dev);
   }
   // The dQ kernel first: it writes the row statistics the dK/dV kernel reads.
-  e = launch_pdl(kdq, a.grid, C::THREADS, C::Q_SMEM, a.stream, a.tm_q128, a.tm_k128, a.tm_v128, a.tm_do128, a.p);
+  e = launch_pdl(kdq, a.grid, C::THREADS, C::Q_SMEM, a.stream, a.tm_q128, a.tm_k128, a.tm_v128, a.tm_do128,
+                 a.tm_dq128, a.p);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kdkdv, a.grid, C::THREADS, C::KV_SMEM, a.stream, a.tm_q128, a.tm_k128, a.tm_v128, a.tm_do128, a.p);
+  return launch_pdl(kdkdv, a.grid, C::THREADS, C::KV_SMEM, a.stream, a.tm_q128, a.tm_k128, a.tm_v128, a.tm_do128,
+                    a.tm_dk128, a.tm_dv128, a.p);
 }
 
 cudaError_t launch_bwd_64(const BwdLaunch &a) {

@@ -16,10 +16,10 @@
 //
 //   attn_bwd_dq_kernel: work item = (head, 128-query tile i), Q_i and dO_i resident, the
 //     key rows streamed in 128-row tiles j (K and V in rings of their own):  S = Q_i K_j^T
-//     and dP = dO_i V_j^T on the tensor core; dS is formed; then dQ_i += dS K_j.  Its elementwise warps also form the row statistics LSE_i log2(e)
-//     and D_i = dO_i . O_i (O and LSE read from global memory one item ahead) and write
-//     them to a workspace of 8 bytes per query row (the only memory beyond the inputs and
-//     outputs).
+//     and dP = dO_i V_j^T on the tensor core; dS is formed; then dQ_i += dS K_j.  Its
+//     elementwise warps also form the row statistics LSE_i log2(e) and D_i = dO_i . O_i
+//     (O and LSE read from global memory one item ahead) and write them to a workspace
+//     of 8 bytes per query row (the only memory beyond the inputs and outputs).
 //   attn_bwd_dkdv_kernel: work item = (head, 128-key tile j), K_j and V_j resident, the
 //     query rows streamed in 128-row tiles i (Q, dO and the row statistics in rings of
 //     their own):  S^T = K_j Q_i^T and dP^T = V_j dO_i^T; P^T and dS^T are formed in fp16
@@ -36,9 +36,11 @@
 // P or dS.  The streamed operands sit in rings deep enough for their loads to run about
 // two steps ahead.  Both kernels are persistent: one CTA per SM walks the items longest
 // first, in "snake" order (CTA b takes items b, 2G-1-b, 2G+b, ... of the sorted list,
-// G = grid size), so that the per-CTA totals even out.  The epilogue writes the accumulators from tensor
-// memory straight to global memory (each thread one row), so the next item's loads are
-// not held up by a staging buffer.
+// G = grid size), so that the per-CTA totals even out.  The epilogue stages the
+// accumulators (fp16) in the ring slots of the item's last step, which its last products
+// have just released, and writes them out by TMA store; the producer refills such a slot
+// once the store has read it.  (Each thread storing its own row to global memory made 32
+// partial-line writes per instruction and cost 1.5 to 3 us per item.)
 //
 // Warp roles (384 threads): warp 0 TMA producer; warp 1 tensor-memory owner and MMA
 // issuer; warps 2-3 idle; warps 4-7 and 8-11 two elementwise warpgroups, each taking one
@@ -58,7 +60,6 @@ constexpr unsigned kDevSmemAlign = 7;  // dynamic shared memory not 1 KB aligned
 struct BwdParams {
   const float *lse;        // [BH, L] forward LSE (natural log)
   const __half *o;         // [BH, L, D] forward output
-  __half *dq, *dk, *dv;    // [BH, L, D] outputs
   float *ws_lse2, *ws_d;   // workspace [BH, Lp] each: LSE log2(e) (+inf past L) and D
   unsigned *status;
   long long wait_limit;
@@ -72,6 +73,7 @@ struct BwdParams {
 
 struct BwdLaunch {
   CUtensorMap tm_q128, tm_do128, tm_k128, tm_v128;  // 128-row x 64-column boxes
+  CUtensorMap tm_dq128, tm_dk128, tm_dv128;         // the outputs, same boxes (TMA stores)
   BwdParams p;
   int grid;  // persistent CTAs (<= items)
   bool causal;
@@ -99,7 +101,10 @@ struct BwdCfg {
                        KB_DOFULL = 3 + 2 * NQS, KB_DOEMPTY = KB_DOFULL + NDS, KB_STFULL = KB_DOEMPTY + NDS,
                        KB_STEMPTY = KB_STFULL + 2, KB_SFULL = KB_STEMPTY + 2, KB_DPFULL = KB_SFULL + 1,
                        KB_PFULL = KB_DPFULL + 1, KB_DSFULL = KB_PFULL + 1, KB_DRAIN = KB_DSFULL + 1,
-                       KB_N = KB_DRAIN + 1;
+                       KB_STGQ = KB_DRAIN + 1, KB_STGDO = KB_STGQ + NQS, KB_STAGED = KB_STGDO + NDS,
+                       KB_N = KB_STAGED + 1;
+  // STGQ / STGDO: the epilogue's TMA stores have read the Q / dO slot it staged dK / dV in
+  // (one per slot); STAGED: every elementwise thread has written its row of the staged tiles.
   static constexpr int KV_SMEM = KV_OFF_BAR + 8 * KB_N + 16;
   // dQ kernel (128-key steps): [Q][dO][K ring: NKS x 128-row tiles][V ring: NVS x 128-row
   // tiles][D halves: 2 x 128 fp32][barriers]
@@ -111,7 +116,10 @@ struct BwdCfg {
   static constexpr int QB_QFULL = 0, QB_QFREE = 1, QB_DOFULL = 2, QB_DOFREE = 3, QB_DPART = 4, QB_IDONE = 5,
                        QB_KFULL = 6, QB_KEMPTY = 6 + NKS, QB_VFULL = 6 + 2 * NKS, QB_VEMPTY = QB_VFULL + NVS,
                        QB_SFULL = QB_VEMPTY + NVS, QB_DPFULL = QB_SFULL + 2, QB_DSFULL = QB_DPFULL + 1,
-                       QB_DRAIN = QB_DSFULL + 1, QB_N = QB_DRAIN + 1;
+                       QB_DRAIN = QB_DSFULL + 1, QB_STGK = QB_DRAIN + 1, QB_STAGED = QB_STGK + NKS,
+                       QB_N = QB_STAGED + 1;
+  // STGK: the epilogue's TMA store has read the K slot it staged dQ in (one per slot);
+  // STAGED: every elementwise thread has written its row of the staged tile.
   // DOFREE: the dO buffer may be refilled: the MMA warp's commit after the item's last dP
   // product and every elementwise thread (done reading dO for D).
   static constexpr int DOFREE_COUNT = 1 + 256;
@@ -143,23 +151,29 @@ __device__ __forceinline__ float bwd_dot8(uint4 a, uint4 b) {
   return acc0 + acc1;
 }
 
-// Epilogue: NC columns of an fp32 accumulator row in tensor memory, times `mult`, to fp16
-// at `dst` (row-contiguous, 16-byte aligned).  The loads are warp-collective; the stores
-// happen only where `store`.
+// Epilogue staging: NC columns of an fp32 accumulator row in tensor memory, times `mult`,
+// to fp16 in row r of a shared-memory tile laid out as the TMA boxes (`chunk` bytes per
+// 64-column box, 128-byte swizzle) from 16-byte unit u0 on; a TMA store then writes the
+// tile out with whole-line transactions (a thread per row storing to global memory
+// directly would touch 32 rows per instruction).
 template <int NC>
-__device__ __forceinline__ void bwd_store_row(uint32_t acc_tmem, __half *dst, float mult, bool store) {
+__device__ __forceinline__ void bwd_stage_row(uint32_t acc_tmem, uint32_t tile, int chunk, int r, int u0,
+                                              float mult) {
+  constexpr int W = NC % 64 == 0 ? 64 : 32;  // columns per tensor-memory load
 #pragma unroll 1
-  for (int c32 = 0; c32 < NC / 32; ++c32) {
-    uint32_t r[32];
-    tmem_ld32x32(acc_tmem + c32 * 32, r);
-    uint32_t h[16];
+  for (int cw = 0; cw < NC / W; ++cw) {
+    uint32_t v[W];
+    if constexpr (W == 64)
+      tmem_ld32x64(acc_tmem + cw * W, v);
+    else
+      tmem_ld32x32(acc_tmem + cw * W, v);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) h[i] = pack_f16x2(__uint_as_float(r[2 * i]) * mult, __uint_as_float(r[2 * i + 1]) * mult);
-    if (store) {
-      uint4 *out = reinterpret_cast<uint4 *>(dst + c32 * 32);
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) out[q4] = make_uint4(h[4 * q4], h[4 * q4 + 1], h[4 * q4 + 2], h[4 * q4 + 3]);
-    }
+    for (int q4 = 0; q4 < W / 8; ++q4)
+      st_shared_v4(bwd_chunk_addr(tile, chunk, r, u0 + (W / 8) * cw + q4),
+                   pack_f16x2(__uint_as_float(v[8 * q4]) * mult, __uint_as_float(v[8 * q4 + 1]) * mult),
+                   pack_f16x2(__uint_as_float(v[8 * q4 + 2]) * mult, __uint_as_float(v[8 * q4 + 3]) * mult),
+                   pack_f16x2(__uint_as_float(v[8 * q4 + 4]) * mult, __uint_as_float(v[8 * q4 + 5]) * mult),
+                   pack_f16x2(__uint_as_float(v[8 * q4 + 6]) * mult, __uint_as_float(v[8 * q4 + 7]) * mult));
   }
 }
 
@@ -168,6 +182,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                          const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -219,12 +234,17 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(BAR(C::KB_PFULL), 256);
     mbar_init(BAR(C::KB_DSFULL), 256);
     mbar_init(BAR(C::KB_DRAIN), 1);
+    for (int i = 0; i < C::NQS; ++i) mbar_init(BAR(C::KB_STGQ + i), 1);
+    for (int i = 0; i < C::NDS; ++i) mbar_init(BAR(C::KB_STGDO + i), 1);
+    mbar_init(BAR(C::KB_STAGED), 256);
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dk);
+    tma_prefetch_desc(&tm_dv);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -246,6 +266,17 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       bool ok = true;
       int g = 0, nq = 0, ndo = 0, nst = 0, kv_loads = 0;
+      // The epilogue stages dK and dV in the Q and dO slots of its item's last step: such a
+      // slot is refilled only once the TMA stores have read it.  Bit b of stg_pend: slot b
+      // (Q slots from bit 0, dO slots from bit 8) awaits that; of stg_par: the phase.
+      uint32_t stg_pend = 0u, stg_par = 0u;
+      auto stage_read = [&](int b, int bar) -> bool {
+        if (!((stg_pend >> b) & 1u)) return true;
+        const uint32_t ph = (stg_par >> b) & 1u;
+        stg_pend &= ~(1u << b);
+        stg_par ^= 1u << b;
+        return wait_bounded(BAR(bar), ph, abort_flag, p.status, kDevTimeoutLoad, LIM);
+      };
       for (int r = 0; ok && r * G < p.items; ++r) {
         const int idx = bwd_item(r, cta, G);
         if (idx >= p.items) continue;
@@ -254,7 +285,8 @@ __global__ void __launch_bounds__(384, 1)
         for (int s = 0; s < nsteps; ++s, ++g) {
           const int qi = q_first + s;
           if (!(ok = wait_bounded(BAR(C::KB_QEMPTY + g % C::NQS), ((g / C::NQS) & 1) ^ 1u, abort_flag, p.status,
-                                  kDevTimeoutLoad, LIM)))
+                                  kDevTimeoutLoad, LIM) &&
+                     stage_read(g % C::NQS, C::KB_STGQ + g % C::NQS)))
             break;
           mbar_arrive_expect_tx(BAR(C::KB_QFULL + g % C::NQS), C::RTILE);
           for (int c = 0; c < C::NCH; ++c)
@@ -274,7 +306,8 @@ __global__ void __launch_bounds__(384, 1)
             ++kv_loads;
           }
           if (!(ok = wait_bounded(BAR(C::KB_DOEMPTY + g % C::NDS), ((g / C::NDS) & 1) ^ 1u, abort_flag, p.status,
-                                  kDevTimeoutLoad, LIM)))
+                                  kDevTimeoutLoad, LIM) &&
+                     stage_read(8 + g % C::NDS, C::KB_STGDO + g % C::NDS)))
             break;
           mbar_arrive_expect_tx(BAR(C::KB_DOFULL + g % C::NDS), C::RTILE);
           for (int c = 0; c < C::NCH; ++c)
@@ -290,6 +323,7 @@ __global__ void __launch_bounds__(384, 1)
           bulk_load(stat_a + (g & 1) * 1024 + 512, p.ws_d + wrow, 512, BAR(C::KB_STFULL + (g & 1)));
           ++nst;
         }
+        stg_pend |= (1u << ((g - 1) % C::NQS)) | (1u << (8 + (g - 1) % C::NDS));
       }
       // Drain: every load issued lands before the CTA may exit.
       if (kv_loads > 0) wait_drain(BAR(C::KB_KVFULL), (kv_loads - 1) & 1, LIM);
@@ -394,6 +428,11 @@ __global__ void __launch_bounds__(384, 1)
     };
     bool ok = true;
     int g = 0, it = 0;
+    // Thread (warp 4, lane 0) issues the epilogue's TMA stores; it hands their slots back
+    // to the producer (once the stores have read them) during the next item's first step,
+    // so that the read does not hold up that step.  stg_gl: last step of the item whose
+    // slots are still held, or -1.
+    int stg_gl = -1;
     for (int r = 0; ok && r * G < p.items; ++r) {
       const int idx = bwd_item(r, cta, G);
       if (idx >= p.items) continue;
@@ -429,6 +468,12 @@ __global__ void __launch_bounds__(384, 1)
         }
         tc_fence_before();
         mbar_arrive(BAR(C::KB_PFULL));
+        if (stg_gl >= 0) {  // only the storing thread holds slots
+          bulk_wait_read0();
+          mbar_arrive(BAR(C::KB_STGQ + stg_gl % C::NQS));
+          mbar_arrive(BAR(C::KB_STGDO + stg_gl % C::NDS));
+          stg_gl = -1;
+        }
         // dS phase: dS^T = P^T (dP^T - D), packed likewise.
         if (!(ok = wait_warp(C::KB_DPFULL, g & 1))) break;
         tc_fence_after();
@@ -455,16 +500,32 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok) break;
       // ---------------------------------------------------------------- epilogue
-      // Warpgroup 0 writes dV, warpgroup 1 writes scale * dK, one key row per thread.
+      // Warpgroup 0 stages dV in the dO slot of the item's last step, warpgroup 1 stages
+      // scale * dK in its Q slot (both free once the item's last products are complete), one
+      // key row per thread; one thread then stores both tiles by TMA (rows past L clipped).
       if (!(ok = wait_warp(C::KB_IDONE, it & 1))) break;
       tc_fence_after();
-      const int krow = kt * 128 + row;
-      __half *const dst = (h == 0 ? p.dv : p.dk) + (static_cast<long long>(bh) * p.L + krow) * D;
-      bwd_store_row<D>(tmem + lane_base + (h == 0 ? C_DV : C_DK), dst, h == 0 ? 1.0f : p.scale,
-                       krow < p.L && *abort_flag == 0u);
+      const int gl = g - 1;
+      bwd_stage_row<D>(tmem + lane_base + (h == 0 ? C_DV : C_DK), h == 0 ? do_tile(gl) : q_tile(gl), C::RCHUNK,
+                       row, 0, h == 0 ? 1.0f : p.scale);
       tc_fence_before();
+      fence_proxy_async_smem();  // the staged rows are read by TMA (async proxy)
+      mbar_arrive(BAR(C::KB_STAGED));
+      if (warp == 4 && lane == 0) {
+        ok = wait_bounded(BAR(C::KB_STAGED), it & 1, abort_flag, p.status, kDevTimeoutSoftmax, LIM);
+        if (ok && *abort_flag == 0u) {
+          for (int c = 0; c < C::NCH; ++c) {
+            tma_store_3d(&tm_dv, do_tile(gl) + c * C::RCHUNK, c * 64, kt * 128, bh);
+            tma_store_3d(&tm_dk, q_tile(gl) + c * C::RCHUNK, c * 64, kt * 128, bh);
+          }
+          bulk_commit();
+        }
+        stg_gl = gl;
+      }
+      if (warp == 4) ok = __shfl_sync(0xffffffffu, ok, 0);
       ++it;
     }
+    if (warp == 4 && lane == 0) bulk_wait0();  // the stores are complete before the CTA exits
   }
   tc_fence_before();
   __syncthreads();
@@ -481,7 +542,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -527,12 +588,15 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(BAR(C::QB_DPFULL), 1);
     mbar_init(BAR(C::QB_DSFULL), 256);
     mbar_init(BAR(C::QB_DRAIN), 1);
+    for (int i = 0; i < C::NKS; ++i) mbar_init(BAR(C::QB_STGK + i), 1);
+    mbar_init(BAR(C::QB_STAGED), 256);
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dq);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -556,6 +620,17 @@ __global__ void __launch_bounds__(384, 1)
       bool ok = true;
       int g = 0, nk = 0, nv = 0, it = 0;  // K and V tiles issued, items whose Q and dO are issued
       bool q_pending = false;              // this item's Q is issued, its dO not yet
+      // The epilogue stages dQ in the K slot of its item's last step: such a slot is refilled
+      // only once the TMA store has read it.  Bit b of stg_pend: slot b awaits that; of
+      // stg_par: the phase.
+      uint32_t stg_pend = 0u, stg_par = 0u;
+      auto stage_read = [&](int b) -> bool {
+        if (!((stg_pend >> b) & 1u)) return true;
+        const uint32_t ph = (stg_par >> b) & 1u;
+        stg_pend &= ~(1u << b);
+        stg_par ^= 1u << b;
+        return wait_bounded(BAR(C::QB_STGK + b), ph, abort_flag, p.status, kDevTimeoutLoad, LIM);
+      };
       for (int r = 0; ok && r * G < p.items; ++r) {
         const int idx = bwd_item(r, cta, G);
         if (idx >= p.items) continue;
@@ -563,7 +638,8 @@ __global__ void __launch_bounds__(384, 1)
         decode(idx, bh, qt, nsteps);
         for (int s = 0; s < nsteps; ++s, ++g) {
           if (!(ok = wait_bounded(BAR(C::QB_KEMPTY + g % C::NKS), ((g / C::NKS) & 1) ^ 1u, abort_flag, p.status,
-                                  kDevTimeoutLoad, LIM)))
+                                  kDevTimeoutLoad, LIM) &&
+                     stage_read(g % C::NKS)))
             break;
           mbar_arrive_expect_tx(BAR(C::QB_KFULL + g % C::NKS), C::RTILE);
           for (int c = 0; c < C::NCH; ++c)
@@ -596,6 +672,7 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_3d(v_tile(g) + c * C::RCHUNK, &tm_v, c * 64, s * 128, bh, BAR(C::QB_VFULL + g % C::NVS));
           ++nv;
         }
+        stg_pend |= 1u << ((g - 1) % C::NKS);
       }
       // Drain: every load issued lands before the CTA may exit.
       if (it + (q_pending ? 1 : 0) > 0) wait_drain(BAR(C::QB_QFULL), (it + (q_pending ? 1 : 0) - 1) & 1, LIM);
@@ -702,29 +779,35 @@ __global__ void __launch_bounds__(384, 1)
     auto wait_warp = [&](int b, uint32_t ph) -> bool {
       return __all_sync(0xffffffffu, wait_bounded(BAR(b), ph, abort_flag, p.status, kDevTimeoutSoftmax, LIM));
     };
-    // This thread's half row of O and its row's LSE, for the item at list round r (loaded
-    // one item ahead of their use).
+    // O and LSE for the item at list round r, loaded one item ahead of their use.  O is read
+    // coalesced: of the 32 x CPH 16-byte chunks of this warp's 32 rows (half h of each),
+    // this thread holds chunks q = i 32 + lane (row q / CPH, chunk q % CPH of the half), so
+    // that one load instruction covers whole line segments; LSE is this thread's own row.
+    // The loads are unconditional (item and row clamped into range; o_valid marks a row
+    // below L), so that nothing waits for them before their use.
     uint4 o_reg[CPH];
-    float lse_reg = INFINITY;
+    float lse_reg;
+    bool o_valid;
     auto fetch = [&](int r) {
-      const int idx = bwd_item(r, cta, G);
-      if (idx >= p.items) return;
       int fbh, fqt, fn;
-      decode(idx, fbh, fqt, fn);
-      const int qrow = fqt * 128 + row;
-      if (qrow < p.L) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.o + (static_cast<long long>(fbh) * p.L + qrow) * D) + CPH * h;
+      decode(min(bwd_item(r, cta, G), p.items - 1), fbh, fqt, fn);
+      const long long hrow = static_cast<long long>(fbh) * p.L;
+      o_valid = fqt * 128 + row < p.L;
+      lse_reg = __ldg(p.lse + hrow + min(fqt * 128 + row, p.L - 1));
 #pragma unroll
-        for (int i = 0; i < CPH; ++i) o_reg[i] = __ldg(src + i);
-        lse_reg = __ldg(p.lse + static_cast<long long>(fbh) * p.L + qrow);
-      } else {
-#pragma unroll
-        for (int i = 0; i < CPH; ++i) o_reg[i] = make_uint4(0u, 0u, 0u, 0u);
-        lse_reg = INFINITY;
+      for (int i = 0; i < CPH; ++i) {
+        const int q = i * 32 + lane;
+        const long long orow = hrow + min(fqt * 128 + quarter * 32 + q / CPH, p.L - 1);
+        o_reg[i] = __ldg(reinterpret_cast<const uint4 *>(p.o + orow * D) + CPH * h + q % CPH);
       }
     };
     bool ok = true;
     int g = 0, it = 0;
+    // Thread (warp 4, lane 0) issues the epilogue's TMA store; it hands the K slot back to
+    // the producer (once the store has read it) at the next item's first step, so that the
+    // read does not hold up the next item.  stg_gl: last step of the item whose slot is
+    // still held, or -1.
+    int stg_gl = -1;
     fetch(0);  // this CTA's first item: bwd_item(0, cta, G) = cta < G <= items
     for (int r = 0; ok && r * G < p.items; ++r) {
       const int idx = bwd_item(r, cta, G);
@@ -735,14 +818,15 @@ __global__ void __launch_bounds__(384, 1)
       // Row statistics: D = dO . O, each warpgroup over its half of the row, the halves
       // added through shared memory; LSE log2(e).  Both go to the workspace.
       if (!(ok = wait_warp(C::QB_DOFULL, it & 1))) break;
-      float part0 = 0.f, part1 = 0.f;
 #pragma unroll
-      for (int i = 0; i < CPH; i += 2) {
-        part0 += bwd_dot8(ld_shared_v4(bwd_chunk_addr(do_s, C::RCHUNK, row, CPH * h + i)), o_reg[i]);
-        part1 += bwd_dot8(ld_shared_v4(bwd_chunk_addr(do_s, C::RCHUNK, row, CPH * h + i + 1)), o_reg[i + 1]);
+      for (int i = 0; i < CPH; ++i) {
+        const int q = i * 32 + lane, rw = quarter * 32 + q / CPH;
+        float part = bwd_dot8(ld_shared_v4(bwd_chunk_addr(do_s, C::RCHUNK, rw, CPH * h + q % CPH)), o_reg[i]);
+#pragma unroll
+        for (int m = 1; m < CPH; m <<= 1) part += __shfl_xor_sync(0xffffffffu, part, m);
+        if (q % CPH == 0) dpart[h * 128 + rw] = qt * 128 + rw < p.L ? part : 0.f;
       }
-      dpart[h * 128 + row] = part0 + part1;
-      const float lrow = lse_reg * kLog2e;
+      const float lrow = o_valid ? lse_reg * kLog2e : INFINITY;
       mbar_arrive(BAR(C::QB_DPART));
       if (!(ok = wait_warp(C::QB_DPART, it & 1))) break;
       const float drow = dpart[row] + dpart[128 + row];
@@ -766,6 +850,11 @@ __global__ void __launch_bounds__(384, 1)
         // the query (diagonal tile) or lies past L.
         if (!(ok = wait_warp(C::QB_SFULL + (g & 1), (static_cast<uint32_t>(g) >> 1) & 1u))) break;
         tc_fence_after();
+        if (stg_gl >= 0) {  // only the storing thread holds a slot
+          bulk_wait_read0();
+          mbar_arrive(BAR(C::QB_STGK + stg_gl % C::NKS));
+          stg_gl = -1;
+        }
         const int key0 = s * 128 + 64 * h;
         const bool edge = (CAUSAL && s == qt) || key0 + 64 > p.L;
         float pv[64];
@@ -804,14 +893,29 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok) break;
       // ---------------------------------------------------------------- epilogue
-      // scale * dQ: warpgroup h writes columns [h D/2, (h+1) D/2) of its query row.
+      // scale * dQ, staged in the K slot of the item's last step (free once the item's last
+      // product is complete): warpgroup h writes columns [h D/2, (h+1) D/2) of its query row;
+      // one thread then stores the tile by TMA (rows past L clipped).
       if (!(ok = wait_warp(C::QB_IDONE, it & 1))) break;
       tc_fence_after();
-      __half *const dst = p.dq + (static_cast<long long>(bh) * p.L + qrow) * D + h * (D / 2);
-      bwd_store_row<D / 2>(tmem + lane_base + C_DQ + h * (D / 2), dst, p.scale, qrow < p.L && *abort_flag == 0u);
+      const int gl = g - 1;
+      bwd_stage_row<D / 2>(tmem + lane_base + C_DQ + h * (D / 2), k_tile(gl), C::RCHUNK, row, h * (D / 16),
+                           p.scale);
       tc_fence_before();
+      fence_proxy_async_smem();  // the staged rows are read by TMA (async proxy)
+      mbar_arrive(BAR(C::QB_STAGED));
+      if (warp == 4 && lane == 0) {
+        ok = wait_bounded(BAR(C::QB_STAGED), it & 1, abort_flag, p.status, kDevTimeoutSoftmax, LIM);
+        if (ok && *abort_flag == 0u) {
+          for (int c = 0; c < C::NCH; ++c) tma_store_3d(&tm_dq, k_tile(gl) + c * C::RCHUNK, c * 64, qt * 128, bh);
+          bulk_commit();
+        }
+        stg_gl = gl;
+      }
+      if (warp == 4) ok = __shfl_sync(0xffffffffu, ok, 0);
       ++it;
     }
+    if (warp == 4 && lane == 0) bulk_wait0();  // the store is complete before the CTA exits
   }
   tc_fence_before();
   __syncthreads();

@@ -560,13 +560,12 @@ extern "C" int attn_bwd(const void *q, const void *k, const void *v, const void 
   BwdLaunch a;
   const int bh = static_cast<int>(BH);
   if (encode_bhld(&a.tm_q128, q, bh, L, d) || encode_bhld(&a.tm_do128, dout, bh, L, d) ||
-      encode_bhld(&a.tm_k128, k, bh, L, d) || encode_bhld(&a.tm_v128, v, bh, L, d))
+      encode_bhld(&a.tm_k128, k, bh, L, d) || encode_bhld(&a.tm_v128, v, bh, L, d) ||
+      encode_bhld(&a.tm_dq128, dq, bh, L, d) || encode_bhld(&a.tm_dk128, dk, bh, L, d) ||
+      encode_bhld(&a.tm_dv128, dv, bh, L, d))
     return GBATTN_ERR_TENSORMAP;
   a.p.lse = lse;
   a.p.o = static_cast<const __half *>(o);
-  a.p.dq = static_cast<__half *>(dq);
-  a.p.dk = static_cast<__half *>(dk);
-  a.p.dv = static_cast<__half *>(dv);
   a.p.status = di->status;
   a.p.wait_limit = kWaitLimitCycles;
   a.p.BH = bh;
