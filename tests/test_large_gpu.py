@@ -1,7 +1,8 @@
 """GPU parity on tensors of more than 2^31 elements (more than 4 GiB of fp16 each), so that
 every byte offset past the first 2^31 elements needs 64-bit arithmetic: the TMA
-coordinates of the query, key and value tiles, the O stores, the LSE rows and (in the
-backward pass) the O rows and the row-statistics workspace.
+coordinates of the query, key and value tiles, the O stores, the LSE rows, (in the
+backward pass) the O rows and the row-statistics workspace, and (in decode) the key and
+value streams of heads past the 2^31st element.
 
 The inputs repeat one seeded block of 9 heads along the head axis (copies, no
 arithmetic), so the oracle needs only that block: head h of the big tensors is head
@@ -97,4 +98,30 @@ def test_bwd_beyond_2_31_elements_matches_oracle():
         for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
             _check(g[0, h], r[0, j], ATOL, RTOL, f"{name} of head {h}")
     del q, k, v, do, o, lse, dq, dk, dv
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("grouped", [True, False], ids=["grouped", "one_cluster_per_head"])
+def test_decode_beyond_2_31_elements_matches_oracle(grouped):
+    """Decode over a key/value cache of 18 heads x 2^20 keys x 128 (2.4e9 elements each).
+    The cache tiles a seeded block of 9 heads x 2^17 keys 8 times along the keys and twice
+    along the heads: every key of a head appears 8 times, which leaves O unchanged and adds
+    ln 8 to the LSE exactly.  A 32-bit wrap moves a head by 16 heads, onto other data."""
+    Lb, reps, d, H = 1 << 17, 8, 128, 18
+    L = Lb * reps
+    assert H * L * d > 2 ** 31
+    bq, bk, bv = inputs.decode_qkv(1, PERIOD, Lb, d, seed=79)
+    q = _tile_heads(bq, H)
+    k, v = (_tile_heads(t, H).view(1, H, 1, Lb, d).expand(1, H, reps, Lb, d).reshape(1, H, L, d) for t in (bk, bv))
+    scale = 1.0 / math.sqrt(d)
+    o = torch.full((1, H, d), float("nan"), device="cuda", dtype=torch.float16)
+    lse = torch.full((1, H), float("nan"), device="cuda")
+    gb.attn_decode(q, k, v, scale=scale, o=o, lse=lse, grouped=grouped)
+    torch.cuda.synchronize()
+    heads = (0, 16, 17)  # heads 16 and 17 start past element 2^31
+    o_ref, lse_ref = oracle.decode(bq, bk, bv, float(np.float32(scale)), heads=[h % PERIOD for h in heads])
+    for j, h in enumerate(heads):
+        _check(o[0, h], o_ref[j], ATOL, RTOL, f"decode O of head {h}")
+        _check(lse[0, h:h + 1], lse_ref[j:j + 1] + math.log(reps), LSE_ATOL, 0.0, f"decode LSE of head {h}")
+    del q, k, v, o, lse
     torch.cuda.empty_cache()
