@@ -116,9 +116,10 @@ constexpr double kItemOverheadSingle = 1.0;  // in single-tile steps
 
 struct SchedKey {
   int kind, BH, nQ, nQB, dvs, causal, grid;
+  int shortest_first;  // each CTA runs its items shortest first (see build_lpt)
   bool operator==(const SchedKey &o) const {
     return kind == o.kind && BH == o.BH && nQ == o.nQ && nQB == o.nQB && dvs == o.dvs && causal == o.causal &&
-           grid == o.grid;
+           grid == o.grid && shortest_first == o.shortest_first;
   }
 };
 
@@ -163,12 +164,8 @@ double build_lpt(const SchedKey &k, SchedTable &t) {
     makespan = std::max(makespan, s.first + w.first);
     heap.push({s.first + w.first, s.second});
   }
-  // A CTA runs its items longest first, except in the two-tile kernel when every item lies
-  // within one 512-query block (items of at most 7 tile steps, two to four per CTA): there
-  // shortest first measured faster on GB300 (8x32x512x128 causal 30.8 -> 30.1 us,
-  // 16x16x512x128 30.8 -> 30.2), while longer rows and the single-tile kernel were flat or
-  // up to 2% slower.
-  const bool shortest_first = k.kind == kPair && k.nQB <= 2;
+  // A CTA runs its items longest first, except when k.shortest_first (make_key).
+  const bool shortest_first = k.shortest_first != 0;
   int pos = 0;
   for (int c = 0; c < k.grid; ++c) {
     t.start[c] = static_cast<uint16_t>(pos);
@@ -220,9 +217,16 @@ double get_schedule(const SchedKey &k, SchedTable *out) {
 // fewer than two items per SM: then whichever of the two has the smaller estimated
 // makespan (measured on GB300 at 1x16x512x64 causal 7.6 vs 11.2 us, 1x32x1024x128
 // causal 15.9 vs 23.7 us, both for the single-tile kernel).
+// Whether each CTA runs its items shortest first: in the two-tile kernel at head_dim 128
+// when every item lies within one 512-query block (items of at most 7 tile steps, two to
+// four per CTA), which measured faster on GB300 (8x32x512x128 causal 30.8 -> 30.1 us,
+// 16x16x512x128 30.8 -> 30.2), while head_dim 64 (8x32x512x64 26.1 -> 26.6), longer rows
+// and the single-tile kernel were flat or up to 2% slower.
+int shortest_first_rule(int kind, int nQB, int d) { return kind == kPair && nQB <= 2 && d == 128 ? 1 : 0; }
+
 SchedKey make_key(int kind, int BH, int L, int d, int causal, int grid) {
   const int nQ = (L + 127) / 128, nQB = (L + 255) / 256, dvs = d > 256 ? d / 256 : 1;
-  SchedKey k{kind, BH, nQ, nQB, kind == kSingle ? dvs : 1, causal != 0 ? 1 : 0, grid};
+  SchedKey k{kind, BH, nQ, nQB, kind == kSingle ? dvs : 1, causal != 0 ? 1 : 0, grid, shortest_first_rule(kind, nQB, d)};
   const long long n = count_items(k);
   if (n < grid) k.grid = static_cast<int>(n);
   return k;
@@ -746,7 +750,7 @@ extern "C" int attn_debug_schedule(int B, int H, int L, int d, int causal, int g
                    : ((flags & (GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE)) || d > 128) ? kSingle
                                                                                            : kPair;
   SchedKey key{kind, B * H, (L + 127) / 128, (L + 255) / 256, kind == kSingle && d > 256 ? d / 256 : 1,
-               causal != 0 ? 1 : 0, grid};
+               causal != 0 ? 1 : 0, grid, shortest_first_rule(kind, (L + 255) / 256, d)};
   if (count_items(key) > INT_MAX) return GBATTN_ERR_DIMS;
   static SchedTable t;  // large; this is a test hook, not thread-safe
   get_schedule(key, &t);
