@@ -15,9 +15,13 @@
  *   - Tensors are contiguous row-major [B, H, L, d] (PyTorch SDPA layout); q, k, v, o
  *     hold IEEE fp16 values, lse holds fp32 [B, H, L].
  *   - Every pointer is a DEVICE pointer owned by the caller (for example memory that
- *     PyTorch allocated).  The library never allocates, frees or retains device memory
- *     and never synchronises; it caches only TMA descriptors' host-side encodings and
- *     per-device attributes.
+ *     PyTorch allocated).  No entry point allocates or frees device memory, and none
+ *     synchronises (attn_last_device_error excepted); the library caches only host-side
+ *     schedules, per-device attributes and the host-buffer pipeline's streams.  The one
+ *     piece of device memory the library itself holds is attn_bwd_noalloc's fixed
+ *     16 MiB buffer (plus a 4-byte status word): a file-scope __device__ array, so every
+ *     GPU that loads the library holds it until the process exits, also in processes
+ *     that never call attn_bwd_noalloc.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
  *     Work is enqueued asynchronously on it; on return the outputs are not yet written.
  *   - Return value: 0 if the work was enqueued, otherwise one of the negative
@@ -176,9 +180,12 @@ long long attn_bwd_workspace_bytes(int B, int H, int L);
  *   attn_bwd_workspace_bytes(B, H, L) exceeds it (more than 2,097,152 query rows after
  *   padding L to a multiple of 128) return GBATTN_ERR_SCRATCH before anything is enqueued.
  *   No device memory is allocated or freed.
+ *   Arguments are checked first, in attn_bwd's order (so the same errors come back for
+ *   the same mistakes), then the size, and only then is any CUDA call made.
  *   The first call on each device looks up the buffer's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call before any
- *   stream capture.  All calls on a device share the one buffer: calls that can run at the
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make that first call
+ *   before any stream capture.  The cached address does not survive cudaDeviceReset: do
+ *   not call this entry point on a device after resetting it in the same process.  All calls on a device share the one buffer: calls that can run at the
  *   same time on the GPU (on streams not ordered against each other) race and must be
  *   serialised by the caller.  Nothing in the buffer needs to start at zero.
  */

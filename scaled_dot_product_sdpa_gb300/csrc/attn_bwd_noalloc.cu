@@ -11,7 +11,9 @@
 //
 // In host code the array's name only stands for the device symbol; its device address is
 // looked up with cudaGetSymbolAddress on the first call on each device (with that device
-// current) and cached per device.  Every call on a device shares the one buffer: calls
+// current) and cached per device.  The cache does not survive cudaDeviceReset (the
+// buffer gets a new address in the new context): a process that resets a device must not
+// call this entry point on it afterwards.  Every call on a device shares the one buffer: calls
 // whose kernels can run at the same time on the GPU (streams not ordered against each
 // other) race on it and must be serialised by the caller.  The buffer keeps the last
 // call's contents, and nothing in it needs to start at zero: the first kernel writes every
@@ -48,16 +50,23 @@ int scratch_address(void **out) {
 
 }  // namespace
 
+namespace gbattn {
+int bwd_check_args(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
+                   const void *dq, const void *dk, const void *dv, const void *workspace, bool check_workspace, int B,
+                   int H, int L, int d, float scale);  // gbattn_abi.cu
+}
+
 extern "C" long long attn_bwd_noalloc_max_bytes(void) { return kBwdScratchBytes; }
 
 extern "C" int attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const float *lse,
                                 const void *dout, void *dq, void *dk, void *dv, int B, int H, int L, int d,
                                 int causal, float scale, void *stream) {
-  const long long need = attn_bwd_workspace_bytes(B, H, L);
-  if (need < 0) return static_cast<int>(need);
-  if (need > kBwdScratchBytes) return GBATTN_ERR_SCRATCH;
-  void *ws = nullptr;
-  const int rc = scratch_address(&ws);
+  // attn_bwd's own checks first (no CUDA call), so that errors come in its order; then
+  // the buffer's size; only then the address lookup.
+  int rc = gbattn::bwd_check_args(q, k, v, o, lse, dout, dq, dk, dv, nullptr, false, B, H, L, d, scale);
   if (rc != GBATTN_OK) return rc;
+  if (attn_bwd_workspace_bytes(B, H, L) > kBwdScratchBytes) return GBATTN_ERR_SCRATCH;
+  void *ws = nullptr;
+  if ((rc = scratch_address(&ws)) != GBATTN_OK) return rc;
   return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, ws, B, H, L, d, causal, scale, stream);
 }

@@ -629,23 +629,7 @@ __global__ void __launch_bounds__(256, 1)
       tc_fence_after();
       const int qb = il % C::NQB;
       const uint32_t stage = q_s + qb * C::QBYTES;  // the item's Q tile is no longer read
-      const float inv_l = 1.0f / l;
-#pragma unroll 1
-      for (int c32 = 0; c32 < C::DV / 32; ++c32) {
-        uint32_t orr[32];
-        tmem_ld32x32(tmem + lane_base + C::O_COL + c32 * 32, orr);
-        uint32_t h[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          h[i] = pack_f16x2(__uint_as_float(orr[2 * i]) * inv_l, __uint_as_float(orr[2 * i + 1]) * inv_l);
-        const uint32_t rowaddr = stage + (c32 >> 1) * C::CHUNK + row * 128;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int chunk = (c32 & 1) * 4 + q4;
-          st_shared_v4(rowaddr + ((chunk ^ (row & 7)) << 4), h[4 * q4], h[4 * q4 + 1], h[4 * q4 + 2],
-                       h[4 * q4 + 3]);
-        }
-      }
+      stage_o_row<C::DV>(tmem + lane_base + C::O_COL, stage, row, 1.0f / l);
       tc_fence_before();
       mbar_arrive(BAR(C::B_OFREE));
       const int grow = qt * C::BM + row;

@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(384, 1)
   static_assert(128 * PPCfg<D>::kRegsLow + 256 * PPCfg<D>::kRegsHigh <= 384 * PPCfg<D>::kLaunchRegs,
                 "register split exceeds the launch allocation");
   if (warp < 4) {
-    setmaxnreg_dec<PPCfg<D>::kRegsLow>();
+    setmaxnreg_to<PPCfg<D>::kLaunchRegs, PPCfg<D>::kRegsLow>();
     if (warp == 0 && lane == 0) {
       // ---------------------------------------------------------- K/V producer
       const uint64_t pol_kv = policy_evict_last();
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     __syncwarp();
   } else {
-    setmaxnreg_inc<PPCfg<D>::kRegsHigh>();
+    setmaxnreg_to<PPCfg<D>::kLaunchRegs, PPCfg<D>::kRegsHigh>();
     // ================================================= softmax + epilogue of one Q tile
     const int slot = (warp - 4) >> 2;  // warps 4-7: Q0, warps 8-11: Q1
     const int quarter = warp & 3;
@@ -442,28 +442,9 @@ __global__ void __launch_bounds__(384, 1)
       if (!(ok = wait_warp(BAR(C::B_OFINAL + slot), il & 1))) break;
       if (!(ok = wait_warp(BAR(C::B_GRANT + slot), il & 1))) break;  // the staging buffer is ours
       tc_fence_after();
-      const uint32_t stage = o_s;
-      const float inv_l = 1.0f / l;
-#pragma unroll 1
-      for (int c32 = 0; c32 < D / 32; ++c32) {
-        uint32_t orr[32];
-        tmem_ld32x32(o_tmem + c32 * 32, orr);
-        if (c32 == D / 32 - 1) {  // O fully read: the next item's first PV may overwrite it
-          tc_fence_before();
-          mbar_arrive(BAR(C::B_OFREE + slot));
-        }
-        uint32_t h[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          h[i] = pack_f16x2(__uint_as_float(orr[2 * i]) * inv_l, __uint_as_float(orr[2 * i + 1]) * inv_l);
-        const uint32_t rowaddr = stage + (c32 >> 1) * C::CHUNK + row * 128;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int chunk = (c32 & 1) * 4 + q4;
-          st_shared_v4(rowaddr + ((chunk ^ (row & 7)) << 4), h[4 * q4], h[4 * q4 + 1], h[4 * q4 + 2],
-                       h[4 * q4 + 3]);
-        }
-      }
+      stage_o_row<D>(o_tmem, o_s, row, 1.0f / l);
+      tc_fence_before();
+      mbar_arrive(BAR(C::B_OFREE + slot));  // O fully read: the next item's first PV may overwrite it
       const int grow = qrow0 + row;
       if (grow < p.L)
         p.lse[static_cast<long long>(item.bh) * p.L + grow] = (m_used + __log2f(l)) * 0.69314718055994531f;

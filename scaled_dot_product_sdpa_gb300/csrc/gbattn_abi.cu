@@ -542,32 +542,48 @@ extern "C" long long attn_bwd_workspace_bytes(int B, int H, int L) {
   return 8 * BH * Lp;
 }
 
-extern "C" int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
-                        const void *dout, void *dq, void *dk, void *dv, void *workspace, int B, int H, int L, int d,
-                        int causal, float scale, void *stream) {
-  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return GBATTN_ERR_NULL;
+namespace gbattn {
+// Every check of attn_bwd's arguments (no CUDA call), in attn_bwd's order: NULL pointers,
+// shape, head_dim, alignment, scale, overlaps.  `workspace` may be NULL only when
+// `check_workspace` is false (attn_bwd_noalloc, whose workspace is the library's own).
+int bwd_check_args(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
+                   const void *dq, const void *dk, const void *dv, const void *workspace, bool check_workspace, int B,
+                   int H, int L, int d, float scale) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || (check_workspace && !workspace))
+    return GBATTN_ERR_NULL;
   int rc = check_shape(B, H, L, d);
   if (rc != GBATTN_OK) return rc;
   if (d != 64 && d != 128) return GBATTN_ERR_HEAD_DIM;
   const long long wsb = attn_bwd_workspace_bytes(B, H, L);
   if (wsb < 0) return GBATTN_ERR_DIMS;
   const void *ins[6] = {q, k, v, o, lse, dout};
-  void *outs[4] = {dq, dk, dv, workspace};
+  const void *outs[4] = {dq, dk, dv, workspace};
+  const int n_out = check_workspace ? 4 : 3;
   for (const void *x : ins)
     if (!aligned16(x)) return GBATTN_ERR_ALIGN;
-  for (const void *x : outs)
-    if (!aligned16(x)) return GBATTN_ERR_ALIGN;
+  for (int i = 0; i < n_out; ++i)
+    if (!aligned16(outs[i])) return GBATTN_ERR_ALIGN;
   if (!std::isfinite(scale) || !(scale > 0.f)) return GBATTN_ERR_SCALE;
   const long long BH = static_cast<long long>(B) * H;
   const size_t tb = static_cast<size_t>(BH) * L * d * 2u, lb = static_cast<size_t>(BH) * L * 4u;
   const size_t in_sz[6] = {tb, tb, tb, tb, lb, tb};
   const size_t out_sz[4] = {tb, tb, tb, static_cast<size_t>(wsb)};
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < n_out; ++i) {
     for (int j = 0; j < 6; ++j)
       if (overlaps(outs[i], out_sz[i], ins[j], in_sz[j])) return GBATTN_ERR_ALIAS;
-    for (int j = i + 1; j < 4; ++j)
+    for (int j = i + 1; j < n_out; ++j)
       if (overlaps(outs[i], out_sz[i], outs[j], out_sz[j])) return GBATTN_ERR_ALIAS;
   }
+  return GBATTN_OK;
+}
+}  // namespace gbattn
+
+extern "C" int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                        const void *dout, void *dq, void *dk, void *dv, void *workspace, int B, int H, int L, int d,
+                        int causal, float scale, void *stream) {
+  int rc = bwd_check_args(q, k, v, o, lse, dout, dq, dk, dv, workspace, true, B, H, L, d, scale);
+  if (rc != GBATTN_OK) return rc;
+  const long long BH = static_cast<long long>(B) * H;
   DevInfo *di = nullptr;
   if ((rc = device_info(&di)) != GBATTN_OK) return rc;
   BwdLaunch a;

@@ -299,6 +299,19 @@ template <int N>
 __device__ __forceinline__ void setmaxnreg_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
+// Move a warpgroup from FROM registers per thread (its current count) to TO: the increase
+// form only for a larger count, the decrease form only for a smaller one (either form
+// given a count on the wrong side of the current one is not a valid instruction).
+template <int FROM, int TO>
+__device__ __forceinline__ void setmaxnreg_to() {
+  static_assert(TO % 8 == 0 && TO >= 24 && TO <= 256, "setmaxnreg: a multiple of 8 in [24, 256]");
+  static_assert(FROM % 8 == 0 && FROM >= 24 && FROM <= 256, "setmaxnreg: a multiple of 8 in [24, 256]");
+  if constexpr (TO > FROM) {
+    setmaxnreg_inc<TO>();
+  } else if constexpr (TO < FROM) {
+    setmaxnreg_dec<TO>();
+  }
+}
 
 // ----------------------------------------------------------------------------- math
 // 2^x on the special-function unit (flush-to-zero; 2^-inf = +0).

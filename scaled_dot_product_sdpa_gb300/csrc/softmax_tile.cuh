@@ -120,6 +120,36 @@ __device__ __forceinline__ bool softmax_regs(uint32_t (&ra)[64], uint32_t (&rb)[
   return true;
 }
 
+// Epilogue of one query row: O / l as fp16 into the swizzled staging tile of the TMA store
+// (64-column chunks of 128-byte rows, CHUNK bytes apart; the 16-byte pieces of a row are
+// XOR-swizzled by row & 7).  128 columns of O are loaded from tensor memory with both
+// loads in flight and one wait, so the loads' latencies overlap.
+template <int DV>
+__device__ __forceinline__ void stage_o_row(uint32_t o_tmem, uint32_t stage, int row, float inv_l) {
+  constexpr int CHUNK = 128 * 128;
+  auto put64 = [&](const uint32_t (&r)[64], int chunk64) {
+    const uint32_t rowaddr = stage + chunk64 * CHUNK + row * 128;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      uint32_t h[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        h[i] = pack_f16x2(__uint_as_float(r[8 * q + 2 * i]) * inv_l, __uint_as_float(r[8 * q + 2 * i + 1]) * inv_l);
+      st_shared_v4(rowaddr + ((q ^ (row & 7)) << 4), h[0], h[1], h[2], h[3]);
+    }
+  };
+#pragma unroll 1
+  for (int c = 0; c < DV; c += 128) {
+    uint32_t a[64], b[64];
+    tmem_ld32x64_async(o_tmem + c, a);
+    if constexpr (DV > 64) tmem_ld32x64_async(o_tmem + c + 64, b);
+    tmem_wait_ld_fence64(a);
+    if constexpr (DV > 64) tmem_wait_ld_fence64(b);
+    put64(a, c / 64);
+    if constexpr (DV > 64) put64(b, c / 64 + 1);
+  }
+}
+
 template <int DV, class Hook = NoWait>
 __device__ __forceinline__ bool softmax_tile(uint32_t s_tmem, uint32_t o_tmem, int lim, float c2, bool first,
                                              float &m_used, float &l, const Hook &before_rescale = Hook(),
