@@ -85,7 +85,9 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
  *   single-tile kernel (every d): each work item is one 128-row query tile.
  * With flags = 0: d > 128 uses the single-tile kernel; d <= 128 the two-tile kernel when
  * it has at least two items per SM, else whichever of the two kernels has the shorter
- * estimated schedule.  Options:
+ * estimated schedule; for d = 64, 128 and 512 the single-tile kernel with key-range splits
+ * (bit 4) replaces that choice when its estimated schedule is clearly shorter (query
+ * tiles with many more key tiles than the average CTA's load).  Options:
  *   flags bit 0 (GBATTN_FLAG_P_SMEM): single-tile kernel, with P staged through shared
  *     memory instead of tensor memory before the PV product (the SMEM-P path of the
  *     STAGE_D.md notes, section 4); only for d <= 128, otherwise GBATTN_ERR_HEAD_DIM.
@@ -100,6 +102,16 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
  *     d = 512 (else GBATTN_ERR_HEAD_DIM) and alone (else GBATTN_ERR_FLAGS).  Slower on
  *     GB300: moving a 64 KB partial S tile between SMs takes longer than the QK work it
  *     saves.
+ *   flags bit 4 (GBATTN_FLAG_SPLIT_KV): the single-tile kernel on clusters of two CTAs,
+ *     where the longest query tiles are split into two disjoint key ranges, each at least
+ *     4 key tiles (512 keys), one per CTA of a cluster; the second CTA hands its partial
+ *     O (normalised, fp16) and each row's running maximum and sum to the first through
+ *     shared memory (one bulk copy per 64 columns), and the first merges the two with the
+ *     log-sum-exp weights (exact for disjoint key ranges: "An Optimal Mapper Meets a Real
+ *     GPU", "Experiment one", and STAGE_D.md, section 2, "Merge") and writes O and LSE.
+ *     Query tiles whose split would leave a part shorter than 4 key tiles are not split.
+ *     Only for d = 64, 128, 512 (else GBATTN_ERR_HEAD_DIM) and alone (else
+ *     GBATTN_ERR_FLAGS); the launch uses an even number of CTAs (at least 2).
  *   grid_limit: 0 = one persistent CTA per SM; n > 0 = at most n CTAs (scheduler tests).
  * Every option gives the same results up to rounding.
  */
@@ -107,6 +119,7 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
 #define GBATTN_FLAG_SINGLE_TILE 2
 #define GBATTN_FLAG_TWO_TILE 4
 #define GBATTN_FLAG_DSPLIT 8
+#define GBATTN_FLAG_SPLIT_KV 16
 int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                 int H, int L, int d, int causal, float scale, void *stream, int flags,
                 int grid_limit);
@@ -267,7 +280,11 @@ int attn_debug_wait_probe(long long limit_cycles, void *stream);
 /*
  * attn_debug_schedule -- test hook: the static work schedule attn_fwd_ex would use for
  * this shape, `grid` CTAs (clusters of two CTAs with GBATTN_FLAG_DSPLIT) and `flags`.
- * Returns the number of work items n and fills
+ * With GBATTN_FLAG_SPLIT_KV (`grid` even: CTAs 2c and 2c + 1 form cluster c) a value
+ * v >= (number of query tiles x value-column halves) in items[] names a split query tile
+ * (the tile of item v - that number), listed by both CTAs of a cluster, first, in the
+ * same order; the table then has one entry per CTA for each split tile.
+ * Returns the number of entries n and fills
  * start[0..grid] (CTA c runs items[start[c] .. start[c+1]) in order) and items[0..n), or
  * returns 0 when the problem is too large for a table (the kernels then use a fixed
  * snake order), or a negative GBATTN_ERR_* code (GBATTN_ERR_DIMS if n > max_items).
@@ -279,8 +296,10 @@ int attn_debug_schedule(int B, int H, int L, int d, int causal, int grid, int fl
 /*
  * attn_debug_plan -- test hook: the kernel attn_fwd_ex would launch for this shape,
  * `flags` and `grid_limit` on a GPU with `sm_count` SMs (host-only; needs no GPU).
- * Fills out[0] = kernel (0 single-tile, 1 two-tile, 2 single-tile with the head_dim split),
- * out[1] = work items, out[2] = CTAs (clusters of two CTAs for kernel 2),
+ * Fills out[0] = kernel (0 single-tile, 1 two-tile, 2 single-tile with the head_dim split,
+ * 3 single-tile with key-range splits), out[1] = work items (query tiles x value-column
+ * halves, before any split), out[2] = CTAs (clusters of two CTAs for kernel 2, CTAs in
+ * clusters of two for kernel 3),
  * out[3] = estimated makespan x 100 (in units of one tile step of a query tile in the
  * two-tile kernel; -100 when the kernels use their fixed order).
  * Returns 0 or a negative GBATTN_ERR_* code.

@@ -7,11 +7,11 @@ query row per head against a long cached key/value sequence, attn_decode) by a
 cluster-split streaming kernel.  This package is the
 thin Python binding of that library; every step of the computation runs on the GPU.
 """
-from ._binding import (FLAG_DSPLIT, FLAG_P_SMEM, FLAG_SINGLE_TILE, FLAG_TWO_TILE, LIB_PATH, GbattnError, attn_debug_decode_plan,
+from ._binding import (FLAG_DSPLIT, FLAG_P_SMEM, FLAG_SINGLE_TILE, FLAG_SPLIT_KV, FLAG_TWO_TILE, LIB_PATH, GbattnError, attn_debug_decode_plan,
                        attn_bwd, attn_bwd_workspace_bytes, attn_debug_plan, attn_debug_schedule, attn_debug_scores, attn_debug_wait_probe, attn_decode,
                        attn_fwd, attn_fwd_host, attn_last_device_error, attn_strerror, attn_version, load_library)
 
 __all__ = ["attn_fwd", "attn_fwd_host", "attn_bwd", "attn_bwd_workspace_bytes", "attn_decode", "attn_debug_plan", "attn_debug_decode_plan",
            "attn_debug_scores", "attn_debug_schedule", "attn_debug_wait_probe",
            "attn_last_device_error", "attn_strerror", "attn_version", "load_library", "GbattnError", "FLAG_P_SMEM",
-           "FLAG_SINGLE_TILE", "FLAG_TWO_TILE", "FLAG_DSPLIT", "LIB_PATH"]
+           "FLAG_SINGLE_TILE", "FLAG_TWO_TILE", "FLAG_DSPLIT", "FLAG_SPLIT_KV", "LIB_PATH"]

@@ -21,6 +21,7 @@ FLAG_P_SMEM = 1
 FLAG_SINGLE_TILE = 2
 FLAG_TWO_TILE = 4
 FLAG_DSPLIT = 8
+FLAG_SPLIT_KV = 16
 
 
 class GbattnError(RuntimeError):
@@ -266,7 +267,9 @@ def attn_debug_wait_probe(limit_cycles: int, stream=None) -> None:
 
 def attn_debug_schedule(B: int, H: int, L: int, d: int, causal: bool, grid: int, flags: int = 0):
     """The static work schedule attn_fwd would use (host-only): a list with, per CTA, the
-    work-item indices it runs in order; None when the kernels use their fixed order."""
+    work-item indices it runs in order; None when the kernels use their fixed order.  With
+    FLAG_SPLIT_KV an index >= the item count names a query tile whose key range the two
+    CTAs of a cluster (CTAs 2c, 2c + 1) share."""
     max_items = 1 << 16
     start = (ctypes.c_int * (grid + 1))()
     items = (ctypes.c_int * max_items)()
@@ -281,7 +284,8 @@ def attn_debug_schedule(B: int, H: int, L: int, d: int, causal: bool, grid: int,
 def attn_debug_plan(B: int, H: int, L: int, d: int, causal: bool, sm_count: int, flags: int = 0,
                     grid_limit: int = 0) -> dict:
     """The kernel attn_fwd would launch on a GPU with `sm_count` SMs (host-only):
-    kind 0 single-tile, 1 two-tile."""
+    kind 0 single-tile, 1 two-tile, 2 single-tile with the head_dim split, 3 single-tile
+    with key-range splits (CTAs in clusters of two)."""
     out = (ctypes.c_int * 4)()
     rc = load_library().attn_debug_plan(B, H, L, d, int(bool(causal)), sm_count, flags, grid_limit, out)
     if rc != 0:

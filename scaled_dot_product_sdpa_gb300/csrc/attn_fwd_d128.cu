@@ -4,4 +4,5 @@
 
 namespace gbattn {
 cudaError_t launch_fwd_128(const FwdLaunch &a) { return launch_fwd_d<128>(a); }
+int splitkv_clusters_128() { return splitkv_max_clusters<128>(); }
 }  // namespace gbattn

@@ -4,4 +4,5 @@
 
 namespace gbattn {
 cudaError_t launch_fwd_512(const FwdLaunch &a) { return launch_fwd_d<512>(a); }
+int splitkv_clusters_512() { return splitkv_max_clusters<512>(); }
 }  // namespace gbattn

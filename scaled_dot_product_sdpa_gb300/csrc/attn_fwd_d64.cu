@@ -4,4 +4,5 @@
 
 namespace gbattn {
 cudaError_t launch_fwd_64(const FwdLaunch &a) { return launch_fwd_d<64>(a); }
+int splitkv_clusters_64() { return splitkv_max_clusters<64>(); }
 }  // namespace gbattn

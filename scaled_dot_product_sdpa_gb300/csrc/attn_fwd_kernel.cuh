@@ -52,7 +52,7 @@ struct FwdParams {
   float c2;                // scale * log2(e)
 };
 
-template <int D, bool P_TMEM, bool DSPLIT = false>
+template <int D, bool P_TMEM, bool DSPLIT = false, bool SPLITKV = false>
 struct FwdCfg {
   static constexpr int BM = 128, BN = 128;
   static constexpr int DVS = D > 256 ? D / 256 : 1;  // value-column splits per (bh, qt)
@@ -78,10 +78,17 @@ struct FwdCfg {
   // head_dim split: the peer's partial S tile (128 x 128 fp32), 16-byte chunks of each
   // 512-byte row XOR-swizzled by row & 7
   static constexpr int RBYTES = DSPLIT ? 128 * 128 * 4 : 0;
+  // Key-range split over a CTA pair (split items): rank 1 hands its partial O (fp16,
+  // normalised by its own l) and each row's (m, l) to rank 0, which merges.  The receive
+  // area: a buffer of its own for head_dim <= 128; at head_dim 512 the Q buffer's columns
+  // 256-511 (free once the item's last QK is done; an item writes only 256 columns of O).
+  static constexpr bool CLUSTER = DSPLIT || SPLITKV;
+  static constexpr int XBYTES = SPLITKV && D <= 128 ? D * 128 * 2 : 0;  // receive buffer
+  static constexpr int STBYTES = SPLITKV ? 128 * 8 : 0;                 // (m, l) per row
   static constexpr int NPB = P_TMEM ? 0 : 2;         // shared-memory P buffers
   static constexpr int PBYTES = 2 * CHUNK;           // 128 x 128 fp16
   static constexpr int TILE_BUDGET = 224 * 1024;
-  static constexpr int NST_FIT = (TILE_BUDGET - NQB * QBYTES - NPB * PBYTES - RBYTES) / STAGE;
+  static constexpr int NST_FIT = (TILE_BUDGET - NQB * QBYTES - NPB * PBYTES - RBYTES - XBYTES) / STAGE;
   static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
   // barrier indices
   static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_FULL = 4, B_EMPTY = 4 + NST;
@@ -90,8 +97,14 @@ struct FwdCfg {
   // head_dim split: RECV completes when the peer's partial S is in this CTA's buffer,
   // RFREE when the peer has read this CTA's partial out of its own buffer
   static constexpr int B_RECV = B_DRAIN + 1, B_RFREE = B_RECV + 1;
-  static constexpr int NBAR = B_RFREE + 1;
-  static constexpr int TILE_BYTES = NQB * QBYTES + NPB * PBYTES + RBYTES + NST * STAGE;
+  // key-range split: READY (on rank 1) completes when rank 0's receive area is free for
+  // the split item, XRECV (on rank 0) when rank 1's partial has landed in it, XACK (on
+  // rank 1) when rank 0 has it (rank 1's staging is free again), XSTAGED (on rank 1) when
+  // its 128 softmax threads have staged their rows
+  static constexpr int B_READY = B_RFREE + 1, B_XRECV = B_READY + 1, B_XACK = B_XRECV + 1;
+  static constexpr int B_XSTAGED = B_XACK + 1;
+  static constexpr int NBAR = B_XSTAGED + 1;
+  static constexpr int TILE_BYTES = NQB * QBYTES + NPB * PBYTES + RBYTES + XBYTES + STBYTES + NST * STAGE;
   static constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + TILE_BYTES + 8 * NBAR + 16;
   // tensor memory columns: S buffer b at [128 b, 128 b + 128), O after the S buffers
   static constexpr int O_COL = 128 * NSB;
@@ -103,6 +116,8 @@ struct FwdCfg {
   static_assert(O_COL + DV <= TMEM_COLS, "tensor memory budget");
   static_assert(QCH % SC == 0 && NCHV % SC == 0, "stage split");
   static_assert(!DSPLIT || (D == 512 && P_TMEM), "head_dim split: D = 512, P in tensor memory");
+  static_assert(!SPLITKV || (P_TMEM && !DSPLIT && D != 256), "key-range split: D = 64, 128, 512, P in TMEM");
+  static_assert(!SPLITKV || D <= 128 || NCH >= 2 * NCHV, "key-range split at D = 512: Q columns hold the partial");
 };
 
 // Static schedule.  With a table (n > 0), CTA c processes items[start[c] .. start[c+1]):
@@ -155,6 +170,25 @@ __device__ __forceinline__ void decode_item(int r, const FwdParams &p, int &bh, 
   bh = rem / DVS;
   half = rem - bh * DVS;
   ntiles = CAUSAL ? qt + 1 : p.nQ;
+}
+
+// Work item in a launch with key-range splits: values >= n_items name a split item,
+// the query tile of item value - n_items (decoded as above) whose key tiles [0, n) are
+// shared by the two CTAs of a cluster: rank 0 takes [0, ceil(n / 2)), rank 1 the rest.
+template <int DVS, bool CAUSAL, bool SPLITKV>
+__device__ __forceinline__ bool decode_work(int r, const FwdParams &p, uint32_t rank, int &bh, int &qt, int &half,
+                                            int &t0, int &t1) {
+  const bool split = SPLITKV && r >= p.n_items;
+  int n;
+  decode_item<DVS, CAUSAL>(split ? r - p.n_items : r, p, bh, qt, half, n);
+  t0 = 0;
+  t1 = n;
+  if (split) {
+    const int n0 = (n + 1) / 2;
+    if (rank == 0) t1 = n0;
+    else t0 = n0;
+  }
+  return split;
 }
 
 // Bounded wait.  Gives up when the abort flag is raised or after `limit` cycles; in the
@@ -263,7 +297,7 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, long l
 // its Q buffer is its O staging tile and receives the Q of the item after next.
 struct PendingPv {
   uint32_t g;
-  int il, t, n, bh, half;
+  int il, t, t0, bh, half;  // t0: the item's first key tile (its first PV starts a fresh O)
 };
 template <int NSB>
 struct PvQueue {
@@ -288,12 +322,12 @@ struct PvQueue {
   __device__ const PendingPv &front() const { return head == 0 ? e[0] : e[CAP - 1]; }
 };
 
-template <int D, bool CAUSAL, bool P_TMEM, bool DSPLIT>
+template <int D, bool CAUSAL, bool P_TMEM, bool DSPLIT, bool SPLITKV = false>
 __global__ void __launch_bounds__(256, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     const FwdParams p, const __grid_constant__ SchedTable tbl) {
-  using C = FwdCfg<D, P_TMEM, DSPLIT>;
+  using C = FwdCfg<D, P_TMEM, DSPLIT, SPLITKV>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -304,7 +338,11 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t q_s = ring_s + C::NST * C::STAGE;          // NQB x QBYTES
   const uint32_t p_s = q_s + C::NQB * C::QBYTES;            // NPB x PBYTES
   const uint32_t recv_s = p_s + C::NPB * C::PBYTES;         // RBYTES (head_dim split)
-  const uint32_t bar_s = recv_s + C::RBYTES;                // NBAR x 8
+  const uint32_t x_s = recv_s + C::RBYTES;                  // XBYTES (key-range split, D <= 128)
+  const uint32_t st_s = x_s + C::XBYTES;                    // STBYTES: rank 1's (m, l) per row
+  const uint32_t bar_s = st_s + C::STBYTES;                 // NBAR x 8
+  // key-range split: where rank 0 receives rank 1's partial O
+  const uint32_t xrecv_s = D <= 128 ? x_s : q_s + C::NCHV * C::CHUNK;
   uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + (bar_s - base) + 8 * C::NBAR);
   volatile uint32_t *const abort_flag = tmem_slot + 1;
   auto BAR = [&](int i) -> uint32_t { return bar_s + 8u * static_cast<uint32_t>(i); };
@@ -312,8 +350,8 @@ __global__ void __launch_bounds__(256, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // head_dim split: the two CTAs of a cluster share every work item; rank r holds Q / K
   // columns [r * D/2, (r + 1) * D/2) and computes the value columns of half r.
-  const uint32_t rank = DSPLIT ? cluster_ctarank() : 0u;
-  const int qc0 = static_cast<int>(rank) * C::QCH;  // first 64-column chunk of Q / K held
+  const uint32_t rank = C::CLUSTER ? cluster_ctarank() : 0u;
+  const int qc0 = DSPLIT ? static_cast<int>(rank) * C::QCH : 0;  // first 64-column chunk of Q / K held
   const int sched_id = DSPLIT ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int sched_n = DSPLIT ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
@@ -321,6 +359,12 @@ __global__ void __launch_bounds__(256, 1)
     if (DSPLIT) {
       mbar_init(BAR(C::B_RECV), 128);   // the peer's 128 softmax threads
       mbar_init(BAR(C::B_RFREE), 128);
+    }
+    if (SPLITKV) {
+      mbar_init(BAR(C::B_READY), 1);    // one thread of rank 0
+      mbar_init(BAR(C::B_XRECV), 1);    // this CTA's expect_tx, plus the copied bytes
+      mbar_init(BAR(C::B_XACK), 1);     // one thread of rank 0
+      mbar_init(BAR(C::B_XSTAGED), 128);
     }
     for (int i = 0; i < C::NQB; ++i) {
       mbar_init(BAR(C::B_QFULL + i), 1);
@@ -355,7 +399,7 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t tmem = *tmem_slot;
   // Both CTAs of a pair have initialised their barriers before either arrives on the
   // other's (every thread reaches this, unconditionally).
-  if constexpr (DSPLIT) cluster_sync_all();
+  if constexpr (C::CLUSTER) cluster_sync_all();
   // The prologue above touches no global memory: the next kernel may launch now, and this
   // one waits here for the previous kernel's writes (inputs may be its outputs).
   grid_launch_dependents();
@@ -390,8 +434,8 @@ __global__ void __launch_bounds__(256, 1)
       PvQueue<C::NSB> pq;
       uint32_t g = 0;
       while (ok && sc.next(item)) {
-        int bh, qt, half, n;
-        decode_item<DSPLIT ? 1 : C::DVS, CAUSAL>(item, p, bh, qt, half, n);
+        int bh, qt, half, t0, t1;
+        decode_work<DSPLIT ? 1 : C::DVS, CAUSAL, SPLITKV>(item, p, rank, bh, qt, half, t0, t1);
         if (DSPLIT) half = static_cast<int>(rank);
         while (ok && pq.size > 0 && pq.front().il < il - (C::LOOKAHEAD ? 1 : 0)) ok = load_v(pq.pop());
         if (!ok) break;
@@ -403,10 +447,10 @@ __global__ void __launch_bounds__(256, 1)
         for (int c = 0; c < C::QCH; ++c)
           tma_load_3d(q_s + qb * C::QBYTES + c * C::CHUNK, &tm_q, (qc0 + c) * 64, qt * C::BM, bh,
                       BAR(C::B_QFULL + qb));
-        for (int t = 0; t < n && ok; ++t, ++g) {
+        for (int t = t0; t < t1 && ok; ++t, ++g) {
           for (int ks = 0; ks < C::KST && ok; ++ks) ok = load_stage(&tm_k, qc0 + ks * C::SC, t * C::BN, bh);
           if (ok && pq.size == C::NSB - 1) ok = load_v(pq.pop());
-          pq.push(PendingPv{g, il, t, n, bh, half});
+          pq.push(PendingPv{g, il, t, t0, bh, half});
         }
         ++il;
       }
@@ -454,7 +498,7 @@ __global__ void __launch_bounds__(256, 1)
       };
       auto issue_pv = [&](const PendingPv &v) -> bool {
         const uint32_t sb = v.g % C::NSB;
-        const bool first = v.t == 0;
+        const bool first = v.t == v.t0;
         if (!wait(BAR(C::B_PFULL + sb), (v.g / C::NSB) & 1u)) return false;
         if (first && v.il > 0 && !wait(BAR(C::B_OFREE), (v.il - 1) & 1)) return false;
         tc_fence_after();
@@ -482,18 +526,18 @@ __global__ void __launch_bounds__(256, 1)
       };
       PvQueue<C::NSB> pq;
       while (ok && sc.next(item)) {
-        int bh, qt, half, n;
-        decode_item<DSPLIT ? 1 : C::DVS, CAUSAL>(item, p, bh, qt, half, n);
+        int bh, qt, half, t0, t1;
+        decode_work<DSPLIT ? 1 : C::DVS, CAUSAL, SPLITKV>(item, p, rank, bh, qt, half, t0, t1);
         if (DSPLIT) half = static_cast<int>(rank);
         while (ok && pq.size > 0 && pq.front().il < il - (C::LOOKAHEAD ? 1 : 0)) ok = issue_pv(pq.pop());
         if (!ok) break;
         const int qb = il % C::NQB;
         if (!(ok = wait(BAR(C::B_QFULL + qb), (il / C::NQB) & 1))) break;
         tc_fence_after();
-        for (int t = 0; t < n && ok; ++t, ++g) {
+        for (int t = t0; t < t1 && ok; ++t, ++g) {
           ok = issue_qk(g, qb);
           if (ok && pq.size == C::NSB - 1) ok = issue_pv(pq.pop());
-          pq.push(PendingPv{g, il, t, n, bh, half});
+          pq.push(PendingPv{g, il, t, t0, bh, half});
         }
         ++il;
       }
@@ -501,6 +545,38 @@ __global__ void __launch_bounds__(256, 1)
       // Drain: all MMAs issued by this thread complete before tensor memory is freed.
       umma_commit(BAR(C::B_DRAIN));
       wait_drain(BAR(C::B_DRAIN), 0, LIM);
+    }
+    __syncwarp();
+  } else if (SPLITKV && warp == 2) {
+    // =============================================================== key-range split sender
+    // Rank 1: per split item, once its softmax warps have staged the partial and rank 0's
+    // receive area is free, copy the partial and the row statistics into rank 0 (one bulk
+    // copy per 64-column chunk, completion on rank 0's XRECV), wait until rank 0 has them,
+    // then give the item's Q buffer (its staging tile) back to the producer.
+    if (lane == 0 && rank == 1) {
+      Sched sc(sched_id, sched_n, p.n_items, &tbl);
+      int il = 0, ks = 0, item;
+      bool ok = true;
+      const uint32_t peer_bar = mapa_shared(BAR(C::B_XRECV), 0u);
+      while (ok && sc.next(item)) {
+        int bh, qt, half, t0, t1;
+        if (decode_work<C::DVS, CAUSAL, SPLITKV>(item, p, rank, bh, qt, half, t0, t1)) {
+          const int qb = il % C::NQB;
+          const uint32_t stage = q_s + qb * C::QBYTES;
+          if (!(ok = wait_bounded(BAR(C::B_XSTAGED), ks & 1, abort_flag, p.status, kDevTimeoutEpilogue, LIM)))
+            break;
+          if (!(ok = wait_bounded_cluster(BAR(C::B_READY), ks & 1, abort_flag, p.status, kDevTimeoutEpilogue, LIM)))
+            break;
+          for (int j = 0; j < C::NCHV; ++j)
+            bulk_s2c(mapa_shared(xrecv_s + j * C::CHUNK, 0u), stage + j * C::CHUNK, C::CHUNK, peer_bar);
+          bulk_s2c(mapa_shared(st_s, 0u), st_s, C::STBYTES, peer_bar);
+          if (!(ok = wait_bounded_cluster(BAR(C::B_XACK), ks & 1, abort_flag, p.status, kDevTimeoutEpilogue, LIM)))
+            break;
+          mbar_arrive(BAR(C::B_QEMPTY + qb));
+          ++ks;
+        }
+        ++il;
+      }
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -533,18 +609,26 @@ __global__ void __launch_bounds__(256, 1)
       const bool r = wait_bounded_cluster(bar, ph, abort_flag, p.status, kDevTimeoutSoftmax, LIM);
       return __all_sync(0xffffffffu, r);
     };
+    int ks = 0;  // split items so far (the phase of the key-range split barriers)
+    int ne = 0;  // items whose O this CTA stores (the phase of EPI; rank 1 stores no split item)
     while (ok && sc.next(item)) {
-      int bh, qt, half, n;
-      decode_item<DSPLIT ? 1 : C::DVS, CAUSAL>(item, p, bh, qt, half, n);
+      int bh, qt, half, t0, t1;
+      const bool split = decode_work<DSPLIT ? 1 : C::DVS, CAUSAL, SPLITKV>(item, p, rank, bh, qt, half, t0, t1);
       if (DSPLIT) half = static_cast<int>(rank);
       float m_used = 0.f, l = 0.f;
-      for (int t = 0; t < n; ++t, ++g) {
+      for (int t = t0; t < t1; ++t, ++g) {
         const uint32_t sb = g % C::NSB;
         if (!(ok = wait_warp(BAR(C::B_SFULL + sb), (g / C::NSB) & 1u))) break;
         tc_fence_after();
+        if (SPLITKV && split && rank == 0 && t == t1 - 1 && warp == 4 && lane == 0) {
+          // The last QK of this part is done: Q is no longer read, and the receive area
+          // is free.  Expect rank 1's partial and tell it to send.
+          mbar_arrive_expect_tx(BAR(C::B_XRECV), C::NCHV * C::CHUNK + C::STBYTES);
+          mbar_arrive_cluster(mapa_shared(BAR(C::B_READY), 1u));
+        }
         const int lim = CAUSAL ? (t == qt ? row + 1 : 128) : min(128, p.L - t * C::BN);
         // ODONE completes once per PV, and every phase is waited for exactly once, in
-        // order: on tile t > 0, the phase of PV(t-1) -- just before a rescale of O (which
+        // order: on tile t > t0, the phase of PV(t-1) -- just before a rescale of O (which
         // must not race with it), else at the end of the tile, when that PV has long been
         // done.  Either way PV(t-2) is complete (it was issued before this tile's QK) and
         // PV(t) cannot be (it needs this tile's P), so the wait's parity is unambiguous.
@@ -595,17 +679,17 @@ __global__ void __launch_bounds__(256, 1)
             rb[4 * c + 3] = __float_as_uint(__uint_as_float(rb[4 * c + 3]) + __uint_as_float(x.w));
           }
           mbar_arrive_cluster(mapa_shared(BAR(C::B_RFREE), rank ^ 1u));
-          if (!(ok = softmax_regs<C::DV>(ra, rb, s_row, tmem + lane_base + C::O_COL, lim, c2, t == 0, m_used, l,
+          if (!(ok = softmax_regs<C::DV>(ra, rb, s_row, tmem + lane_base + C::O_COL, lim, c2, t == t0, m_used, l,
                                          wait_prev_pv, &rescaled)))
             break;
         } else if constexpr (P_TMEM) {
-          if (!(ok = softmax_tile<C::DV>(tmem + lane_base + sb * 128u, tmem + lane_base + C::O_COL, lim, c2, t == 0,
+          if (!(ok = softmax_tile<C::DV>(tmem + lane_base + sb * 128u, tmem + lane_base + C::O_COL, lim, c2, t == t0,
                                          m_used, l, wait_prev_pv, &rescaled)))
             break;
         } else {
           // P through shared memory: run the step into tensor memory, then move the fp16
           // P from the S columns into the swizzled shared-memory operand tile.
-          if (!(ok = softmax_tile<C::DV>(tmem + lane_base + sb * 128u, tmem + lane_base + C::O_COL, lim, c2, t == 0,
+          if (!(ok = softmax_tile<C::DV>(tmem + lane_base + sb * 128u, tmem + lane_base + C::O_COL, lim, c2, t == t0,
                                          m_used, l, wait_prev_pv, &rescaled)))
             break;
           uint32_t pk[64];
@@ -618,10 +702,10 @@ __global__ void __launch_bounds__(256, 1)
           }
           fence_proxy_async_smem();
         }
-        if (t > 0 && !rescaled && !(ok = wait_prev_pv())) break;
+        if (t > t0 && !rescaled && !(ok = wait_prev_pv())) break;
         tc_fence_before();
         mbar_arrive(BAR(C::B_PFULL + sb));
-        if (t == 0 && warp == 4 && lane == 0) release_pending();
+        if (t == t0 && warp == 4 && lane == 0) release_pending();
       }
       if (!ok) break;
       // ------------------------------------------------------------- epilogue
@@ -629,16 +713,51 @@ __global__ void __launch_bounds__(256, 1)
       tc_fence_after();
       const int qb = il % C::NQB;
       const uint32_t stage = q_s + qb * C::QBYTES;  // the item's Q tile is no longer read
-      stage_o_row<C::DV>(tmem + lane_base + C::O_COL, stage, row, 1.0f / l);
+      const uint32_t o_row = tmem + lane_base + C::O_COL;
+      if (SPLITKV && split && rank == 1) {
+        // Rank 1 of a split item: its partial O / l (fp16) into its own staging tile and
+        // its (m, l) beside it; warp 2 copies both into rank 0's receive area.  The stats
+        // area is reused only once rank 0 has the previous split item's copy.
+        if (ks > 0 && !(ok = wait_warp_cluster(BAR(C::B_XACK), (ks - 1) & 1))) break;
+        stage_o_row<C::DV>(o_row, stage, row, 1.0f / l);
+        float *const st = reinterpret_cast<float *>(base_ptr + (st_s - base)) + 2 * row;
+        st[0] = m_used;
+        st[1] = l;
+        tc_fence_before();
+        mbar_arrive(BAR(C::B_OFREE));
+        fence_proxy_async_smem();
+        mbar_arrive(BAR(C::B_XSTAGED));
+        ++ks;
+        ++il;
+        continue;
+      }
+      float lse2 = m_used + __log2f(l);  // base-2 LSE of the row
+      if (SPLITKV && split) {
+        // Rank 0 of a split item: merge the two disjoint key ranges (STAGE_D.md, "Merge":
+        // valid because no key is in both).  With M = max(m0, m1), the row's sum is
+        // L = 2^(m0 - M) l0 + 2^(m1 - M) l1 and O = (2^(m0 - M) O0 + 2^(m1 - M) l1 O1hat) / L,
+        // where O0 is this CTA's unnormalised accumulator and O1hat rank 1's O1 / l1.
+        if (!(ok = wait_warp(BAR(C::B_XRECV), ks & 1))) break;
+        if (warp == 4 && lane == 0) mbar_arrive_cluster(mapa_shared(BAR(C::B_XACK), 1u));
+        const float *const st = reinterpret_cast<const float *>(base_ptr + (st_s - base)) + 2 * row;
+        const float m1 = st[0], l1 = st[1];
+        const float mx = fmaxf(m_used, m1);
+        const float a0 = ex2_approx(m_used - mx), a1 = ex2_approx(m1 - mx) * l1;
+        const float lsum = a0 * l + a1, inv = 1.0f / lsum;
+        merge_o_row<C::DV>(o_row, xrecv_s, stage, row, a0 * inv, a1 * inv);
+        lse2 = mx + __log2f(lsum);
+        ++ks;
+      } else {
+        stage_o_row<C::DV>(o_row, stage, row, 1.0f / l);
+      }
       tc_fence_before();
       mbar_arrive(BAR(C::B_OFREE));
       const int grow = qt * C::BM + row;
-      if (half == 0 && grow < p.L)
-        p.lse[static_cast<long long>(bh) * p.L + grow] = (m_used + __log2f(l)) * 0.69314718055994531f;
+      if (half == 0 && grow < p.L) p.lse[static_cast<long long>(bh) * p.L + grow] = lse2 * 0.69314718055994531f;
       fence_proxy_async_smem();
       mbar_arrive(BAR(C::B_EPI));
       if (warp == 4 && lane == 0) {
-        if (wait_bounded(BAR(C::B_EPI), il & 1, abort_flag, p.status, kDevTimeoutEpilogue, LIM)) {
+        if (wait_bounded(BAR(C::B_EPI), ne & 1, abort_flag, p.status, kDevTimeoutEpilogue, LIM)) {
           for (int j = 0; j < C::NCHV; ++j)
             tma_store_3d(&tm_o, stage + j * C::CHUNK, half * C::DV + j * 64, qt * C::BM, bh);
           bulk_commit();
@@ -648,6 +767,7 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
       __syncwarp();
+      ++ne;
       ++il;
     }
     if (warp == 4 && lane == 0) {
@@ -664,7 +784,7 @@ __global__ void __launch_bounds__(256, 1)
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
   // A CTA of a pair stays until the other has stopped writing into its shared memory.
-  if constexpr (DSPLIT) cluster_sync_all();
+  if constexpr (C::CLUSTER) cluster_sync_all();
 }
 
 // Launch with programmatic stream serialization: the kernel may begin (prologue only, see
@@ -689,12 +809,72 @@ struct FwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_o;
   FwdParams p;
   const SchedTable *tbl;
-  int grid;     // CTAs (pairs of CTAs with dsplit)
+  int grid;     // CTAs (pairs of CTAs with dsplit; an even number of CTAs with splitkv)
   bool causal;
   bool p_smem;
-  bool dsplit;  // head_dim 512 split over the two CTAs of a cluster
+  bool dsplit;   // head_dim 512 split over the two CTAs of a cluster
+  bool splitkv;  // long query tiles' key ranges split over the two CTAs of a cluster
   cudaStream_t stream;
 };
+
+// Clusters of two CTAs, `ctas` CTAs in all, with programmatic stream serialization.
+template <class Kern>
+cudaError_t launch_pairs(Kern kern, int ctas, int smem, const FwdLaunch &a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p, *a.tbl);
+}
+
+// Clusters of two CTAs of the key-range split kernel that the current device can hold at
+// once (clusters stay within a GPC, so an SM may be left over); -1 if the query fails.
+template <int D>
+int splitkv_max_clusters() {
+  using C = FwdCfg<D, true, false, true>;
+  auto *kern = attn_fwd_kernel<D, true, true, false, true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess) return -1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = static_cast<size_t>(C::SMEM_BYTES);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return -1;
+  return n;
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_splitkv(const FwdLaunch &a) {
+  using C = FwdCfg<D, true, false, true>;
+  auto *kern = attn_fwd_kernel<D, CAUSAL, true, false, true>;
+  static int configured_mask = 0;  // one bit per device ordinal < 31
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 31 || !(configured_mask & (1 << dev))) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev < 31) configured_mask |= (1 << dev);
+  }
+  return launch_pairs(kern, a.grid, C::SMEM_BYTES, a);
+}
 
 template <int D, bool CAUSAL>
 cudaError_t launch_fwd_dsplit(const FwdLaunch &a) {
@@ -709,21 +889,7 @@ cudaError_t launch_fwd_dsplit(const FwdLaunch &a) {
     if (e != cudaSuccess) return e;
     if (dev < 31) configured_mask |= (1 << dev);
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2u * static_cast<unsigned>(a.grid));
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = static_cast<size_t>(C::SMEM_BYTES);
-  cfg.stream = a.stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p, *a.tbl);
+  return launch_pairs(kern, 2 * a.grid, C::SMEM_BYTES, a);
 }
 
 template <int D, bool CAUSAL, bool P_TMEM>
@@ -744,6 +910,9 @@ cudaError_t launch_fwd_variant(const FwdLaunch &a) {
 
 template <int D>
 cudaError_t launch_fwd_d(const FwdLaunch &a) {
+  if constexpr (D != 256) {
+    if (a.splitkv) return a.causal ? launch_fwd_splitkv<D, true>(a) : launch_fwd_splitkv<D, false>(a);
+  }
   if constexpr (D <= 128) {
     if (a.p_smem)
       return a.causal ? launch_fwd_variant<D, true, false>(a) : launch_fwd_variant<D, false, false>(a);
@@ -763,5 +932,8 @@ cudaError_t launch_fwd_64(const FwdLaunch &a);
 cudaError_t launch_fwd_128(const FwdLaunch &a);
 cudaError_t launch_fwd_256(const FwdLaunch &a);
 cudaError_t launch_fwd_512(const FwdLaunch &a);
+int splitkv_clusters_64();
+int splitkv_clusters_128();
+int splitkv_clusters_512();
 
 }  // namespace gbattn

@@ -41,6 +41,7 @@ struct DevInfo {
   int cc_major = 0, cc_minor = 0, sm_count = 0;
   unsigned *status = nullptr;
   int dec_max_ranks[4] = {0, 0, 0, 0};  // decode cluster size limit per head_dim (0: not yet asked)
+  int split_ctas[3] = {0, 0, 0};        // CTAs the key-range split kernel can hold at once, d = 64, 128, 512
 };
 DevInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -104,7 +105,10 @@ int encode_bhld(CUtensorMap *tm, const void *ptr, int BH, int L, int D, int box_
 // of a cluster (an option: slower on GB300, whose distributed shared memory moves the
 // partial logits at ~17 B per cycle per SM); its schedule deals (head, query tile) items
 // to clusters.
-enum Kind { kSingle = 0, kPair = 1, kDSplit = 2 };
+// kSplitKV: the single-tile kernel on clusters of two CTAs, the longest query tiles' key
+// ranges split over the two CTAs of a cluster and merged by the first; its schedule lists
+// such split tiles first, in the same order, for both CTAs of the cluster that runs them.
+enum Kind { kSingle = 0, kPair = 1, kDSplit = 2, kSplitKV = 3 };
 
 // Cost of a work item in units of one 128 x 128 tile step of one query tile in the
 // two-tile kernel (it runs two such steps at once, one per query tile of its item), plus
@@ -113,6 +117,11 @@ enum Kind { kSingle = 0, kPair = 1, kDSplit = 2 };
 constexpr double kItemOverheadTwoSlot = 1.7;
 constexpr double kSingleStepCost = 1.2;
 constexpr double kItemOverheadSingle = 1.0;  // in single-tile steps
+// Key-range split: each part at least 4 key tiles (512 keys), and each part of a split
+// tile costs the handover and merge on top of its steps (in single-tile steps).
+constexpr int kSplitMinPart = 4;
+constexpr double kSplitOverhead = 1.5;
+constexpr double kSplitGain = 0.9;  // taken only below this fraction of the other makespan
 
 struct SchedKey {
   int kind, BH, nQ, nQB, dvs, causal, grid;
@@ -128,6 +137,9 @@ long long count_items(const SchedKey &k) {
 }
 // (kDSplit keys have dvs = 1: one item per head and query tile.)
 
+// Key tiles of single-tile item r (decode_item's order: longest first when causal).
+int item_tiles(const SchedKey &k, int r) { return k.causal ? k.nQ - r / (k.BH * k.dvs) : k.nQ; }
+
 // Cost of item r, mirroring the kernels' item decoding (decode_item / pp_decode).
 double item_cost(const SchedKey &k, int r) {
   if (k.kind == kPair) {
@@ -135,8 +147,82 @@ double item_cost(const SchedKey &k, int r) {
     const int qb = k.nQB - 1 - r / k.BH;
     return (2 * qb + 1) + std::min(2 * qb + 2, k.nQ) + kItemOverheadTwoSlot;
   }
-  const int n = k.causal ? k.nQ - r / (k.BH * k.dvs) : k.nQ;
-  return kSingleStepCost * (n + kItemOverheadSingle);
+  return kSingleStepCost * (item_tiles(k, r) + kItemOverheadSingle);
+}
+
+// Schedule with key-range splits: the first `ns` items (the longest) are split; each goes
+// to the cluster (CTAs 2c, 2c + 1) where it ends earliest, rank 0 taking ceil(n / 2) key
+// tiles and rank 1 the rest; the other items then go longest first to the least-loaded
+// CTA.  Returns the makespan; fills `lists` when given.
+double split_assign(const SchedKey &k, int ns, std::vector<std::vector<uint16_t>> *lists) {
+  const int N = static_cast<int>(count_items(k)), G = k.grid, C = G / 2;
+  std::vector<double> load(G, 0.0);
+  if (lists) lists->assign(G, {});
+  for (int s = 0; s < ns; ++s) {
+    const int n = item_tiles(k, s);
+    const double c0 = kSingleStepCost * ((n + 1) / 2 + kSplitOverhead);
+    const double c1 = kSingleStepCost * (n / 2 + kSplitOverhead);
+    int best = 0;
+    double best_end = 0.0;
+    for (int c = 0; c < C; ++c) {
+      const double e = std::max(load[2 * c] + c0, load[2 * c + 1] + c1);
+      if (c == 0 || e < best_end) {
+        best = c;
+        best_end = e;
+      }
+    }
+    load[2 * best] += c0;
+    load[2 * best + 1] += c1;
+    if (lists) {
+      (*lists)[2 * best].push_back(static_cast<uint16_t>(N + s));
+      (*lists)[2 * best + 1].push_back(static_cast<uint16_t>(N + s));
+    }
+  }
+  using Slot = std::pair<double, int>;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int c = 0; c < G; ++c) heap.push({load[c], c});
+  double makespan = 0.0;
+  for (const double x : load) makespan = std::max(makespan, x);
+  for (int r = ns; r < N; ++r) {  // r order is longest first (item_tiles is non-increasing)
+    const Slot sl = heap.top();
+    heap.pop();
+    const double w = item_cost(k, r);
+    if (lists) (*lists)[sl.second].push_back(static_cast<uint16_t>(r));
+    makespan = std::max(makespan, sl.first + w);
+    heap.push({sl.first + w, sl.second});
+  }
+  return makespan;
+}
+
+// The split schedule: the number of split tiles (among those whose parts keep at least
+// kSplitMinPart key tiles) with the smallest estimated makespan, at most two per cluster.
+double build_split(const SchedKey &k, SchedTable &t) {
+  std::memset(&t, 0, sizeof(t));
+  const long long N = count_items(k);
+  if (k.grid < 2 || k.grid % 2 || k.grid > kSchedMaxCtas || N > kSchedMaxItems) return -1.0;
+  int cand = 0;
+  while (cand < N && item_tiles(k, cand) >= 2 * kSplitMinPart) ++cand;
+  const int ns_max = std::min({cand, k.grid, kSchedMaxItems - static_cast<int>(N)});
+  const int step = std::max(1, ns_max / 48);
+  int best_ns = 0;
+  double best = split_assign(k, 0, nullptr);
+  for (int ns = step; ns <= ns_max; ns += step) {
+    const double m = split_assign(k, ns, nullptr);
+    if (m < best - 1e-9) {
+      best = m;
+      best_ns = ns;
+    }
+  }
+  std::vector<std::vector<uint16_t>> lists;
+  split_assign(k, best_ns, &lists);
+  int pos = 0;
+  for (int c = 0; c < k.grid; ++c) {
+    t.start[c] = static_cast<uint16_t>(pos);
+    for (uint16_t r : lists[c]) t.items[pos++] = r;
+  }
+  t.start[k.grid] = static_cast<uint16_t>(pos);
+  t.n = pos;
+  return best;
 }
 
 // Longest-processing-time-first: take items by decreasing cost, give each to the CTA with
@@ -144,6 +230,7 @@ double item_cost(const SchedKey &k, int r) {
 // Returns the largest accumulated cost (the estimated makespan), or -1 with t.n = 0
 // (the kernels' fixed snake order) when the items or CTAs do not fit the table.
 double build_lpt(const SchedKey &k, SchedTable &t) {
+  if (k.kind == kSplitKV) return build_split(k, t);
   std::memset(&t, 0, sizeof(t));
   const long long n_items = count_items(k);
   if (n_items > kSchedMaxItems || k.grid > kSchedMaxCtas || k.grid <= 0) return -1.0;
@@ -226,20 +313,35 @@ int shortest_first_rule(int kind, int nQB, int d) { return kind == kPair && nQB 
 
 SchedKey make_key(int kind, int BH, int L, int d, int causal, int grid) {
   const int nQ = (L + 127) / 128, nQB = (L + 255) / 256, dvs = d > 256 ? d / 256 : 1;
-  SchedKey k{kind, BH, nQ, nQB, kind == kSingle ? dvs : 1, causal != 0 ? 1 : 0, grid, shortest_first_rule(kind, nQB, d)};
+  SchedKey k{kind, BH, nQ, nQB, kind == kSingle || kind == kSplitKV ? dvs : 1, causal != 0 ? 1 : 0, grid,
+             shortest_first_rule(kind, nQB, d)};
   const long long n = count_items(k);
-  if (n < grid) k.grid = static_cast<int>(n);
+  if (kind == kSplitKV) {
+    // An even number of CTAs (clusters of two), at most two per item.
+    k.grid = static_cast<int>(std::min<long long>(grid, 2 * n)) & ~1;
+    if (k.grid < 2) k.grid = 2;
+  } else if (n < grid) {
+    k.grid = static_cast<int>(n);
+  }
   return k;
 }
 
+// head_dims the key-range split is built for
+bool split_kv_dim(int d) { return d == 64 || d == 128 || d == 512; }
+
+// `split_ctas`: CTAs (clusters of two) the key-range split kernel can hold at once.
 int choose_plan(int BH, int L, int d, int causal, int sm_count, int flags, int grid_limit, SchedKey &out,
-                double &makespan) {
+                double &makespan, int split_ctas) {
   int grid = sm_count;
   if (grid_limit > 0 && grid_limit < grid) grid = grid_limit;
+  const int split_grid = std::max(2, std::min(grid, split_ctas));
   int kind;
   if (flags & GBATTN_FLAG_DSPLIT) {
     kind = kDSplit;  // clusters of two CTAs: the schedule's lanes are the clusters
     grid = std::max(1, grid / 2);
+  } else if (flags & GBATTN_FLAG_SPLIT_KV) {
+    kind = kSplitKV;
+    grid = split_grid;
   } else if (flags & (GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE) || d > 128) {
     kind = kSingle;
   } else if (flags & GBATTN_FLAG_TWO_TILE) {
@@ -262,6 +364,17 @@ int choose_plan(int BH, int L, int d, int causal, int sm_count, int flags, int g
       if (kind < 0) kind = kPair;
     }
   }
+  // Without options, key-range splits replace the choice above when their schedule is
+  // clearly shorter (few query tiles, some much longer than the average load); not when
+  // the two-tile kernel has enough items (that kernel's grid is full).
+  if (flags == 0 && split_kv_dim(d) && grid >= 2 && (kind == kSingle || count_items(make_key(kPair, BH, L, d, causal, grid)) < 2LL * grid)) {
+    const double cur = get_schedule(make_key(kind, BH, L, d, causal, grid), nullptr);
+    const double split = get_schedule(make_key(kSplitKV, BH, L, d, causal, split_grid), nullptr);
+    if (cur >= 0.0 && split >= 0.0 && split < kSplitGain * cur) {
+      kind = kSplitKV;
+      grid = split_grid;
+    }
+  }
   out = make_key(kind, BH, L, d, causal, grid);
   if (count_items(out) > INT_MAX) return GBATTN_ERR_DIMS;
   makespan = get_schedule(out, nullptr);
@@ -278,8 +391,11 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // The option bits of attn_fwd_ex: known bits only, the two-tile kernel not together with
 // a single-tile option, and the two-tile kernel and shared-memory P only for d <= 128.
 int check_flags(int flags, int d) {
-  if (flags & ~(GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE | GBATTN_FLAG_TWO_TILE | GBATTN_FLAG_DSPLIT))
+  if (flags & ~(GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE | GBATTN_FLAG_TWO_TILE | GBATTN_FLAG_DSPLIT |
+                GBATTN_FLAG_SPLIT_KV))
     return GBATTN_ERR_FLAGS;
+  if ((flags & GBATTN_FLAG_SPLIT_KV) && (flags & ~GBATTN_FLAG_SPLIT_KV)) return GBATTN_ERR_FLAGS;
+  if ((flags & GBATTN_FLAG_SPLIT_KV) && !split_kv_dim(d)) return GBATTN_ERR_HEAD_DIM;
   if ((flags & GBATTN_FLAG_TWO_TILE) && (flags & (GBATTN_FLAG_SINGLE_TILE | GBATTN_FLAG_P_SMEM)))
     return GBATTN_ERR_FLAGS;
   if ((flags & GBATTN_FLAG_DSPLIT) && (flags & ~GBATTN_FLAG_DSPLIT)) return GBATTN_ERR_FLAGS;
@@ -352,9 +468,19 @@ extern "C" int attn_fwd_ex(const void *q, const void *k, const void *v, void *o,
   if ((rc = device_info(&di)) != GBATTN_OK) return rc;
 
   const int BH = B * H;
+  int split_ctas = di->sm_count;
+  if (split_kv_dim(d)) {
+    int &sc = di->split_ctas[d == 64 ? 0 : d == 128 ? 1 : 2];
+    if (sc == 0) {
+      const int n = d == 64 ? splitkv_clusters_64() : d == 128 ? splitkv_clusters_128() : splitkv_clusters_512();
+      sc = n > 0 ? std::min(2 * n, di->sm_count & ~1) : (di->sm_count & ~1);
+    }
+    split_ctas = sc;
+  }
   SchedKey key;
   double makespan = 0.0;
-  if ((rc = choose_plan(BH, L, d, causal, di->sm_count, flags, grid_limit, key, makespan)) != GBATTN_OK) return rc;
+  if ((rc = choose_plan(BH, L, d, causal, di->sm_count, flags, grid_limit, key, makespan, split_ctas)) != GBATTN_OK)
+    return rc;
   const bool two_tile = key.kind == kPair;
 
   FwdLaunch a;
@@ -368,6 +494,7 @@ extern "C" int attn_fwd_ex(const void *q, const void *k, const void *v, void *o,
   a.causal = causal != 0;
   a.p_smem = p_smem;
   a.dsplit = key.kind == kDSplit;
+  a.splitkv = key.kind == kSplitKV;
   a.stream = static_cast<cudaStream_t>(stream);
   a.p.lse = lse;
   a.p.status = di->status;
@@ -762,11 +889,15 @@ extern "C" int attn_debug_schedule(int B, int H, int L, int d, int causal, int g
   // The schedule of the kernel the flags name (no flag, d <= 128: the two-tile kernel;
   // the head_dim split's `grid` lanes are clusters of two CTAs; the automatic choice of
   // attn_fwd is not applied here).
-  const int kind = (flags & GBATTN_FLAG_DSPLIT) ? kDSplit
+  if ((rc = check_flags(flags, d)) != GBATTN_OK) return rc;
+  const int kind = (flags & GBATTN_FLAG_DSPLIT)     ? kDSplit
+                   : (flags & GBATTN_FLAG_SPLIT_KV) ? kSplitKV
                    : ((flags & (GBATTN_FLAG_P_SMEM | GBATTN_FLAG_SINGLE_TILE)) || d > 128) ? kSingle
                                                                                            : kPair;
-  SchedKey key{kind, B * H, (L + 127) / 128, (L + 255) / 256, kind == kSingle && d > 256 ? d / 256 : 1,
-               causal != 0 ? 1 : 0, grid, shortest_first_rule(kind, (L + 255) / 256, d)};
+  if (kind == kSplitKV && grid % 2) return GBATTN_ERR_DIMS;
+  SchedKey key{kind, B * H, (L + 127) / 128, (L + 255) / 256,
+               (kind == kSingle || kind == kSplitKV) && d > 256 ? d / 256 : 1, causal != 0 ? 1 : 0, grid,
+               shortest_first_rule(kind, (L + 255) / 256, d)};
   if (count_items(key) > INT_MAX) return GBATTN_ERR_DIMS;
   static SchedTable t;  // large; this is a test hook, not thread-safe
   get_schedule(key, &t);
@@ -786,7 +917,9 @@ extern "C" int attn_debug_plan(int B, int H, int L, int d, int causal, int sm_co
   if ((rc = check_flags(flags, d)) != GBATTN_OK) return rc;
   SchedKey key;
   double makespan = 0.0;
-  if ((rc = choose_plan(B * H, L, d, causal, sm_count, flags, grid_limit, key, makespan)) != GBATTN_OK) return rc;
+  if ((rc = choose_plan(B * H, L, d, causal, sm_count, flags, grid_limit, key, makespan, sm_count & ~1)) !=
+      GBATTN_OK)
+    return rc;
   out[0] = key.kind;
   out[1] = static_cast<int>(count_items(key));
   out[2] = key.grid;

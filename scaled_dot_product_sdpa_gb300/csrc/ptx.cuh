@@ -137,6 +137,15 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
                : "memory");
 }
+// Bulk copy from this CTA's shared memory into the shared memory of a CTA of the cluster
+// (`dst` and `bar` are shared::cluster addresses, from mapa): `bytes` a multiple of 16,
+// both addresses 16-byte aligned; completion is signalled on the destination CTA's
+// mbarrier `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_s2c(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
 // Same, with an L2 cache-policy hint (a createpolicy value).
 __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *tm, int x,
                                                  int y, int z, uint32_t bar, uint64_t policy) {

@@ -150,6 +150,51 @@ __device__ __forceinline__ void stage_o_row(uint32_t o_tmem, uint32_t stage, int
   }
 }
 
+// fp16x2 -> two fp32 (low half first), exact.
+__device__ __forceinline__ void unpack_f16x2(uint32_t v, float &lo, float &hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(v));
+}
+
+// Epilogue of one query row of a query tile whose keys two CTAs shared: out = w_own * O
+// (this CTA's unnormalised accumulator in tensor memory) + w_peer * O_peer (the other
+// CTA's partial, normalised, fp16, in the staging layout at `recv`), as fp16 into the
+// staging tile.  The weights carry the merge over the two disjoint key ranges.
+template <int DV>
+__device__ __forceinline__ void merge_o_row(uint32_t o_tmem, uint32_t recv, uint32_t stage, int row, float w_own,
+                                            float w_peer) {
+  constexpr int CHUNK = 128 * 128;
+  auto put64 = [&](const uint32_t (&r)[64], int chunk64) {
+    const uint32_t off = chunk64 * CHUNK + row * 128;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint32_t sw = (q ^ (row & 7)) << 4;
+      const uint4 x = ld_shared_v4(recv + off + sw);
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+      uint32_t h[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float a, b;
+        unpack_f16x2(xs[i], a, b);
+        h[i] = pack_f16x2(fmaf(w_own, __uint_as_float(r[8 * q + 2 * i]), w_peer * a),
+                          fmaf(w_own, __uint_as_float(r[8 * q + 2 * i + 1]), w_peer * b));
+      }
+      st_shared_v4(stage + off + sw, h[0], h[1], h[2], h[3]);
+    }
+  };
+#pragma unroll 1
+  for (int c = 0; c < DV; c += 128) {
+    uint32_t a[64], b[64];
+    tmem_ld32x64_async(o_tmem + c, a);
+    if constexpr (DV > 64) tmem_ld32x64_async(o_tmem + c + 64, b);
+    tmem_wait_ld_fence64(a);
+    if constexpr (DV > 64) tmem_wait_ld_fence64(b);
+    put64(a, c / 64);
+    if constexpr (DV > 64) put64(b, c / 64 + 1);
+  }
+}
+
 template <int DV, class Hook = NoWait>
 __device__ __forceinline__ bool softmax_tile(uint32_t s_tmem, uint32_t o_tmem, int lim, float c2, bool first,
                                              float &m_used, float &l, const Hook &before_rescale = Hook(),
