@@ -88,11 +88,12 @@ def test_smem_p_only_up_to_128(lib):
 def test_flag_combinations(lib):
     c = _codes()
     assert _fwd(lib, d=512, flags=4) == c["GBATTN_ERR_HEAD_DIM"]
-    for bad in (4 | 2, 4 | 1, 16, 32, 64):
+    for bad in (4 | 2, 4 | 1, 32, 64, 16 | 1, 16 | 2, 16 | 4, 16 | 8):
         assert _fwd(lib, flags=bad) == c["GBATTN_ERR_FLAGS"], bad
     assert _fwd(lib, flags=8) == c["GBATTN_ERR_HEAD_DIM"]  # the head_dim split is for d = 512 only
     for bad in (8 | 1, 8 | 2, 8 | 4):
         assert _fwd(lib, d=512, flags=bad) == c["GBATTN_ERR_FLAGS"], bad
+    assert _fwd(lib, d=256, flags=16) == c["GBATTN_ERR_HEAD_DIM"]  # no key-range split at d = 256
 
 
 @pytest.mark.parametrize("kw", ["q", "k", "v", "o", "lse"])
