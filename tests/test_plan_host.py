@@ -2,7 +2,8 @@
 variant a launch uses, with how many work items and CTAs.
 
 Kernels (include/gbattn.h, attn_fwd_ex): 0 single-tile (items: one 128-row query tile
-per value-column half), 1 two-tile (items: 256-row query blocks).  The item counts below
+per value-column half), 1 two-tile (items: 256-row query blocks), 3 single-tile with
+key-range splits over clusters of two CTAs (the same items, some split).  The item counts below
 follow from those definitions alone."""
 import math
 
@@ -51,8 +52,15 @@ def test_auto_plan(B, H, L, d, causal):
         q = gb.attn_debug_plan(B, H, L, d, causal, SM, flags=gb.FLAG_DSPLIT)
         n = _items(2, B, H, L, d)
         assert (q["kind"], q["items"], q["grid"]) == (2, n, min(SM // 2, n))
+    # Key-range splits (head_dim 64, 128, 512) replace the choice below when their schedule
+    # is more than 10% shorter.
+    split = gb.attn_debug_plan(B, H, L, d, causal, SM, flags=gb.FLAG_SPLIT_KV)["makespan"] if d != 256 else -1
     if d > 128:
-        assert p["kind"] == 0
+        best = gb.attn_debug_plan(B, H, L, d, causal, SM, flags=gb.FLAG_SINGLE_TILE)["makespan"]
+        if 0 <= split < 0.9 * best:
+            assert (p["kind"], p["makespan"]) == (3, split)
+        else:
+            assert (p["kind"], p["makespan"]) == (0, best)
         return
     pair = gb.attn_debug_plan(B, H, L, d, causal, SM, flags=4)
     if pair["items"] >= 2 * SM:
@@ -60,7 +68,11 @@ def test_auto_plan(B, H, L, d, causal):
         return
     # Few blocks: the kernel with the shorter estimated schedule.
     alternatives = [gb.attn_debug_plan(B, H, L, d, causal, SM, flags=f)["makespan"] for f in (4, 2)]
-    assert p["makespan"] == min(m for m in alternatives if m >= 0)
+    best = min(m for m in alternatives if m >= 0)
+    if 0 <= split < 0.9 * best:
+        assert (p["kind"], p["makespan"]) == (3, split)
+    else:
+        assert p["makespan"] == best and p["kind"] in (0, 1)
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])
