@@ -108,8 +108,9 @@ def stored_traffic(workload: str, kernel: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling while the timed region runs."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle sampling (read-only queries, every 100 ms).  stop() keeps
+    only the samples whose timestamps fall inside a given host-clock window."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -130,7 +131,18 @@ class ClockSampler:
             self.proc = None
         time.sleep(0.25)
 
-    def stop(self):
+    @staticmethod
+    def _epoch(stamp: str):
+        """nvidia-smi's local-time stamp 'YYYY/MM/DD HH:MM:SS.mmm' as epoch seconds."""
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def stop(self, window=None):
+        """Stop sampling; with window = (t0, t1) (time.time() values) keep only the samples
+        taken inside it (a margin of half the sampling period on each side)."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         time.sleep(0.15)
@@ -139,15 +151,18 @@ class ClockSampler:
         rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 9:
+            if len(parts) >= 10:
                 rows.append(parts)
         os.unlink(self.path)
+        if window is not None:
+            t0, t1 = window
+            rows = [r for r in rows if (e := self._epoch(r[0])) is not None and t0 - 0.05 <= e <= t1 + 0.05]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
         loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
         return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(rows)}
@@ -174,6 +189,17 @@ def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def workload_config(w, world: int) -> dict:
+    """The `config` of the JSON line, identical in both arms: the workload, and how the
+    GPU arm keeps every step's inputs out of L2."""
+    R = n_rotating_sets(w)
+    return {"workload": w.name, "shape": w.describe(), "global_batch": w.B * world, "seq_len": w.L,
+            "head_dim": w.d, "heads": w.H, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": f"GPU arm: {R} rotating input/output sets ({R * w.bytes() / 2**20:.0f} MiB > 2x L2); no flush",
+            "timing": "GPU arm: CUDA graph of the steps, CUDA events on the replay stream; reference arm: "
+                      "host wall clock"}
 
 
 # ----------------------------------------------------------------------------- ours
@@ -233,6 +259,7 @@ def bench_workload(w, steps, warmup, device, torch, gb, inputs, world):
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
+    h0 = time.time()
     with torch.cuda.stream(stream):
         a.record(stream)
         for _ in range(n_main):
@@ -241,10 +268,11 @@ def bench_workload(w, steps, warmup, device, torch, gb, inputs, world):
             tail.replay()
         b.record(stream)
     b.synchronize()
+    h1 = time.time()
     torch.cuda.synchronize()
     barrier(world)
     t = a.elapsed_time(b) * 1e-3 / steps
-    return t, steps, R, host, sets, (main, stream, per)
+    return t, steps, R, host, sets, (main, stream, per, (h0, h1))
 
 
 def bench_e2e(w, steps, warmup, device, torch, gb, host):
@@ -446,6 +474,27 @@ def backward_only(name):
     print(json.dumps({"backward": res}), flush=True)
 
 
+def matmul_tflops(torch, dtype, n=8192, reps=10):
+    """Best of `reps` torch.matmul n x n x n products of `dtype` (2 n^3 FLOPs each), CUDA
+    events: the library GEMM rate in this run, for the fp16/bf16 ratio of the tensor peak."""
+    a = torch.randn(n, n, device="cuda", dtype=dtype)
+    b = torch.randn(n, n, device="cuda", dtype=dtype)
+    for _ in range(3):
+        torch.matmul(a, b)
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.matmul(a, b)
+        e1.record()
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1e-3)
+    del a, b
+    torch.cuda.empty_cache()
+    return 2.0 * n ** 3 / best / 1e12
+
+
 def cpu_oracle_baseline(w, min_seconds=10.0, max_reps=20):
     """Float64 oracle, as it stands, on the host cores: whole workload, repeated until
     about `min_seconds` of CPU work (bounded by max_reps)."""
@@ -500,21 +549,26 @@ def bench_ours(args):
     if sampler:
         sampler.start()
     t, nsteps, R, host, sets, graph = bench_workload(w, args.steps, args.warmup, device, torch, gb, inputs, world)
-    clock_note = "sampled during the timed region"
+    g_main, g_stream, per_graph, window = graph
     if sampler:
-        clocks = sampler.stop()
+        # Only the samples taken inside the timed region count.
+        clocks = sampler.stop(window)
+        span_ms = (window[1] - window[0]) * 1e3
+        clock_note = f"samples taken inside the timed region ({span_ms:.1f} ms)"
         if clocks.get("samples", 0) < 3:
-            # Timed region too short for 100 ms sampling: sample again over ~1.5 s of the
-            # same graph replays (untimed) and say so.
+            # The timed region is shorter than three sampling periods: sample over ~1.5 s
+            # of the same graph replays right after it (untimed) and say so.
             sampler.start()
-            g, stream, per_graph = graph
-            t_end = time.perf_counter() + 1.5
-            while time.perf_counter() < t_end:
-                for _ in range(20):
-                    g.replay()
-                torch.cuda.synchronize()
-            clocks = sampler.stop()
-            clock_note = "timed region shorter than the sampling period; sampled over 1.5 s of the same replays"
+            h0 = time.time()
+            with torch.cuda.stream(g_stream):
+                t_end = time.perf_counter() + 1.5
+                while time.perf_counter() < t_end:
+                    for _ in range(20):
+                        g_main.replay()
+                    torch.cuda.synchronize()
+            clocks = sampler.stop((h0, time.time()))
+            clock_note = (f"timed region {span_ms:.1f} ms, shorter than three 100 ms sampling periods; sampled "
+                          "over 1.5 s of the same graph replays right after it")
         clocks["note"] = clock_note
     else:
         clocks = None
@@ -549,11 +603,7 @@ def bench_ours(args):
         "warmup": args.warmup, "ms_per_step": round(t_max * 1e3, 6), "us_per_call": round(t_max * 1e6, 3),
         "pct_fp16_peak": round(100 * w.flops() / t_max / 1e12 / fp16_peak, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "accumulate": "f32", "data": "synthetic",
-        "config": {"workload": w.name, "shape": w.describe(), "global_batch": w.B * world,
-                   "seq_len": w.L, "head_dim": w.d, "heads": w.H,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"{R} rotating input/output sets ({R * w.bytes() / 2**20:.0f} MiB > 2x L2); no flush",
-                   "timing": "CUDA graph of the steps, CUDA events on the replay stream"},
+        "config": workload_config(w, world),
         "gpu_launches": nsteps, "roofline": roof, "clocks": clocks,
     }
     if not args.quick:
@@ -581,6 +631,13 @@ def bench_ours(args):
         line["per_config_timing"] = ("us: mean of 200 graph-replayed calls over rotating input sets; "
                                      "per_call_*: 300 single calls interleaved across the configs, CUDA events "
                                      "around each call behind a GPU-side sleep")
+        # fp16 and bf16 library GEMMs in this run: the roofline's peak is the measured bf16
+        # figure of MEASURED_PEAKS.json, taken for fp16 at the nominal ratio of 1; this
+        # records the measured ratio beside it.
+        f16 = matmul_tflops(torch, torch.float16)
+        b16 = matmul_tflops(torch, torch.bfloat16)
+        roof["matmul_8192_tflops_this_run"] = {"fp16": round(f16, 1), "bf16": round(b16, 1),
+                                               "fp16_over_bf16": round(f16 / b16, 4)}
         line["decode"] = bench_decode(device, torch, gb, inputs, hbm_peak)
         line["backward"] = bench_backward(device, torch, gb, inputs, fp16_peak)
         status = gb.attn_last_device_error()
@@ -639,8 +696,7 @@ def bench_reference(args):
     line = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOPS", "impl": "reference", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "shape": w.describe(), "global_batch": w.B, "seq_len": w.L,
-                       "head_dim": w.d, "parallelism": "host cores"},
+            "config": workload_config(w, world),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cores, "kind": "oracle",
                              "sample": f"{nh} of {heads} heads of {w.name} per step"},
             "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
