@@ -543,7 +543,8 @@ def bench_ours(args):
     torch.cuda.set_device(device)
     gb.load_library(gbuild.build())
     peaks, peak_kind = load_peaks()
-    w = WORKLOADS[args.workload]
+    from scaled_dot_product_sdpa_gb300.configs import EXTRA_WORKLOADS
+    w = WORKLOADS[args.workload] if args.workload in WORKLOADS else EXTRA_WORKLOADS[args.workload]
 
     sampler = ClockSampler(local) if not args.quick else None
     if sampler:

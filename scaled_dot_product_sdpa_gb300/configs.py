@@ -51,6 +51,14 @@ WORKLOADS = {
     "hd512": Workload("hd512", 1, 8, 2048, 512, True, 5, 0.5),
 }
 
+# Shapes beyond the five, for profiling the paths the five do not take: few heads of long
+# causal rows, where the planner splits the longest query tiles' key ranges over clusters
+# of two CTAs (split-KV).  bench.py --workload accepts these names; per_config times only
+# the five workloads above.
+EXTRA_WORKLOADS = {
+    "long4": Workload("long4", 1, 4, 4096, 128, True, 8),
+}
+
 
 @dataclass(frozen=True)
 class DecodeWorkload:
