@@ -12,6 +12,17 @@
 // and dealt to a persistent grid in a snake order; every CTA walks its own list, so no
 // scheduler state lives in global memory.
 //
+// Key-range split (SPLITKV, on clusters of two CTAs): a long query tile's key tiles are
+// shared by the two CTAs of a cluster, rank 0 taking the first ceil(n / 2) and rank 1 the
+// rest; each CTA runs its part like an item, then rank 1 hands its partial O (normalised,
+// fp16) and each row's (m, l) to rank 0 through shared memory, and rank 0 merges the two
+// with the log-sum-exp weights -- exact because the two key ranges are disjoint (STAGE_D.md,
+// section 2, "Merge").  Such split tiles come first in both CTAs' lists, in the same order.
+//
+// Head_dim split (DSPLIT, on clusters of two CTAs; an option at head_dim 512): each CTA
+// holds half of Q and of every K tile, the two exchange their partial S tiles, and each
+// produces half of the output columns.
+//
 // Warp roles (256 threads):
 //   warp 0      TMA producer: Q tile per item, then K / V tiles through an mbarrier ring in
 //               exactly the order the MMA issuer consumes them.
@@ -23,7 +34,9 @@
 //               lazy O rescale (only when the running max grows by more than 2^8), P as
 //               fp16 back into tensor memory (aliasing S) or into shared memory; then
 //               O / l -> fp16 -> swizzled staging tile -> TMA store, and LSE.
-//   warps 2,3   idle.
+//   warp 2      key-range split, rank 1: copies each split tile's partial to rank 0 and
+//               gives the staging Q buffer back once rank 0 has it; idle otherwise.
+//   warp 3      idle.
 //
 // Every wait is bounded (about two seconds of SM clock); a wait that runs out records a
 // status code, raises a CTA-wide abort flag, and the CTA drains its in-flight copies and
