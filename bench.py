@@ -71,16 +71,25 @@ KERNEL_SOURCES = {
 SHARED_SOURCES = ("ptx.cuh", "tmem_ldst.inc", "gbattn_abi.cu")
 
 
+def _code_only(text: str) -> str:
+    """C++ source without its comments and blank lines (comment edits leave a kernel's
+    compiled code, and so its stored ncu capture, unchanged)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(kind: str = "fwd") -> str:
-    """Hash of the sources a kernel family (fwd, decode, bwd) is built from, to tell
-    whether a stored ncu capture still describes the current kernel."""
+    """Hash of the code (comments left out) of the sources a kernel family (fwd, decode,
+    bwd) is built from, to tell whether a stored ncu capture still describes the current
+    kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "scaled_dot_product_sdpa_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.startswith(KERNEL_SOURCES[kind]) or name in SHARED_SOURCES:
-            with open(os.path.join(csrc, name), "rb") as f:
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
                 h.update(name.encode())
-                h.update(f.read())
+                h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
