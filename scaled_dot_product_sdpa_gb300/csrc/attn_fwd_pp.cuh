@@ -120,6 +120,12 @@ struct PPIssuer {
   uint32_t side_base = 0;
 
   __device__ uint32_t bar(int i) const { return bar_s + 8u * static_cast<uint32_t>(i); }
+  // A parity test is unambiguous only while the barrier is at most one phase behind: the
+  // K_0 stage's previous use (ring position side_base - NST) must have completed.  The
+  // issue order guarantees that for the kernel's own items (n1 - n0 <= 1: that position
+  // is K_{n1-2} of the current item, already consumed by QK1_{n1-2}); items whose slot 1
+  // needs three or more key tiles beyond slot 0's would break it (a host-side model of the
+  // issue order checks both).
   __device__ bool side_ready() const {
     return mbar_test(bar(C::B_QFULL + 0), side_il & 1) &&
            mbar_test(bar(C::B_FULL + side_base % C::NST), (side_base / C::NST) & 1u);
