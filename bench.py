@@ -322,7 +322,11 @@ def interleaved_per_call(workloads, reps, device, torch, gb, inputs):
     round calls every workload once, on its next rotating input set, so inputs come
     from HBM).  A GPU-side sleep before each timed call keeps the stream busy while the
     host enqueues the call, so the events bracket the kernel and not the host's launch
-    work.  Returns {name: (median, p10, p90) seconds}."""
+    work.  Two brackets with the same sleep are timed alongside: nothing between the
+    events ("events", what the bracket itself adds) and a one-thread torch kernel
+    ("launch", what any kernel launch adds on top).  Returns {name: (median, p10, p90,
+    mean of the middle 80%) seconds}, the two brackets under the names "_events" and
+    "_launch"."""
     prepared = {}
     for name, w in workloads.items():
         R = n_rotating_sets(w)
@@ -333,8 +337,20 @@ def interleaved_per_call(workloads, reps, device, torch, gb, inputs):
         s = sets[0]
         gb.attn_fwd(s[0], s[1], s[2], causal=w.causal, scale=w.scale, o=s[3], lse=s[4], stream=stream)
     torch.cuda.synchronize()
-    events = {name: [] for name in prepared}
+    events = {name: [] for name in list(prepared) + ["_events", "_launch"]}
+    one = torch.zeros(1, device=device)
+    one.add_(1.0)  # its kernel loaded before anything is timed
+    torch.cuda.synchronize()
     for r in range(reps):
+        for name in ("_events", "_launch"):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(200000)
+            a.record(stream)
+            if name == "_launch":
+                one.add_(1.0)
+            b.record(stream)
+            events[name].append((a, b))
         for name, (w, sets) in prepared.items():
             s = sets[r % len(sets)]
             a = torch.cuda.Event(enable_timing=True)
@@ -351,7 +367,8 @@ def interleaved_per_call(workloads, reps, device, torch, gb, inputs):
     for name, ev in events.items():
         ts = sorted(a.elapsed_time(b) * 1e-3 for a, b in ev)
         n = len(ts)
-        out[name] = (ts[n // 2], ts[max(0, n // 10)], ts[min(n - 1, (9 * n) // 10)])
+        mid = ts[n // 10:n - n // 10] or ts  # mean of the middle 80%: rare stalls left out
+        out[name] = (ts[n // 2], ts[max(0, n // 10)], ts[min(n - 1, (9 * n) // 10)], sum(mid) / len(mid))
     del prepared
     return out
 
@@ -634,13 +651,23 @@ def bench_ours(args):
                          "attainable_tflops": round(attain, 1), "pct_attainable": round(100 * fl / attain, 2)}
         # Per-call distribution, interleaved across the configs (300 rounds).
         dist_t = interleaved_per_call(WORKLOADS, 300, device, torch, gb, inputs)
-        for name, (med, p10, p90) in dist_t.items():
+        ev_floor = dist_t.pop("_events")
+        launch_floor = dist_t.pop("_launch")
+        for name, (med, p10, p90, mean) in dist_t.items():
             per[name].update({"per_call_us_median": round(med * 1e6, 3), "per_call_us_p10": round(p10 * 1e6, 3),
-                              "per_call_us_p90": round(p90 * 1e6, 3)})
+                              "per_call_us_p90": round(p90 * 1e6, 3), "per_call_us_mean": round(mean * 1e6, 3),
+                              "per_call_us_mean_net_of_events": round((mean - ev_floor[3]) * 1e6, 3)})
         line["per_config"] = per
+        line["per_call_floor_us"] = {"events_only": {"median": round(ev_floor[0] * 1e6, 3),
+                                                     "mean": round(ev_floor[3] * 1e6, 3)},
+                                     "one_thread_kernel": {"median": round(launch_floor[0] * 1e6, 3),
+                                                           "mean": round(launch_floor[3] * 1e6, 3)}}
         line["per_config_timing"] = ("us: mean of 200 graph-replayed calls over rotating input sets; "
                                      "per_call_*: 300 single calls interleaved across the configs, CUDA events "
-                                     "around each call behind a GPU-side sleep")
+                                     "around each call behind a GPU-side sleep; per_call_floor_us: the same "
+                                     "bracket around nothing and around a one-thread kernel; the event "
+                                     "timestamps come in steps of up to ~2 us, so medians are coarse and "
+                                     "the net figure uses means (of the middle 80% of the calls)")
         # fp16 and bf16 library GEMMs in this run: the roofline's peak is the measured bf16
         # figure of MEASURED_PEAKS.json, taken for fp16 at the nominal ratio of 1; this
         # records the measured ratio beside it.

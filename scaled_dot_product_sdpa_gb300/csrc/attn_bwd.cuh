@@ -818,13 +818,26 @@ __global__ void __launch_bounds__(384, 1)
       // Row statistics: D = dO . O, each warpgroup over its half of the row, the halves
       // added through shared memory; LSE log2(e).  Both go to the workspace.
       if (!(ok = wait_warp(C::QB_DOFULL, it & 1))) break;
+      // Every dO chunk is read before any product is formed: the shared-memory reads are
+      // ordered with the stores below, so reading them one row at a time would serialise
+      // the loop.
+      uint4 do_reg[CPH];
 #pragma unroll
       for (int i = 0; i < CPH; ++i) {
         const int q = i * 32 + lane, rw = quarter * 32 + q / CPH;
-        float part = bwd_dot8(ld_shared_v4(bwd_chunk_addr(do_s, C::RCHUNK, rw, CPH * h + q % CPH)), o_reg[i]);
+        do_reg[i] = ld_shared_v4(bwd_chunk_addr(do_s, C::RCHUNK, rw, CPH * h + q % CPH));
+      }
+      float part[CPH];
 #pragma unroll
-        for (int m = 1; m < CPH; m <<= 1) part += __shfl_xor_sync(0xffffffffu, part, m);
-        if (q % CPH == 0) dpart[h * 128 + rw] = qt * 128 + rw < p.L ? part : 0.f;
+      for (int i = 0; i < CPH; ++i) part[i] = bwd_dot8(do_reg[i], o_reg[i]);
+#pragma unroll
+      for (int m = 1; m < CPH; m <<= 1)
+#pragma unroll
+        for (int i = 0; i < CPH; ++i) part[i] += __shfl_xor_sync(0xffffffffu, part[i], m);
+#pragma unroll
+      for (int i = 0; i < CPH; ++i) {
+        const int q = i * 32 + lane, rw = quarter * 32 + q / CPH;
+        if (q % CPH == 0) dpart[h * 128 + rw] = qt * 128 + rw < p.L ? part[i] : 0.f;
       }
       const float lrow = o_valid ? lse_reg * kLog2e : INFINITY;
       mbar_arrive(BAR(C::QB_DPART));

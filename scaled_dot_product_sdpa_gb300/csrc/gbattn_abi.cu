@@ -228,7 +228,9 @@ double build_split(const SchedKey &k, SchedTable &t) {
 // Longest-processing-time-first: take items by decreasing cost, give each to the CTA with
 // the least accumulated cost (ties: lowest CTA).  Each CTA's list keeps assignment order.
 // Returns the largest accumulated cost (the estimated makespan), or -1 with t.n = 0
-// (the kernels' fixed snake order) when the items or CTAs do not fit the table.
+// (the kernels' fixed snake order) when the items or CTAs do not fit the table.  With at
+// most one item per CTA that snake order is the schedule itself: t.n = 0, and the
+// makespan is returned.
 double build_lpt(const SchedKey &k, SchedTable &t) {
   if (k.kind == kSplitKV) return build_split(k, t);
   std::memset(&t, 0, sizeof(t));
@@ -239,6 +241,11 @@ double build_lpt(const SchedKey &k, SchedTable &t) {
   for (int r = 0; r < n_items; ++r) order.push_back({item_cost(k, r), r});
   std::stable_sort(order.begin(), order.end(),
                    [](const std::pair<double, int> &a, const std::pair<double, int> &b) { return a.first > b.first; });
+  // At most one item per CTA (make_key then sets the grid to the item count): the order
+  // above, longest first, puts item c on CTA c, which is the kernels' own order, so no
+  // table is passed (t.n = 0) and the kernels take their item without reading one.
+  if (n_items <= k.grid && (k.kind == kSingle || k.kind == kPair))
+    return order.empty() ? 0.0 : order.front().first;
   using Slot = std::pair<double, int>;
   std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
   for (int c = 0; c < k.grid; ++c) heap.push({0.0, c});
