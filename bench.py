@@ -323,7 +323,7 @@ def interleaved_per_call(workloads, reps, device, torch, gb, inputs):
     from HBM).  A GPU-side sleep before each timed call keeps the stream busy while the
     host enqueues the call, so the events bracket the kernel and not the host's launch
     work.  Two brackets with the same sleep are timed alongside: nothing between the
-    events ("events", what the bracket itself adds) and a one-thread torch kernel
+    events ("events", what the bracket itself adds) and a torch kernel on one element
     ("launch", what any kernel launch adds on top).  Returns {name: (median, p10, p90,
     mean of the middle 80%) seconds}, the two brackets under the names "_events" and
     "_launch"."""
@@ -660,12 +660,12 @@ def bench_ours(args):
         line["per_config"] = per
         line["per_call_floor_us"] = {"events_only": {"median": round(ev_floor[0] * 1e6, 3),
                                                      "mean": round(ev_floor[3] * 1e6, 3)},
-                                     "one_thread_kernel": {"median": round(launch_floor[0] * 1e6, 3),
+                                     "one_element_kernel": {"median": round(launch_floor[0] * 1e6, 3),
                                                            "mean": round(launch_floor[3] * 1e6, 3)}}
         line["per_config_timing"] = ("us: mean of 200 graph-replayed calls over rotating input sets; "
                                      "per_call_*: 300 single calls interleaved across the configs, CUDA events "
                                      "around each call behind a GPU-side sleep; per_call_floor_us: the same "
-                                     "bracket around nothing and around a one-thread kernel; the event "
+                                     "bracket around nothing and around a torch kernel on one element; the event "
                                      "timestamps come in steps of up to ~2 us, so medians are coarse and "
                                      "the net figure uses means (of the middle 80% of the calls)")
         # fp16 and bf16 library GEMMs in this run: the roofline's peak is the measured bf16
