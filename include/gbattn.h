@@ -286,8 +286,10 @@ int attn_debug_wait_probe(long long limit_cycles, void *stream);
  * same order; the table then has one entry per CTA for each split tile.
  * Returns the number of entries n and fills
  * start[0..grid] (CTA c runs items[start[c] .. start[c+1]) in order) and items[0..n), or
- * returns 0 when the problem is too large for a table (the kernels then use a fixed
- * snake order), or a negative GBATTN_ERR_* code (GBATTN_ERR_DIMS if n > max_items).
+ * returns 0 when the kernels take no table and use their fixed snake order: the problem
+ * is too large for a table, or (single-tile and two-tile kernels) no CTA has more than one
+ * item, where that order is the schedule; or a negative GBATTN_ERR_* code
+ * (GBATTN_ERR_DIMS if n > max_items).
  * Host-only; needs no GPU.  Not thread-safe.
  */
 int attn_debug_schedule(int B, int H, int L, int d, int causal, int grid, int flags, int *start, int *items,
