@@ -105,8 +105,9 @@ struct FwdCfg {
   static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
   // barrier indices
   static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_FULL = 4, B_EMPTY = 4 + NST;
+  // ODONE[g & 1] completes when the PV of key tile g (counted across items) is done.
   static constexpr int B_SFULL = 4 + 2 * NST, B_PFULL = B_SFULL + NSB, B_ODONE = B_PFULL + NSB;
-  static constexpr int B_OFREE = B_ODONE + 1, B_EPI = B_OFREE + 1, B_DRAIN = B_EPI + 1;
+  static constexpr int B_OFREE = B_ODONE + 2, B_EPI = B_OFREE + 1, B_DRAIN = B_EPI + 1;
   // head_dim split: RECV completes when the peer's partial S is in this CTA's buffer,
   // RFREE when the peer has read this CTA's partial out of its own buffer
   static constexpr int B_RECV = B_DRAIN + 1, B_RFREE = B_RECV + 1;
@@ -392,6 +393,7 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(BAR(C::B_PFULL + i), 128);
     }
     mbar_init(BAR(C::B_ODONE), 1);
+    mbar_init(BAR(C::B_ODONE + 1), 1);
     mbar_init(BAR(C::B_OFREE), 128);
     mbar_init(BAR(C::B_EPI), 128);
     mbar_init(BAR(C::B_DRAIN), 1);
@@ -534,7 +536,7 @@ __global__ void __launch_bounds__(256, 1)
           umma_commit(BAR(C::B_EMPTY + s));
           ++it;
         }
-        umma_commit(BAR(C::B_ODONE));
+        umma_commit(BAR(C::B_ODONE + (v.g & 1u)));
         return true;
       };
       PvQueue<C::NSB> pq;
@@ -640,14 +642,15 @@ __global__ void __launch_bounds__(256, 1)
           mbar_arrive_cluster(mapa_shared(BAR(C::B_READY), 1u));
         }
         const int lim = CAUSAL ? (t == qt ? row + 1 : 128) : min(128, p.L - t * C::BN);
-        // ODONE completes once per PV, and every phase is waited for exactly once, in
-        // order: on tile t > t0, the phase of PV(t-1) -- just before a rescale of O (which
-        // must not race with it), else at the end of the tile, when that PV has long been
-        // done.  Either way PV(t-2) is complete (it was issued before this tile's QK) and
-        // PV(t) cannot be (it needs this tile's P), so the wait's parity is unambiguous.
-        // The softmax of tile t+1 therefore never waits for PV(t) on the common path.
+        // PV(g) completes a phase of ODONE[g & 1] (the (g >> 1)-th).  The softmax waits for
+        // PV(g - 1) only before rescaling O (which must not race with it) and for the item's
+        // last PV before its epilogue; it skips the phases in between.  A wait for PV(x) is
+        // never two phases behind its barrier: that barrier's next phase is PV(x + 2), which
+        // needs P of a tile this softmax has not formed yet (in the epilogue: the next
+        // item's second PV, which waits for this epilogue's OFREE).  The P stored over S(t)
+        // never races with PV(t - 2), which ran before QK(t) wrote S(t).
         auto wait_prev_pv = [&]() -> bool {
-          if (!wait_warp(BAR(C::B_ODONE), (g - 1) & 1u)) return false;
+          if (!wait_warp(BAR(C::B_ODONE + ((g - 1u) & 1u)), ((g - 1u) >> 1) & 1u)) return false;
           tc_fence_after();
           return true;
         };
@@ -715,14 +718,13 @@ __global__ void __launch_bounds__(256, 1)
           }
           fence_proxy_async_smem();
         }
-        if (t > t0 && !rescaled && !(ok = wait_prev_pv())) break;
         tc_fence_before();
         mbar_arrive(BAR(C::B_PFULL + sb));
         if (t == t0 && warp == 4 && lane == 0) release_pending();
       }
       if (!ok) break;
       // ------------------------------------------------------------- epilogue
-      if (!(ok = wait_warp(BAR(C::B_ODONE), (g - 1) & 1u))) break;
+      if (!(ok = wait_warp(BAR(C::B_ODONE + ((g - 1u) & 1u)), ((g - 1u) >> 1) & 1u))) break;
       tc_fence_after();
       const int qb = il % C::NQB;
       const uint32_t stage = q_s + qb * C::QBYTES;  // the item's Q tile is no longer read
