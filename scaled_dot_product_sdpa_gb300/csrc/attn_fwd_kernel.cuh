@@ -514,12 +514,17 @@ __global__ void __launch_bounds__(256, 1)
       auto issue_pv = [&](const PendingPv &v) -> bool {
         const uint32_t sb = v.g % C::NSB;
         const bool first = v.t == v.t0;
-        if (!wait(BAR(C::B_PFULL + sb), (v.g / C::NSB) & 1u)) return false;
-        if (first && v.il > 0 && !wait(BAR(C::B_OFREE), (v.il - 1) & 1)) return false;
+        // P, the first V stage and (on an item's first PV) the free O are tested together:
+        // their barrier probes' latencies overlap.
+        WaitSet ws;
+        ws.add(BAR(C::B_PFULL + sb), (v.g / C::NSB) & 1u);
+        ws.add(BAR(C::B_FULL + it % C::NST), (it / C::NST) & 1u);
+        if (first && v.il > 0) ws.add(BAR(C::B_OFREE), (v.il - 1) & 1);
+        if (!ws.wait(abort_flag, p.status, kDevTimeoutMma, LIM)) return false;
         tc_fence_after();
         for (int vs = 0; vs < C::VST; ++vs) {
           const uint32_t s = it % C::NST;
-          if (!wait(BAR(C::B_FULL + s), (it / C::NST) & 1u)) return false;
+          if (vs > 0 && !wait(BAR(C::B_FULL + s), (it / C::NST) & 1u)) return false;
           tc_fence_after();
           const uint32_t o_tmem = tmem + C::O_COL + vs * C::SC * 64;
           const SDesc b = sdesc_split(sdesc_sw128(ring_s + s * C::STAGE, C::CHUNK, 1024));
