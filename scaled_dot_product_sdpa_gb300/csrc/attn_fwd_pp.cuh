@@ -19,8 +19,8 @@
 //
 // Warp roles (384 threads):
 //   warp 0      K/V producer: per item, K_0, V_0, K_1, V_1, ... into an mbarrier ring; a
-//               stage is free again once both slots released it (the producer itself
-//               gives the release for tiles only Q1 uses).
+//               stage is free again once slot 1's QK or PV of it is done (slot 1 reads every
+//               K/V tile of an item, always after slot 0; one commit covers both).
 //   warp 1      TMEM owner + MMA issuer;  warp 2 idle.
 //   warp 3      Q loader and O store issuer.  Each slot has one Q buffer, released by the
 //               commit of the slot's last QK of an item, so the next item's Q tile lands
@@ -114,6 +114,9 @@ struct PPIssuer {
   volatile uint32_t *abort_flag;
   uint32_t base = 0;                // ring position of K_0 of the current item
   uint32_t n_pv0 = 0, n_pv1 = 0;    // PVs per slot so far (phases of the P barriers)
+  // The last ring position whose FULL phase this thread has seen complete: slot 1's QK and
+  // PV of a key tile follow slot 0's, and do not probe the same stage again.
+  uint32_t seen_full = ~0u, seen_v = ~0u;
   // The next item's slot-0 QK, while it waits for its Q and K tiles.
   bool side_pending = false, side_last = false;
   int side_il = 0;
@@ -144,7 +147,9 @@ struct PPIssuer {
         umma_ss_off(d_tmem, a, c * C::CHUNK + kk * 32, b, c * C::CHUNK + kk * 32, C::IDESC_QK,
                     (c | kk) != 0 ? 1u : 0u);
     umma_commit(bar(C::B_SFULL + slot));
-    umma_commit(bar(C::B_EMPTY + pos % C::NST));
+    // Slot 1's QK of a K tile comes after slot 0's (or slot 0 does not use it): its commit
+    // covers both and frees the stage.
+    if (slot == 1) umma_commit(bar(C::B_EMPTY + pos % C::NST));
     if (last) umma_commit(bar(C::B_QEMPTY + slot));
   }
   // Wait for every phase of ws.  While the next item's slot-0 QK is pending, the wait
@@ -157,6 +162,7 @@ struct PPIssuer {
         if (side_ready()) {
           tc_fence_after();
           qk_issue(0, side_base, side_last);
+          seen_full = side_base;
           side_pending = false;
           if (!ws.wait(abort_flag, p->status, kDevTimeoutMma, p->wait_limit)) return false;
           break;
@@ -180,8 +186,9 @@ struct PPIssuer {
     const uint32_t pos = item_base + 2u * static_cast<uint32_t>(j);
     WaitSet ws;
     if (j == 0) ws.add(bar(C::B_QFULL + slot), il & 1);
-    ws.add(bar(C::B_FULL + pos % C::NST), (pos / C::NST) & 1u);
-    if (!wait_all(ws)) return false;
+    if (pos != seen_full) ws.add(bar(C::B_FULL + pos % C::NST), (pos / C::NST) & 1u);
+    if (ws.n > 0 && !wait_all(ws)) return false;
+    seen_full = pos;
     qk_issue(slot, pos, last);
     return true;
   }
@@ -193,15 +200,17 @@ struct PPIssuer {
     WaitSet ws;
     ws.add(bar(C::B_PFULL + slot), np & 1u);
     if (j == 0 && il > 0) ws.add(bar(C::B_OFREE + slot), (il - 1) & 1);
-    ws.add(bar(C::B_FULL + pos % C::NST), (pos / C::NST) & 1u);
+    const bool v_seen = slot == 1 && pos == seen_v;
+    if (!v_seen) ws.add(bar(C::B_FULL + pos % C::NST), (pos / C::NST) & 1u);
     if (!wait_all(ws)) return false;
+    seen_v = pos;
     const SDesc b = sdesc_split(sdesc_sw128(ring_s + (pos % C::NST) * C::TILE, C::CHUNK, 1024));
     const uint32_t o_tmem = tmem + C::O_COL + static_cast<uint32_t>(slot) * D;
     const uint32_t p_tmem = tmem + static_cast<uint32_t>(slot) * 128u;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       umma_ts_off(o_tmem, p_tmem + kk * 8u, b, kk * 2048, C::IDESC_PV, (j == 0 && kk == 0) ? 0u : 1u);
-    umma_commit(bar(C::B_EMPTY + pos % C::NST));
+    if (slot == 1) umma_commit(bar(C::B_EMPTY + pos % C::NST));  // the V tile's last reader
     if (j == n_slot - 1) umma_commit(bar(C::B_OFINAL + slot));
     if (slot == 0)
       ++n_pv0;
@@ -283,7 +292,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(BAR(C::B_DRAIN), 1);
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(BAR(C::B_FULL + i), 1);
-      mbar_init(BAR(C::B_EMPTY + i), 2);  // one release per slot
+      mbar_init(BAR(C::B_EMPTY + i), 1);  // released by slot 1's use, the last
     }
     *abort_flag = 0u;
     fence_mbar_init();
@@ -332,7 +341,6 @@ __global__ void __launch_bounds__(384, 1)
             for (int c = 0; c < C::NCH; ++c)
               tma_load_3d_hint(ring_s + s * C::TILE + c * C::CHUNK, tm, c * 64, j * 128, item.bh, BAR(C::B_FULL + s),
                                pol_kv);
-            if (j >= item.n0) mbar_arrive(BAR(C::B_EMPTY + s));  // Q0 never uses this tile
           }
       }
       // Drain: every load issued must have landed before the CTA may exit.
