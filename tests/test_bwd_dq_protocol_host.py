@@ -2,11 +2,14 @@
 thread, the tensor pipe and the elementwise threads (attn_bwd.cuh, attn_bwd_dq_kernel).
 
 Per step s (global step g) of an item the tensor pipe runs S(g) = Q K^T into S buffer g&1,
-dP(g) = dO V^T into the dP columns and dQ += dS(g) K, reading dS(g) (fp16) from S buffer
-g&1; the elementwise threads read S(g) (for P), read dP(g), hand the dP columns back
-(DPREAD), write dS(g) over S(g) and signal DSFULL.  The MMA thread issues, per item,
-S(g), dP(g), S(g+1), then per step: dP(g+1) once DPREAD(g) is complete, dQ(g) once
-DSFULL(g) is, S(g+2) into the buffer dQ(g) has just read.
+dP(g) = dO V^T into the dP columns and dQ += dS(g) K.  The elementwise threads read S(g)
+(for P) and dP(g), write dS(g) (fp16) over dP(g) and signal DSFULL.  The MMA thread
+issues, per item, S(g), dP(g), S(g+1), then per step: dQ(g) once DSFULL(g) is complete,
+then dP(g+1) into the columns dQ(g) has just read, then S(g+2) into S buffer g&1.
+
+A variant that was measured and not kept writes dS(g) over S(g) instead, hands the dP
+columns back as soon as they are read (DPREAD), and issues dP(g+1) once DPREAD(g) is
+complete, before waiting for DSFULL(g).
 
 An mbarrier parity wait is only unambiguous while the barrier is at most one phase away
 from the waited phase: waiting for phase k, the barrier must have completed k or k+1
@@ -16,10 +19,12 @@ the three roles under randomly skewed schedules (the tensor pipe and each role s
 racing at random) and checks both rules at every scheduling step, plus every tensor-memory
 read and overwrite (a region is only overwritten once its content has been consumed).
 
-Because dP(g+1) is issued before the MMA thread waits for dS(g), the elementwise threads
-can finish dS(g+1) before that wait looks: with a single DSFULL barrier the wait would
-then be two phases behind.  The kernel uses one DSFULL barrier per step parity; the model
-shows that this holds, and that the single-barrier variant fails.
+In the kernel, dS(g+1) needs dP(g+1), which is issued only after the wait for dS(g), so
+one DSFULL barrier suffices.  In the variant dP(g+1) is issued before that wait, so the
+elementwise threads can finish dS(g+1) before the wait looks, and one barrier can then
+be two phases ahead of it.  The variant needs one DSFULL barrier per step parity.  The
+model shows that the kernel's protocol and the two-barrier variant hold, and that it
+finds the gap in the one-barrier variant.
 """
 import random
 
@@ -34,10 +39,14 @@ class Bar:
 
 
 class Model:
-    def __init__(self, items, nthreads, two_dsfull, rng):
+    """variant: "kernel" (the protocol above), "early_dp" (the variant, two DSFULL
+    barriers) or "early_dp_one_barrier"."""
+
+    def __init__(self, items, nthreads, variant, rng):
         self.items = items
         self.nt = nthreads
-        self.two = two_dsfull
+        self.early = variant != "kernel"
+        self.two = variant == "early_dp"
         self.rng = rng
         self.bars = {"SFULL0": Bar(1), "SFULL1": Bar(1), "DPFULL": Bar(1), "IDONE": Bar(1),
                      "DSFULL0": Bar(nthreads), "DSFULL1": Bar(nthreads), "DPREAD": Bar(nthreads)}
@@ -106,7 +115,7 @@ class Model:
         def issue_dq(gg, first):
             def run():
                 for t in range(self.nt):
-                    self.read(f"S{gg & 1}", t, ("dS", gg))
+                    self.read(f"S{gg & 1}" if self.early else "DP", t, ("dS", gg))
                     self.write("DQ", t, ("dQ", gg), None if first else ("dQ", gg - 1))
             self.pipe.append(("mma", run))
 
@@ -119,13 +128,16 @@ class Model:
                 issue_s(g + 1)
                 yield None
             for s in range(n):
-                if s + 1 < n:
+                if self.early and s + 1 < n:
                     yield ("wait", "DPREAD", g)
                     issue_dp(g + 1)
                     yield None
                 yield ("wait",) + self.ds_bar(g)
                 issue_dq(g, s == 0)
                 yield None
+                if not self.early and s + 1 < n:
+                    issue_dp(g + 1)
+                    yield None
                 if s + 2 < n:
                     issue_s(g + 2)
                     yield None
@@ -142,9 +154,10 @@ class Model:
                 yield None
                 yield ("wait", "DPFULL", g)
                 self.read("DP", t, ("dP", g))
-                self.arrive("DPREAD", g)
+                if self.early:
+                    self.arrive("DPREAD", g)
                 yield None
-                self.write(f"S{g & 1}", t, ("dS", g))
+                self.write(f"S{g & 1}" if self.early else "DP", t, ("dS", g))
                 self.arrive(*self.ds_bar(g))
                 yield None
                 g += 1
@@ -210,13 +223,13 @@ def dq_items(B, H, L, causal):
     return out
 
 
-def run_many(two_dsfull, seeds, nthreads=3):
+def run_many(variant, seeds, nthreads=3):
     bad = []
     for seed in seeds:
         rng = random.Random(seed)
         # one CTA's items: a mix of 1..4-step items as in an 8x32x512 causal launch
         items = [rng.choice([1, 2, 3, 4]) for _ in range(rng.randint(2, 7))]
-        m = Model(items, nthreads, two_dsfull, rng)
+        m = Model(items, nthreads, variant, rng)
         ok = m.run()
         if m.errors or not ok:
             bad.append((seed, items, m.errors[:3], ok))
@@ -229,21 +242,27 @@ def test_item_lists_match_the_kernel_decoding():
     assert sorted(set(dq_items(8, 32, 512, True))) == [1, 2, 3, 4]
 
 
-def test_protocol_with_two_dsfull_barriers_holds():
-    bad = run_many(True, range(300))
+def test_kernel_protocol_holds():
+    bad = run_many("kernel", range(300))
     assert not bad, bad[:2]
 
 
-def test_single_dsfull_barrier_is_caught():
-    # the variant whose wait can fall two phases behind: the model must find it
-    bad = run_many(False, range(300))
+def test_early_dp_variant_with_two_dsfull_barriers_holds():
+    bad = run_many("early_dp", range(300))
+    assert not bad, bad[:2]
+
+
+def test_early_dp_variant_with_one_dsfull_barrier_is_caught():
+    # the wait can fall two phases behind: the model must find it
+    bad = run_many("early_dp_one_barrier", range(300))
     assert bad, "the model did not find the two-phase gap of a single DSFULL barrier"
     assert any("DSFULL" in e for _, _, errs, _ in bad for e in errs)
 
 
+@pytest.mark.parametrize("variant", ["kernel", "early_dp"])
 @pytest.mark.parametrize("items", [[1], [4], [1, 1, 1], [4, 1, 4, 1], [2, 3, 1, 4, 2]])
-def test_every_role_finishes(items):
+def test_every_role_finishes(items, variant):
     for seed in range(20):
-        m = Model(items, 2, True, random.Random(seed))
+        m = Model(items, 2, variant, random.Random(seed))
         assert m.run(), (items, seed)
         assert not m.errors, m.errors[:3]
