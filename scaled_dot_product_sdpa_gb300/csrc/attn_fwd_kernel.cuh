@@ -415,6 +415,16 @@ __global__ void __launch_bounds__(256, 1)
   // Both CTAs of a pair have initialised their barriers before either arrives on the
   // other's (every thread reaches this, unconditionally).
   if constexpr (C::CLUSTER) cluster_sync_all();
+  // This CTA's first schedule entry, read while the previous kernel may still be running
+  // (the kernel parameters never depend on it), so that the loaders' first reads of the
+  // table after the wait below hit the constant cache.
+  if (warp == 2 && lane == 0 && tbl.n > 0) {
+    const int s0 = tbl.start[blockIdx.x];
+    if (s0 < tbl.start[blockIdx.x + 1]) {
+      const int i0 = tbl.items[s0];
+      asm volatile("" ::"r"(i0));
+    }
+  }
   // The prologue above touches no global memory: the next kernel may launch now, and this
   // one waits here for the previous kernel's writes (inputs may be its outputs).
   grid_launch_dependents();

@@ -309,6 +309,16 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // This CTA's first schedule entry, read while the previous kernel may still be running
+  // (the kernel parameters never depend on it), so that the loaders' first reads of the
+  // table after the wait below hit the constant cache.
+  if (warp == 2 && lane == 0 && tbl.n > 0) {
+    const int s0 = tbl.start[blockIdx.x];
+    if (s0 < tbl.start[blockIdx.x + 1]) {
+      const int i0 = tbl.items[s0];
+      asm volatile("" ::"r"(i0));
+    }
+  }
   // The prologue above touches no global memory: the next kernel may launch now, and this
   // one waits here for the previous kernel's writes (inputs may be its outputs).
   grid_launch_dependents();
