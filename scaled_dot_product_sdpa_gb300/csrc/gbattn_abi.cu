@@ -420,26 +420,43 @@ int check_shape(int B, int H, int L, int d) {
 }
 
 // Decode launch plan: the CTAs per head (one cluster, a power of two) and the keys each
-// one streams (whole key tiles).  Enough CTAs for two waves of two CTAs per SM, at most
-// max_ranks (and the head_dim's own bound), and at least one key tile per CTA.
+// one streams (whole key tiles).  The widest cluster that keeps the launch within one wave
+// of two CTAs per SM, at most max_ranks (and the head_dim's own bound), at least one key
+// tile per CTA, and one CTA per head when the heads alone fill that wave.  (Measured on
+// GB300 at L = 8192, same box, against the earlier rule of two such waves: 64 heads 54.0
+// -> 40.8 us, 128 heads 84.9 -> 77.3, 256 heads 158.9 -> 150.6 (at d = 64 83.8 -> 76.9),
+// 512 heads 312 -> 297; fewer, longer CTAs stream faster than more, shorter ones.)
 // When the widest cluster still leaves the SMs short of CTAs (few heads) and a workspace
-// is given, each head's keys are also split over `groups` clusters of at most 8 CTAs: as
-// many as one wave of two CTAs per SM holds, at least one key tile per CTA, at most
-// kDecMaxGroups.  (Measured on GB300, 1 x 8 heads x 1M keys at d = 128: clusters of 16 CTAs
-// 870 us, of 8 588 us, of 4 643 us; 1 x 1 x 1M: 107, 85, 115 us.)
+// is given, each head's keys are also split over `groups` clusters: clusters of two CTAs,
+// as many per head as one wave of two CTAs per SM holds, when that is at most
+// kDecMaxGroups and leaves every CTA a key tile; otherwise clusters of at most 8 CTAs, as
+// many as that wave holds, at most kDecMaxGroups.  Clusters of two fill the SMs' two CTA
+// slots evenly; wider ones leave some SMs with one CTA (and so half the keys of the rest)
+// and, past one wave, a tail.  (Measured on GB300 at d = 128, same box: 1 x 8 heads x 1M
+// keys 8 x 4 clusters of 8 CTAs 619-629 us, 2 x 19 of 2 584 us; 1 x 12 x 256K 315 -> 224
+// us; 1 x 16 x 256K 344 -> 296; 1 x 32 x 128K 299 -> 296; 1 x 6 x 512K at d = 64 151 ->
+// 117; 320 CTAs in clusters of 4 or 8, just past one wave, 800-830 us on the 1M shape.)
 void decode_plan(long long BH, int L, int d, int sm_count, int max_ranks, bool grouped, int &ranks, int &groups,
                  int &keys_per_rank) {
   max_ranks = std::min(max_ranks, dec_max_ranks_for(d));
   const int kt = dec_key_tile(d);
   const long long tiles = (static_cast<long long>(L) + kt - 1) / kt;
-  const long long want = (4LL * sm_count + BH - 1) / BH;
+  const long long want = std::max(1LL, 2LL * sm_count / BH);  // CTAs per head in that wave
   int r = 1;
-  while (r < want && 2 * r <= max_ranks && 2 * r <= tiles) r *= 2;
+  while (2 * r <= want && 2 * r <= max_ranks && 2 * r <= tiles) r *= 2;
   long long g = 1;
   if (grouped && r < want) {
-    r = std::min(r, kDecGroupedRanks);
-    g = std::max(1LL, 2LL * sm_count / (BH * r));
-    g = std::min({g, static_cast<long long>(kDecMaxGroups), std::max(1LL, tiles / r)});
+    // Clusters of two CTAs, as many per head as one wave of two CTAs per SM holds, when
+    // that fits the workspace's rows per head; otherwise wider clusters.
+    const long long g2 = 2LL * sm_count / (BH * 2);
+    if (g2 >= 2 && g2 <= kDecMaxGroups && tiles >= 2 * g2) {
+      r = 2;
+      g = g2;
+    } else {
+      r = std::min(r, kDecGroupedRanks);
+      g = std::max(1LL, 2LL * sm_count / (BH * r));
+      g = std::min({g, static_cast<long long>(kDecMaxGroups), std::max(1LL, tiles / r)});
+    }
   }
   ranks = r;
   groups = static_cast<int>(g);

@@ -124,6 +124,8 @@ def test_decode_workloads_full_size(name):
     (1, 1, 19457, 128),   # 32 clusters of 8 CTAs per head, the last ones without keys
     (1, 2, 40000, 128),   # several clusters per head, ragged last tile
     (1, 1, 70000, 256),   # head_dim 256: clusters of 8
+    (1, 12, 5000, 128),   # clusters of two CTAs, 12 per head, ragged last tile
+    (2, 3, 7000, 64),     # clusters of two CTAs, 25 per head, ragged last tile
 ])
 def test_decode_grouped_and_single_cluster_agree_with_oracle(B, H, L, d):
     """Few heads: with a workspace each head's keys are split over several clusters and the

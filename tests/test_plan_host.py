@@ -130,10 +130,16 @@ def test_decode_plan_fills_the_gpu():
     (up to one wave of two CTAs per SM); many heads stay at one CTA per head."""
     assert gb.attn_debug_decode_plan(1, 8, 1 << 20, 128, 152, 16)["ranks"] == 16
     assert gb.attn_debug_decode_plan(1, 8, 1 << 20, 128, 152, 8)["ranks"] == 8
-    assert gb.attn_debug_decode_plan(8, 32, 8192, 128, 152, 16)["ranks"] == 4
+    assert gb.attn_debug_decode_plan(8, 32, 8192, 128, 152, 16)["ranks"] == 1  # 256 heads fill the wave
+    assert gb.attn_debug_decode_plan(1, 64, 8192, 128, 152, 16)["ranks"] == 4  # 256 CTAs <= 304
+    assert gb.attn_debug_decode_plan(1, 128, 8192, 128, 152, 16)["ranks"] == 2
     assert gb.attn_debug_decode_plan(64, 64, 4096, 64, 152, 16)["ranks"] == 1
     p = gb.attn_debug_decode_plan(1, 8, 1 << 20, 128, 152, 16, grouped=True)
-    assert (p["ranks"], p["groups"]) == (8, 4)  # 8 heads x 4 clusters x 8 CTAs = 256 <= 304
+    assert (p["ranks"], p["groups"]) == (2, 19)  # 8 heads x 19 clusters x 2 CTAs = 304: two per SM
+    p = gb.attn_debug_decode_plan(1, 12, 1 << 18, 128, 152, 16, grouped=True)
+    assert (p["ranks"], p["groups"]) == (2, 12)
+    p = gb.attn_debug_decode_plan(1, 4, 1 << 20, 128, 152, 16, grouped=True)
+    assert (p["ranks"], p["groups"]) == (8, 9)  # clusters of two would need 38 per head
     p = gb.attn_debug_decode_plan(1, 1, 100000, 64, 152, 16, grouped=True)
     assert (p["ranks"], p["groups"]) == (8, 32)
     assert gb.attn_debug_decode_plan(8, 32, 8192, 128, 152, 16, grouped=True)["groups"] == 1
