@@ -1,7 +1,8 @@
 // Instantiations and launches of the backward kernels (attn_bwd.cuh): the dQ kernel, then
 // the dK/dV kernel, on the caller's stream, each a persistent grid of one CTA per SM
-// (programmatic dependent launch lets the second one's prologue overlap the first one's
-// tail; its loads wait until the first one has completed).
+// (programmatic dependent launch: a dK/dV CTA starts on an SM the dQ kernel has left and
+// loads its Q, K, V and dO tiles and runs its first products while the dQ kernel finishes;
+// only its loads of the row statistics wait until the dQ kernel has completed).
 #include "attn_bwd.cuh"
 
 namespace gbattn {

@@ -255,7 +255,12 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   grid_launch_dependents();
-  grid_wait_prior();
+  // The producer and the MMA thread start on Q, K, V and dO (which the dQ kernel does not
+  // write) before the dQ kernel has completed; the producer waits for it before its first
+  // load of the row statistics (which the dQ kernel writes), every other thread here.  The
+  // dQ kernel lets this one launch only after its own wait, so the kernels before both
+  // have completed by then.
+  if (warp >= 2) grid_wait_prior();
   // Tensor memory: S^T [0,128) (P^T packed into [0,32) and [64,96)), dP^T [128,256) (dS^T
   // likewise), dV [256, 256+D), dK [256+D, 256+2D).
   constexpr uint32_t C_S = 0, C_DP = 128, C_DV = 256, C_DK = 256 + D;
@@ -314,6 +319,7 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_3d(do_tile(g) + c * C::RCHUNK, &tm_do, c * 64, qi * 128, bh, BAR(C::KB_DOFULL + g % C::NDS));
           ++ndo;
           // The 128 rows' statistics, written by the dQ kernel (byte offsets multiples of 512).
+          if (nst == 0) grid_wait_prior();
           if (!(ok = wait_bounded(BAR(C::KB_STEMPTY + (g & 1)), ((g >> 1) & 1) ^ 1u, abort_flag, p.status,
                                   kDevTimeoutLoad, LIM)))
             break;
@@ -606,8 +612,10 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  grid_launch_dependents();
+  // Dependents launch only once the kernels before this one have completed (the dK/dV
+  // kernel reads its inputs before its own wait).
   grid_wait_prior();
+  grid_launch_dependents();
   // Tensor memory: S of step gg at [128 (gg & 1), +128), dP at [256, 384) (dS packed over
   // [256, 288) and [320, 352)), dQ at [384, 384 + D).
   constexpr uint32_t C_DP = 256, C_DQ = 384;
