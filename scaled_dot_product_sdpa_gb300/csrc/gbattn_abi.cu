@@ -117,6 +117,9 @@ enum Kind { kSingle = 0, kPair = 1, kDSplit = 2, kSplitKV = 3 };
 constexpr double kItemOverheadTwoSlot = 1.7;
 constexpr double kSingleStepCost = 1.2;
 constexpr double kItemOverheadSingle = 1.0;  // in single-tile steps
+// Without a mask every step is a full tile, and a single-tile step costs only about 1.06
+// units (non-causal, head_dim 64 and 128, measured on GB300: 1.05-1.07 on six shapes).
+constexpr double kSingleStepCostNonCausal = 1.06;
 // Key-range split: each part at least 4 key tiles (512 keys), and each part of a split
 // tile costs the handover and merge on top of its steps (in single-tile steps).
 constexpr int kSplitMinPart = 4;
@@ -358,6 +361,20 @@ int choose_plan(int BH, int L, int d, int causal, int sm_count, int flags, int g
     if (count_items(pair) > INT_MAX) return GBATTN_ERR_DIMS;
     if (count_items(pair) >= 2LL * grid) {
       kind = kPair;
+      if (!causal) {
+        // Non-causal items are all alike, so either kernel's makespan is its busiest
+        // CTA's whole items: ceil(items / grid) of them.  The two-tile kernel's items are
+        // half as many and twice as long, and when its count leaves the last round of
+        // items thinly spread the single-tile kernel's is the shorter (GB300, non-causal
+        // head_dim 64, 512 two-tile items: 4 x 16 x 2048 103.0 -> 97.1 us, 2 x 16 x 4096
+        // 197.3 -> 182.5).
+        const SchedKey single = make_key(kSingle, BH, L, d, causal, grid);
+        const double rp = std::ceil(static_cast<double>(count_items(pair)) / grid);
+        const double rs = std::ceil(static_cast<double>(count_items(single)) / grid);
+        const double mp = rp * (2.0 * pair.nQ + kItemOverheadTwoSlot);
+        const double ms = rs * kSingleStepCostNonCausal * (single.nQ + kItemOverheadSingle);
+        if (ms < mp) kind = kSingle;
+      }
     } else {
       double best = 0.0;
       kind = -1;

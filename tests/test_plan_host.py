@@ -152,3 +152,21 @@ def test_decode_plan_validation():
         gb.attn_debug_decode_plan(1, 1, 128, 64, 152, 32)
     with pytest.raises(gb.GbattnError):
         gb.attn_debug_decode_plan(1, 1, 0, 64, 152)
+
+
+@pytest.mark.parametrize("B,H,L,d,kind", [
+    # 512 two-tile items (3.4 per SM): the single-tile kernel's 1024 items spread more evenly
+    (4, 16, 2048, 64, 0), (2, 16, 4096, 64, 0), (4, 8, 4096, 64, 0), (2, 32, 2048, 64, 0),
+    # 1024 or 256 two-tile items: the two-tile kernel
+    (8, 16, 2048, 64, 1), (4, 16, 1024, 64, 1), (2, 16, 2048, 128, 1), (8, 16, 512, 128, 1),
+])
+def test_non_causal_plan_compares_whole_item_rounds(B, H, L, d, kind):
+    """Non-causal items are all alike, so with enough items for the two-tile kernel the
+    planner still compares the two kernels' busiest CTAs, in whole items (measured on
+    GB300: these choices were the faster kernel)."""
+    assert gb.attn_debug_plan(B, H, L, d, False, 152)["kind"] == kind
+
+
+def test_causal_plan_with_many_items_stays_two_tile():
+    for B, H, L, d in [(8, 32, 512, 128), (16, 16, 512, 128), (1, 32, 4096, 128), (8, 32, 512, 64)]:
+        assert gb.attn_debug_plan(B, H, L, d, True, 152)["kind"] == 1
