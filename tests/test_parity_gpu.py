@@ -167,6 +167,22 @@ def test_fwd_many_items_use_the_fixed_order():
         _check(o, lse, o_ref, lse_ref, f"many items flags={flags}")
 
 
+def test_fwd_non_causal_long_rows_plan_matches_oracle():
+    """Non-causal, head_dim 64, 63 heads of 2048 keys: 504 two-tile items (3.3 per SM), for
+    which the planner takes the single-tile kernel and its 1008 items in the schedule table.
+    The heads repeat a seeded block of 9 (copies), so the oracle runs on the block; every
+    head is compared."""
+    B, H, L, d, P = 1, 63, 2048, 64, 9
+    q9, k9, v9 = inputs.qkv(B, P, L, d, seed=91)
+    q, k, v = (t.repeat(1, H // P, 1, 1).contiguous() for t in (q9, k9, v9))
+    scale = 1.0 / math.sqrt(d)
+    o9, l9 = oracle.sdpa_fwd(q9, k9, v9, False, float(np.float32(scale)))
+    o_ref, lse_ref = np.tile(o9, (1, H // P, 1, 1)), np.tile(l9, (1, H // P, 1))
+    for flags in (0, 2):
+        o, lse = _run(*_dev(q, k, v), False, scale, flags=flags)
+        _check(o, lse, o_ref, lse_ref, f"63x2048x64 non-causal flags={flags}")
+
+
 # ------------------------------------------------------------------ the five workloads
 _ORACLE_CACHE = {}
 
