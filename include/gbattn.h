@@ -223,12 +223,15 @@ long long attn_bwd_noalloc_max_bytes(void);
  *               contents on entry do not matter.
  *   B, H, L : > 0.  d : 64, 128, 256 or 512.  scale : finite and > 0.
  * Ownership, stream, return values and errors as for attn_fwd.  Each head's keys are
- * split over the CTAs of one thread-block cluster (up to 16), which merge their partial
- * results in distributed shared memory.  With few heads (B * H below about ten) one
- * cluster per head cannot occupy every SM: given a workspace, each head's keys are then
- * also split over several clusters, each cluster writes its normalised partial (o, lse)
- * to the workspace, and a second small kernel merges them.  Without a workspace the
- * launch keeps one cluster per head.  The work is bound by the HBM reads of K and V.
+ * split over the CTAs of one thread-block cluster (a power of two, up to 16: the widest
+ * that keeps the launch within one wave of two CTAs per SM, so one CTA per head once the
+ * heads alone fill it), which merge their partial results in distributed shared memory.
+ * When no such cluster fills that wave (fewer than about 40 heads) and a workspace is
+ * given, each head's keys are instead split over several clusters (of two CTAs, or of up
+ * to 8 when a head would need more than 32 clusters), each cluster writes its normalised
+ * partial (o, lse) to the workspace, and a second small kernel merges them.  Without a
+ * workspace the launch keeps one cluster per head.  The work is bound by the HBM reads of
+ * K and V.
  */
 int attn_decode(const void *q, const void *k, const void *v, void *o, float *lse, void *workspace, int B, int H,
                 int L, int d, float scale, void *stream);
