@@ -104,12 +104,12 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
  *     saves.
  *   flags bit 4 (GBATTN_FLAG_SPLIT_KV): the single-tile kernel on clusters of two CTAs,
  *     where the longest query tiles are split into two disjoint key ranges, each at least
- *     4 key tiles (512 keys), one per CTA of a cluster; the second CTA hands its partial
+ *     3 key tiles (384 keys), one per CTA of a cluster; the second CTA hands its partial
  *     O (normalised, fp16) and each row's running maximum and sum to the first through
  *     shared memory (one bulk copy per 64 columns), and the first merges the two with the
  *     log-sum-exp weights (exact for disjoint key ranges: "An Optimal Mapper Meets a Real
  *     GPU", "Experiment one", and STAGE_D.md, section 2, "Merge") and writes O and LSE.
- *     Query tiles whose split would leave a part shorter than 4 key tiles are not split.
+ *     Query tiles whose split would leave a part shorter than 3 key tiles are not split.
  *     Only for d = 64, 128, 512 (else GBATTN_ERR_HEAD_DIM) and alone (else
  *     GBATTN_ERR_FLAGS); the launch uses an even number of CTAs (at least 2).
  *   grid_limit: 0 = one persistent CTA per SM; n > 0 = at most n CTAs (scheduler tests).

@@ -120,9 +120,11 @@ constexpr double kItemOverheadSingle = 1.0;  // in single-tile steps
 // Without a mask every step is a full tile, and a single-tile step costs only about 1.06
 // units (non-causal, head_dim 64 and 128, measured on GB300: 1.05-1.07 on six shapes).
 constexpr double kSingleStepCostNonCausal = 1.06;
-// Key-range split: each part at least 4 key tiles (512 keys), and each part of a split
+// Key-range split: each part at least 3 key tiles (384 keys: a coarse split, far from the
+// one-key splits that measured slowest; parts of 2 tiles made 512-key rows slower, parts of
+// at least 4 left 1 x 12 x 1024 x 64 causal 8% slower than 3 on GB300), and each part of a split
 // tile costs the handover and merge on top of its steps (in single-tile steps).
-constexpr int kSplitMinPart = 4;
+constexpr int kSplitMinPart = 3;
 constexpr double kSplitOverhead = 1.5;
 constexpr double kSplitGain = 0.9;  // taken only below this fraction of the other makespan
 

@@ -3,7 +3,7 @@
 The split schedule ("An Optimal Mapper Meets a Real GPU", "Experiment one": split the key
 reduction only coarsely; STAGE_D.md, section 2, "Merge": merging partial results is exact
 only over disjoint key sets): a query tile may be split in two disjoint key ranges, one per
-CTA of a cluster of two (CTAs 2c and 2c + 1), each range at least 4 key tiles (512 keys).
+CTA of a cluster of two (CTAs 2c and 2c + 1), each range at least 3 key tiles (384 keys).
 Every query tile must be computed exactly once: either as a plain item on one CTA, or as a
 split item listed by both CTAs of one cluster, at the head of both lists, in the same order.
 """
@@ -35,7 +35,7 @@ def _check(B, H, L, d, causal, grid):
         (c0, p0), (c1, p1) = where  # exactly two CTAs ...
         assert c0 % 2 == 0 and c1 == c0 + 1 and p0 == p1, f"split item {v} at {where}"  # ... of one cluster
         n = _tiles(B, H, L, d, causal, v - n_items)
-        assert n // 2 >= 4, f"split item with {n} key tiles: a part shorter than 4 tiles"
+        assert n // 2 >= 3, f"split item with {n} key tiles: a part shorter than 3 tiles"
     covered = sorted(plain + [v - n_items for v in split])
     assert covered == list(range(n_items)), "every query tile exactly once"
     return sched, split
@@ -67,10 +67,10 @@ def test_split_schedule_splits_the_long_tiles_of_an_underfilled_grid():
 
 
 def test_split_schedule_never_splits_short_tiles():
-    """Tiles of fewer than 8 key tiles are never split (each part at least 512 keys)."""
+    """Tiles of fewer than 6 key tiles are never split (each part at least 384 keys)."""
     sched, split = _check(1, 16, 512, 64, True, 152)
     assert not split
-    sched, split = _check(1, 8, 896, 128, True, 152)  # 7 key tiles at most
+    sched, split = _check(1, 8, 640, 128, True, 152)  # 5 key tiles at most
     assert not split
 
 
